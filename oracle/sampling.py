@@ -1,0 +1,303 @@
+"""Modified rejection sampling for a batch of ragged sequences, in float64.
+
+TEST INFRASTRUCTURE ONLY: part of the CPU oracle.  Only tests, the smoke check
+and the bench's CPU-baseline leg may import it.
+
+Method source: "Accelerating Large Language Model Decoding with Speculative
+Sampling" (Chen et al.; called SpS below):
+  * section "Modified rejection sampling" (改进的拒绝采样): accept draft x~ with
+    probability min(1, q(x~)/p(x~)); go left to right and stop at the first
+    rejection; on rejection resample from (q - p)_+ = max(0, q-p)/sum max(0, q-p);
+    if every draft is accepted, sample one more token from the last target row
+    (at least one and at most K+1 tokens per loop);
+  * same section, "compatibility with standard sampling methods": temperature /
+    nucleus / top-k change the probabilities *before* the rejection scheme;
+  * appendix "Proof", Theorem 1: the scheme recovers q exactly.
+Batch shape (ragged draft counts, no padding): "EMS-SD: Efficient Multi-sample
+Speculative Decoding" abstract; "BASS: Batched Attention-optimized Speculative
+Sampling" abstract.
+
+Readings where the pages are silent (each one is listed in the design notes):
+  * the compare is `u * p_hat(x~) < q_hat(x~)` with u in [0,1): for p_hat > 0
+    this is u < min(1, q/p) with no division, p == q always accepts, and for
+    p_hat == 0 the draft is accepted iff q_hat > 0;
+  * temperature first (z = logit / T), then nucleus on the tempered softmax;
+    the nucleus keeps {x : z_x >= tau}, tau the largest attained value whose
+    upper set holds mass >= top_p (tie-inclusive, no index tie-break);
+  * the same processing is applied to q and p;
+  * the inverse-CDF draw walks the vocabulary in index order and takes the first
+    x whose cumulative weight exceeds u * Z (strict, so zero weights are never
+    chosen); if a rejection leaves Z == 0 the draw falls back to q_hat and the
+    EMPTY_RESIDUAL status bit is set;
+  * a draft token outside [0, V) is a rejection with the BAD_TOKEN bit;
+  * a row holding NaN or +inf, or only -inf, makes its sequence fail: no token,
+    no append, NONFINITE bit.
+"""
+import numpy as np
+
+from .philox import verify_uniforms
+
+# Device-status bits (same meaning as the C-ABI's bits; values restated here).
+DEV_CAPACITY = 1
+DEV_BAD_TOKEN = 2
+DEV_NONFINITE = 4
+DEV_EMPTY_RESIDUAL = 8
+DEV_BAD_LENGTH = 16
+
+# Near-tie audit windows.  Decisions this close to a boundary may legitimately
+# differ between an fp32 GPU path and this fp64 oracle; they are counted and
+# excluded from bit-exact comparison (with everything after them in that
+# sequence).  RESIDUAL_MASS_MIN: below it the residual is a difference of nearly
+# equal probabilities whose normalized CDF fp32 cannot resolve to TIE_EPS.
+TIE_EPS = 1e-5
+RESIDUAL_MASS_MIN = 1e-2
+TIE_ACCEPT = 1
+TIE_DRAW = 2
+
+
+# --------------------------------------------------------------------------
+# exact conversions of the stored inputs
+# --------------------------------------------------------------------------
+def bf16_bits_to_f64(bits):
+    """bfloat16 bit patterns (uint16) -> float64, exactly."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def to_f64(x):
+    """Stored tensor (float32 array, or uint16 bfloat16 bits) -> float64 exactly."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return bf16_bits_to_f64(x)
+    return x.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# probability processing (SpS, "compatibility with standard sampling methods")
+# --------------------------------------------------------------------------
+class ProcessedRow:
+    """One processed logits row.
+
+    probs:   float64 [V], the processed distribution (0 outside the nucleus)
+    valid:   False if the row held NaN/+inf or only -inf
+    tau:     nucleus threshold on z (-inf when top_p >= 1)
+    margin:  distance of the nucleus boundary masses from top_p (inf if none)
+    """
+    __slots__ = ("probs", "valid", "tau", "margin")
+
+    def __init__(self, probs, valid, tau, margin):
+        self.probs, self.valid, self.tau, self.margin = probs, valid, tau, margin
+
+
+def process_row(logits, temperature, top_p):
+    """Temperature then nucleus, on one row of exact float64 logits.
+
+    temperature and top_p are taken as the float32 values the C-ABI receives.
+    """
+    T = float(np.float32(temperature))
+    tp = float(np.float32(top_p))
+    l = np.asarray(logits, dtype=np.float64)
+    V = l.shape[0]
+    if np.any(np.isnan(l)) or np.any(l == np.inf) or not np.any(l > -np.inf):
+        return ProcessedRow(np.zeros(V), False, np.nan, np.inf)
+    z = l / T
+    w = np.exp(z - z.max())              # exp(-inf) = 0 for masked entries
+    if tp >= 1.0:
+        return ProcessedRow(w / w.sum(), True, -np.inf, np.inf)
+    P = w / w.sum()
+    # Tie classes of equal z, highest first; upper-set masses M_k.
+    vals, inv = np.unique(z, return_inverse=True)
+    cls_mass = np.bincount(inv.ravel(), weights=P, minlength=vals.shape[0])
+    vals, cls_mass = vals[::-1], cls_mass[::-1]
+    M = np.cumsum(cls_mass)
+    k = int(np.argmax(M >= tp)) if np.any(M >= tp) else vals.shape[0] - 1
+    tau = vals[k]
+    above = M[k] - tp
+    below = tp - (M[k - 1] if k > 0 else 0.0)
+    keep = z >= tau
+    wk = np.where(keep, w, 0.0)
+    return ProcessedRow(wk / wk.sum(), True, tau, min(abs(above), abs(below)))
+
+
+# --------------------------------------------------------------------------
+# the three primitive decisions (SpS, "Modified rejection sampling")
+# --------------------------------------------------------------------------
+def accept(u_acc, p_of_draft, q_of_draft):
+    """Accept the draft iff u * p(x~) < q(x~), i.e. with prob. min(1, q/p)."""
+    return u_acc * p_of_draft < q_of_draft
+
+
+def residual(q_row, p_row):
+    """Unnormalized residual max(0, q - p) over the vocabulary."""
+    return np.maximum(0, q_row - p_row)
+
+
+def sample_index(weights, u):
+    """Inverse CDF in index order: first x with sum_{y<=x} w_y > u * Z.
+
+    Works on float64 arrays and on object arrays of Fractions; `u` may be an
+    array (vectorized draw).  Returns None when Z <= 0.
+    """
+    c = np.cumsum(weights)               # sequential, left to right
+    Z = c[-1]
+    if not Z > 0:
+        return None
+    idx = np.searchsorted(c, u * Z, side="right")
+    return idx if np.ndim(idx) else int(idx)
+
+
+def _cdf_margin(weights, x, u):
+    """Distance of u from the two ends of x's CDF interval, Z, and the nearest
+    indices on either side of x that carry weight (None at the ends)."""
+    c = np.cumsum(weights)
+    Z = c[-1]
+    hi = c[x] / Z
+    lo = c[x - 1] / Z if x > 0 else 0.0
+    nz = np.flatnonzero(np.asarray(weights, dtype=np.float64) > 0)
+    k = int(np.searchsorted(nz, x))
+    prev_x = int(nz[k - 1]) if k > 0 else None
+    next_x = int(nz[k + 1]) if k + 1 < nz.shape[0] else None
+    return min(u - lo, hi - u), Z, (prev_x, next_x)
+
+
+# --------------------------------------------------------------------------
+# one sequence
+# --------------------------------------------------------------------------
+def verify_sequence(q_rows, p_rows, drafts, u_acc, u_smp, audit=None):
+    """Left-to-right accept loop, then residual or bonus draw.
+
+    q_rows: [K+1, V] processed target rows; p_rows: [K, V] processed draft rows;
+    drafts: [K] tokens; u_acc, u_smp: [K+1] uniforms for rows 0..K.
+    Returns (n_accepted, sampled_token, status_bits).  If `audit` is a list, one
+    (row, kind, margin, neighbours) tuple is appended per decision taken; kind
+    is "accept", "residual", "bonus" or "empty", neighbours (draws only) the
+    nearest weighted indices on either side of the drawn token, or None when a
+    draw within the tie window could land anywhere.
+    """
+    K = len(drafts)
+    V = q_rows.shape[1] if hasattr(q_rows, "shape") else len(q_rows[0])
+    status = 0
+    for j in range(K):
+        d = int(drafts[j])
+        if d < 0 or d >= V:
+            status |= DEV_BAD_TOKEN
+            if audit is not None:
+                audit.append((j, "accept", np.inf, None))
+            break
+        pd, qd = p_rows[j][d], q_rows[j][d]
+        ok = accept(u_acc[j], pd, qd)
+        if audit is not None:
+            if pd > 0:
+                ratio = min(1.0, float(qd) / float(pd))
+                audit.append((j, "accept", abs(float(u_acc[j]) - ratio), None))
+            else:
+                audit.append((j, "accept", np.inf, None))
+        if not ok:
+            break
+    else:
+        j = K
+    n = j
+    kind = "bonus"
+    if n < K:
+        kind = "residual"
+        w = residual(q_rows[n], p_rows[n])
+        x = sample_index(w, u_smp[n])
+        if x is None:                      # rejected, yet no positive residual
+            status |= DEV_EMPTY_RESIDUAL
+            kind = "empty"
+            w = q_rows[n]
+            x = sample_index(w, u_smp[n])
+    else:
+        w = q_rows[K]
+        x = sample_index(w, u_smp[K])
+    if audit is not None:
+        m, Z, nb = _cdf_margin(w, x, float(u_smp[n]))
+        if kind == "empty" or (kind == "residual" and not float(Z) >= RESIDUAL_MASS_MIN):
+            m, nb = 0.0, None
+        audit.append((n, kind, m, nb))
+    return n, x, status
+
+
+# --------------------------------------------------------------------------
+# the batch
+# --------------------------------------------------------------------------
+def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
+                  temperature, top_p, seed, seq_ids=None):
+    """Batched verify sampling over ragged sequences (no padding).
+
+    target_logits [R, V], draft_logits [R-B, V] (stored float32 or bf16 bits);
+    rows of sequence i: target cu_q[i] + j (j = 0..K_i), draft cu_q[i] - i + j
+    (j = 0..K_i-1); draft_tokens [R-B] indexed like the draft rows.
+    Row j decides token index pos = kv_len[i] + j + 1 with Philox uniforms
+    keyed by (seed, seq_id, pos).
+
+    Returns dict with num_accepted [B] (-1 for a failed sequence), out_tokens
+    [R] (drafts for j < n_i, the sampled token at j = n_i, -1 after; all -1 for
+    a failed sequence), status (OR of bits), seq_status [B], and the near-tie
+    audit:
+      tie_row [B]   row of the first decision inside a tie window, or -1;
+      tie_kind [B]  0 none, TIE_ACCEPT (an accept/reject decision: rows before
+                    tie_row are still exact), TIE_DRAW (the final draw: n_i, the
+                    accepted drafts and the append are still exact);
+      tie_alts      {i: set of tokens a draw tie may also yield} (missing: any);
+      tie_count     number of sequences with a tie.
+    A decision is inside a tie window when |u - min(1, q/p)| < TIE_EPS, when
+    the draw's normalized CDF interval has an end within TIE_EPS of u, when a
+    residual's mass is below RESIDUAL_MASS_MIN, or when a row it uses has a
+    nucleus boundary mass within TIE_EPS of top_p.
+    """
+    cu_q = np.asarray(cu_q, dtype=np.int64)
+    B = cu_q.shape[0] - 1
+    R = int(cu_q[-1])
+    kv_len = np.asarray(kv_len, dtype=np.int64)
+    if seq_ids is None:
+        seq_ids = np.arange(B, dtype=np.int64)
+    num_acc = np.zeros(B, dtype=np.int32)
+    out_tokens = np.full(R, -1, dtype=np.int32)
+    seq_status = np.zeros(B, dtype=np.uint32)
+    tie_row = np.full(B, -1, dtype=np.int64)
+    tie_kind = np.zeros(B, dtype=np.int64)
+    tie_alts = {}
+    tie_count = 0
+    for i in range(B):
+        r0, r1 = int(cu_q[i]), int(cu_q[i + 1])
+        K = r1 - r0 - 1
+        p0 = r0 - i
+        pos = kv_len[i] + np.arange(K + 1, dtype=np.int64) + 1
+        u_acc, u_smp = verify_uniforms(seed, seq_ids[i], pos)
+        qp = [process_row(to_f64(target_logits[r0 + j]), temperature, top_p)
+              for j in range(K + 1)]
+        pp = [process_row(to_f64(draft_logits[p0 + j]), temperature, top_p)
+              for j in range(K)]
+        if not all(r.valid for r in qp + pp):
+            seq_status[i] = DEV_NONFINITE
+            num_acc[i] = -1
+            continue
+        audit = []
+        n, x, st = verify_sequence(np.stack([r.probs for r in qp]),
+                                   np.stack([r.probs for r in pp]) if K else
+                                   np.zeros((0, qp[0].probs.shape[0])),
+                                   draft_tokens[p0:p0 + K], u_acc, u_smp, audit)
+        seq_status[i] = st
+        num_acc[i] = n
+        out_tokens[r0:r0 + n] = draft_tokens[p0:p0 + n]
+        out_tokens[r0 + n] = x
+        # first decision inside a tie window (including nucleus boundaries of
+        # the rows that decision used)
+        for (j, kind, m, nb) in audit:
+            nuc = qp[j].margin if kind == "bonus" else min(
+                qp[j].margin, pp[j].margin if j < K else np.inf)
+            if m < TIE_EPS or nuc < TIE_EPS:
+                tie_row[i] = j
+                tie_count += 1
+                if kind == "accept" or nuc < TIE_EPS:
+                    tie_kind[i] = TIE_ACCEPT
+                else:
+                    tie_kind[i] = TIE_DRAW
+                    if nb is not None:
+                        tie_alts[i] = {x} | {t for t in nb if t is not None}
+                break
+    status = int(np.bitwise_or.reduce(seq_status)) if B else 0
+    return dict(num_accepted=num_acc, out_tokens=out_tokens, status=status,
+                seq_status=seq_status, tie_row=tie_row, tie_kind=tie_kind,
+                tie_alts=tie_alts, tie_count=tie_count)

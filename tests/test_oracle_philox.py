@@ -1,0 +1,106 @@
+"""Pins of the oracle's Philox4x32-10 (Salmon et al., SC'11, section "Philox").
+
+Absolute known-answer vectors are not available offline, so these pin the
+published constants and round structure through an independently written
+inverse, plus the statistical properties the rejection sampler relies on.
+"""
+import numpy as np
+import pytest
+from scipy import stats
+
+from oracle.philox import philox4x32, verify_uniforms, word_to_uniform
+
+M32 = (1 << 32) - 1
+# Constants as printed in the SC'11 paper's Philox4x32 definition.
+PAPER_M = (0xD2511F53, 0xCD9E8D57)
+PAPER_W = (0x9E3779B9, 0xBB67AE85)
+
+
+def _inverse(y, key, rounds=10):
+    """Invert Philox4x32 on python ints: the round is a bijection because the
+    multipliers are odd, so the low product halves invert by modular inverse."""
+    y0, y1, y2, y3 = y
+    keys = [((key[0] + r * PAPER_W[0]) & M32, (key[1] + r * PAPER_W[1]) & M32)
+            for r in range(rounds)]
+    inv0 = pow(PAPER_M[0], -1, 1 << 32)
+    inv1 = pow(PAPER_M[1], -1, 1 << 32)
+    for k0, k1 in reversed(keys):
+        c0 = (y3 * inv0) & M32
+        c2 = (y1 * inv1) & M32
+        hi0 = (PAPER_M[0] * c0) >> 32
+        hi1 = (PAPER_M[1] * c2) >> 32
+        c3 = y2 ^ hi0 ^ k1
+        c1 = y0 ^ hi1 ^ k0
+        y0, y1, y2, y3 = c0, c1, c2, c3
+    return y0, y1, y2, y3
+
+
+def test_inverse_recovers_counter():
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        c = [int(x) for x in rng.integers(0, 1 << 32, size=4, dtype=np.uint64)]
+        k = [int(x) for x in rng.integers(0, 1 << 32, size=2, dtype=np.uint64)]
+        y = [int(v) for v in philox4x32(*c, *k)]
+        assert _inverse(y, k) == tuple(c)
+
+
+def test_vectorized_matches_scalar_calls():
+    c0 = np.arange(1000, dtype=np.uint64)
+    vec = philox4x32(c0, 7, 9, 1, 123, 456)
+    for n in (0, 1, 999):
+        sc = philox4x32(n, 7, 9, 1, 123, 456)
+        assert all(int(vec[w][n]) == int(sc[w]) for w in range(4))
+
+
+def test_avalanche_single_bit_flip():
+    rng = np.random.default_rng(5)
+    flips = []
+    for _ in range(300):
+        c = [int(x) for x in rng.integers(0, 1 << 32, size=4, dtype=np.uint64)]
+        bit = int(rng.integers(0, 128))
+        c2 = list(c)
+        c2[bit // 32] ^= 1 << (bit % 32)
+        a = philox4x32(*c, 1, 2)
+        b = philox4x32(*c2, 1, 2)
+        flips.append(sum(bin(int(x) ^ int(y)).count("1") for x, y in zip(a, b)))
+    # 128 output bits, each flipping with prob. 1/2
+    assert abs(np.mean(flips) - 64) < 1.5
+
+
+def test_uniform_is_24_bit_and_in_range():
+    w = np.array([0, 255, 256, M32], dtype=np.uint64)
+    u = word_to_uniform(w)
+    assert list(u) == [0.0, 0.0, 2.0 ** -24, 1.0 - 2.0 ** -24]
+    ua, us = verify_uniforms(3, 17, np.arange(1, 5000))
+    assert np.all((ua >= 0) & (ua < 1) & (us >= 0) & (us < 1))
+    assert np.all(np.floor(ua * 2 ** 24) == ua * 2 ** 24)
+
+
+def test_uniformity_chi_square():
+    ua, us = verify_uniforms(0, 0, np.arange(1 << 20))
+    for u in (ua, us):
+        h = np.bincount((u * 1024).astype(np.int64), minlength=1024)
+        assert stats.chisquare(h).pvalue > 1e-3
+
+
+def test_pair_independence_chi_square():
+    ua, us = verify_uniforms(99, 5, np.arange(1 << 19))
+    cells = (ua * 32).astype(np.int64) * 32 + (us * 32).astype(np.int64)
+    h = np.bincount(cells, minlength=1024)
+    assert stats.chisquare(h).pvalue > 1e-3
+    assert abs(np.corrcoef(ua, us)[0, 1]) < 5 / np.sqrt(ua.size)
+
+
+@pytest.mark.parametrize("which", ["seed", "seq", "stream", "pos"])
+def test_key_and_counter_fields_all_matter(which):
+    pos = np.arange(1, 4097)
+    base = verify_uniforms(1, 2, pos)[0]
+    if which == "seed":
+        other = verify_uniforms(1 + (1 << 32), 2, pos)[0]      # high key word
+    elif which == "seq":
+        other = verify_uniforms(1, 2 + (1 << 32), pos)[0]      # high seq word
+    elif which == "stream":
+        other = verify_uniforms(1, 2, pos, stream=1)[0]
+    else:
+        other = verify_uniforms(1, 2, pos + 1)[0]
+    assert np.mean(base == other) < 0.01
