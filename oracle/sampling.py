@@ -51,6 +51,10 @@ DEV_BAD_LENGTH = 16
 # equal probabilities whose normalized CDF fp32 cannot resolve to TIE_EPS.
 TIE_EPS = 1e-5
 RESIDUAL_MASS_MIN = 1e-2
+# Nucleus cut window: the cut compares a mass with top_p; an fp32 path with
+# fp64 cross-thread sums gets that mass to ~5e-7, so boundaries within 2e-6 of
+# top_p are treated as ties (the 1e-5 windows above are for u comparisons).
+NUCLEUS_TIE_EPS = 2e-6
 TIE_ACCEPT = 1
 TIE_DRAW = 2
 
@@ -244,7 +248,7 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
     A decision is inside a tie window when |u - min(1, q/p)| < TIE_EPS, when
     the draw's normalized CDF interval has an end within TIE_EPS of u, when a
     residual's mass is below RESIDUAL_MASS_MIN, or when a row it uses has a
-    nucleus boundary mass within TIE_EPS of top_p.
+    nucleus boundary mass within NUCLEUS_TIE_EPS of top_p.
     """
     cu_q = np.asarray(cu_q, dtype=np.int64)
     B = cu_q.shape[0] - 1
@@ -287,10 +291,10 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
         for (j, kind, m, nb) in audit:
             nuc = qp[j].margin if kind == "bonus" else min(
                 qp[j].margin, pp[j].margin if j < K else np.inf)
-            if m < TIE_EPS or nuc < TIE_EPS:
+            if m < TIE_EPS or nuc < NUCLEUS_TIE_EPS:
                 tie_row[i] = j
                 tie_count += 1
-                if kind == "accept" or nuc < TIE_EPS:
+                if kind == "accept" or nuc < NUCLEUS_TIE_EPS:
                     tie_kind[i] = TIE_ACCEPT
                 else:
                     tie_kind[i] = TIE_DRAW
