@@ -1,0 +1,198 @@
+/*
+ * spec_verify.h -- C ABI of the batched speculative-decoding verify step
+ * (sm_103a).
+ *
+ * One verify step, for B sequences with their own KV lengths L_i and their own
+ * draft counts K_i (no padding anywhere), does three things:
+ *   1. verify attention: every query head of the K_i + 1 block rows of
+ *      sequence i attends over that sequence's KV cache plus the block itself,
+ *      causally inside the block ("Accelerating Large Language Model Decoding
+ *      with Speculative Sampling", section "Conditional scoring"; batch without
+ *      padding: BASS and EMS-SD abstracts); optionally over a prefill KV block
+ *      shared by a group of sequences (bifurcated attention abstract);
+ *   2. modified rejection sampling over the vocabulary (same SpS paper,
+ *      section "Modified rejection sampling"): temperature and nucleus applied
+ *      to both q and p first, accept draft x~ while u < min(1, q(x~)/p(x~)),
+ *      on the first rejection draw from max(0, q - p) normalized, after K_i
+ *      acceptances draw a bonus token from the last target row;
+ *   3. append of the accepted rows' K/V only (EMS-SD abstract), giving every
+ *      sequence its own new length.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked [dev] are device pointers, [host] are host pointers.
+ *     Every buffer is owned by the caller; the library keeps no pointer after
+ *     a call returns and allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and never synchronize.
+ *   - Row bookkeeping: cu_q[B+1] is the prefix sum of R_i = K_i + 1 (block
+ *     rows of sequence i are cu_q[i] .. cu_q[i+1]-1, R = cu_q[B]); draft rows
+ *     (draft logits, draft tokens) of sequence i are cu_q[i]-i .. cu_q[i+1]-i-2
+ *     (R - B rows in total).  Block row 0 is the pending token (its K/V not yet
+ *     cached), rows 1..K_i the drafts; block row j sits at token index L_i + j
+ *     and its logits decide token index L_i + j + 1.
+ *   - KV pool layout: token-major [pool_rows, Hkv, D]; sequence i's committed
+ *     rows are kv_start[i] .. kv_start[i] + kv_len[i] - 1.  The regions
+ *     [kv_start[i], kv_start[i] + kv_cap[i]) must not overlap each other or a
+ *     shared prefix.
+ *   - Host-checkable errors return a status != SV_OK synchronously and launch
+ *     nothing; sv_last_error() then describes it.  Data-dependent problems set
+ *     bits in *dev_status (atomic OR, never cleared by the library) and skip
+ *     only the affected sequence.  Kernels never trap.
+ *   - Workspace: sv_workspace_bytes() gives the size; the buffer must be
+ *     16-byte aligned and zeroed once (sv_workspace_init) before its first
+ *     use; every call leaves it ready for the next.  Calls that share one
+ *     workspace must not overlap in time (same stream, or ordered).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_API __attribute__((visibility("default")))
+#define SV_ABI_VERSION 1
+
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_INVALID = 1,      /* bad argument (null pointer, size out of range) */
+  SV_ERR_WORKSPACE = 2,    /* workspace missing, misaligned or too small */
+  SV_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, attribute) */
+  SV_ERR_UNSUPPORTED = 4   /* valid but not built: e.g. head_dim not 64/128 */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+enum {
+  SV_DEV_CAPACITY = 1u,        /* append would pass kv_cap[i]: append skipped,
+                                  new_kv_len[i] = kv_len[i] */
+  SV_DEV_BAD_TOKEN = 2u,       /* a draft token outside [0, V): treated as a
+                                  rejection at that row */
+  SV_DEV_NONFINITE = 4u,       /* a logits row holds NaN/+inf or only -inf:
+                                  the sequence fails (num_accepted = -1, its
+                                  out_tokens stay -1, no append) */
+  SV_DEV_EMPTY_RESIDUAL = 8u,  /* rejected but max(0, q-p) sums to 0: the
+                                  token is drawn from the target row instead */
+  SV_DEV_BAD_LENGTH = 16u      /* cu_q / kv_len / kv_start / prefix values
+                                  inconsistent with the host bounds or the
+                                  pool: that sequence is skipped */
+};
+
+/* Verify attention (a1, a1b).  scale * q.k softmax over keys
+ *   [prefix rows of group[i] (if num_groups > 0)] ++ [kv rows of i] ++
+ *   [block rows 0..j of i]
+ * with KV head h / (Hq / Hkv); fp32 accumulation.  Split over KV chunks
+ * (partials in the workspace) and merged by the last chunk to finish. */
+typedef struct sv_attn_args {
+  int32_t batch;            /* B >= 0 */
+  int32_t num_q_heads;      /* Hq >= 1 */
+  int32_t num_kv_heads;     /* Hkv >= 1, Hq % Hkv == 0 */
+  int32_t head_dim;         /* D: 64 or 128 */
+  int32_t dtype;            /* sv_dtype of q, k_new, v_new, caches and out */
+  int32_t max_q_rows;       /* host bound on R_i, 1..16; (Hq/Hkv)*max_q_rows <= 64 */
+  int64_t num_rows;         /* R = cu_q[B] (host copy) */
+  int64_t kv_rows_bound;    /* host bound on sum_i kv_len[i] (sizes the split) */
+  int64_t pool_rows;        /* rows of k_cache / v_cache */
+  float scale;              /* softmax scale; 0 -> 1/sqrt(D) */
+  int32_t num_groups;       /* G; 0 = no shared prefix */
+  int64_t prefix_rows_bound;/* host bound on sum_g prefix_len[g] (0 if G = 0) */
+  const int32_t *cu_q;      /* [dev] [B+1] */
+  const void *q;            /* [dev] [R, Hq, D] */
+  const void *k_new;        /* [dev] [R, Hkv, D] block K rows */
+  const void *v_new;        /* [dev] [R, Hkv, D] block V rows */
+  const void *k_cache;      /* [dev] [pool_rows, Hkv, D] */
+  const void *v_cache;      /* [dev] [pool_rows, Hkv, D] */
+  const int64_t *kv_start;  /* [dev] [B] first pool row of sequence i */
+  const int32_t *kv_len;    /* [dev] [B] L_i >= 0 */
+  const int32_t *group;     /* [dev] [B] group of sequence i (NULL if G = 0) */
+  const int64_t *prefix_start; /* [dev] [G] first pool row of the prefix */
+  const int32_t *prefix_len;   /* [dev] [G] */
+  void *out;                /* [dev] [R, Hq, D] */
+  uint32_t *dev_status;     /* [dev] one word */
+} sv_attn_args;
+
+/* Rejection sampling (a2-a5, a7).  Per sequence: processes its target rows
+ * (K_i + 1) and draft rows (K_i) with temperature then nucleus, accepts
+ * drafts left to right with Philox4x32-10 uniforms keyed by (seed,
+ * seq_ids[i], position, stream 0), draws the residual or bonus token by
+ * inverse CDF in vocabulary order.  Outputs: num_accepted[i] = n_i in
+ * [0, K_i] (-1 on failure); out_tokens[cu_q[i] + j] = draft j+1 for j < n_i,
+ * the drawn token at j = n_i, -1 after. */
+typedef struct sv_sample_args {
+  int32_t batch;            /* B >= 0 (must equal the attention's B in a step) */
+  int32_t vocab;            /* V >= 1 */
+  int32_t dtype;            /* sv_dtype of both logits tensors */
+  int32_t max_q_rows;       /* host bound on R_i, 1..16 */
+  int64_t num_rows;         /* R = cu_q[B] (host copy) */
+  float temperature;        /* > 0 */
+  float top_p;              /* (0, 1]; >= 1 disables the nucleus */
+  uint64_t seed;            /* Philox key */
+  const int32_t *cu_q;      /* [dev] [B+1] */
+  const void *target_logits;/* [dev] [R, V] */
+  const void *draft_logits; /* [dev] [R - B, V] */
+  const int32_t *draft_tokens; /* [dev] [R - B] */
+  const int32_t *kv_len;    /* [dev] [B] L_i: row j decides token L_i + j + 1 */
+  const int64_t *seq_ids;   /* [dev] [B] Philox sequence ids; NULL -> i */
+  int32_t *num_accepted;    /* [dev] [B] out */
+  int32_t *out_tokens;      /* [dev] [R] out */
+  uint32_t *dev_status;     /* [dev] one word */
+} sv_sample_args;
+
+/* Workspace bytes for an attention call, a sampling call, or (both
+ * non-NULL) a fused step.  Returns 0 if the arguments are invalid. */
+SV_API size_t sv_workspace_bytes(const sv_attn_args *attn, const sv_sample_args *sample);
+
+/* Zero a workspace once before its first use (cudaMemsetAsync on stream). */
+SV_API sv_status sv_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Verify attention only: writes attn->out. */
+SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+/* Rejection sampling only: writes num_accepted and out_tokens. */
+SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,
+                                    void *stream);
+
+/* Ragged append of accepted rows (a6).  For every sequence with
+ * num_accepted[i] = n >= 0 and kv_len[i] + n + 1 <= kv_cap[i]: copies block
+ * rows cu_q[i] .. cu_q[i] + n of k_new / v_new to pool rows kv_start[i] +
+ * kv_len[i] .. + n, and writes new_kv_len[i] = kv_len[i] + n + 1; otherwise
+ * new_kv_len[i] = kv_len[i] (with SV_DEV_CAPACITY on overflow).  Layouts as
+ * in sv_attn_args.  new_kv_len must not alias kv_len. */
+SV_API sv_status kv_append_ragged(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t dtype, int32_t max_q_rows, int64_t num_rows,
+                                  const int32_t *cu_q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, int64_t pool_rows,
+                                  const int64_t *kv_start, const int32_t *kv_len,
+                                  const int32_t *kv_cap, const int32_t *num_accepted,
+                                  int32_t *new_kv_len, uint32_t *dev_status, void *stream);
+
+/* The fused verify step: attention, rejection sampling and the append of the
+ * accepted rows, on one stream with no host synchronization.  attn and sample
+ * must describe the same batch (same cu_q and kv_len pointers).  kv_cap [dev]
+ * [B]; new_kv_len [dev] [B] out (must not alias kv_len).  The append writes
+ * only pool rows at or beyond kv_len[i], which the attention does not read. */
+SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args *sample,
+                                  const int32_t *kv_cap, int32_t *new_kv_len, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/* Thread-local description of the last non-OK status returned on this
+ * thread ("" if none). */
+SV_API const char *sv_last_error(void);
+
+/* SV_ABI_VERSION of the loaded library. */
+SV_API int32_t sv_abi_version(void);
+
+/* sizeof(sv_attn_args) for which = 0, sizeof(sv_sample_args) for which = 1
+ * (lets a binding check its struct mirrors). */
+SV_API size_t sv_struct_size(int32_t which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

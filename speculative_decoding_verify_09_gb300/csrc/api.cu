@@ -1,0 +1,312 @@
+// C ABI of the verify step: argument checks, workspace layout, launches.
+// See include/spec_verify.h for the contract of every entry point.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+sv_status fail(sv_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+sv_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxGrid = 2048;   // bound on persistent attention CTAs
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+sv_status check_attn(const sv_attn_args *a) {
+  if (!a) return fail(SV_ERR_INVALID, "attention args: null");
+  if (a->batch < 0 || a->batch > sv::attention_max_batch())
+    return fail(SV_ERR_INVALID, "attention: batch %d outside [0, %d]", a->batch,
+                sv::attention_max_batch());
+  if (a->num_q_heads < 1 || a->num_kv_heads < 1 || a->num_q_heads % a->num_kv_heads)
+    return fail(SV_ERR_INVALID, "attention: heads Hq=%d Hkv=%d (need Hq %% Hkv == 0)",
+                a->num_q_heads, a->num_kv_heads);
+  if (a->head_dim != 64 && a->head_dim != 128)
+    return fail(SV_ERR_UNSUPPORTED, "attention: head_dim %d (built: 64, 128)", a->head_dim);
+  if (a->dtype != SV_F32 && a->dtype != SV_BF16)
+    return fail(SV_ERR_INVALID, "attention: dtype %d", a->dtype);
+  if (a->max_q_rows < 1 || a->max_q_rows > sv::kMaxQRows)
+    return fail(SV_ERR_INVALID, "attention: max_q_rows %d outside [1, %d]", a->max_q_rows,
+                sv::kMaxQRows);
+  const int g = a->num_q_heads / a->num_kv_heads;
+  if (a->max_q_rows * g > sv::kMaxRowsM)
+    return fail(SV_ERR_UNSUPPORTED, "attention: max_q_rows * Hq/Hkv = %d > %d",
+                a->max_q_rows * g, sv::kMaxRowsM);
+  if (a->num_rows < a->batch || a->num_rows > static_cast<int64_t>(a->batch) * a->max_q_rows)
+    return fail(SV_ERR_INVALID, "attention: num_rows %lld inconsistent with batch %d and max_q_rows %d",
+                static_cast<long long>(a->num_rows), a->batch, a->max_q_rows);
+  if (a->kv_rows_bound < 0 || a->pool_rows < 0)
+    return fail(SV_ERR_INVALID, "attention: negative kv_rows_bound or pool_rows");
+  if (!std::isfinite(a->scale) || a->scale < 0.0f)
+    return fail(SV_ERR_INVALID, "attention: scale must be finite and >= 0");
+  if (a->num_groups != 0)
+    return fail(SV_ERR_UNSUPPORTED, "attention: shared-prefix groups not built in this library");
+  if (a->batch > 0) {
+    if (!a->cu_q || !a->q || !a->k_new || !a->v_new || !a->kv_start || !a->kv_len || !a->out)
+      return fail(SV_ERR_INVALID, "attention: null device pointer");
+    if (a->pool_rows > 0 && (!a->k_cache || !a->v_cache))
+      return fail(SV_ERR_INVALID, "attention: null cache pointer");
+    if (!aligned16(a->q) || !aligned16(a->k_new) || !aligned16(a->v_new) || !aligned16(a->out) ||
+        !aligned16(a->k_cache) || !aligned16(a->v_cache))
+      return fail(SV_ERR_INVALID, "attention: tensors must be 16-byte aligned");
+  }
+  return SV_OK;
+}
+
+sv_status check_sample(const sv_sample_args *a) {
+  if (!a) return fail(SV_ERR_INVALID, "sampling args: null");
+  if (a->batch < 0) return fail(SV_ERR_INVALID, "sampling: batch %d", a->batch);
+  if (a->vocab < 1 || a->vocab > sv::sampler_max_vocab(a->dtype))
+    return fail(SV_ERR_UNSUPPORTED, "sampling: vocab %d outside [1, %d]", a->vocab,
+                sv::sampler_max_vocab(a->dtype));
+  if (a->dtype != SV_F32 && a->dtype != SV_BF16)
+    return fail(SV_ERR_INVALID, "sampling: dtype %d", a->dtype);
+  if (a->max_q_rows < 1 || a->max_q_rows > sv::kMaxQRows)
+    return fail(SV_ERR_INVALID, "sampling: max_q_rows %d outside [1, %d]", a->max_q_rows,
+                sv::kMaxQRows);
+  if (a->num_rows < a->batch || a->num_rows > static_cast<int64_t>(a->batch) * a->max_q_rows)
+    return fail(SV_ERR_INVALID, "sampling: num_rows %lld inconsistent with batch %d and max_q_rows %d",
+                static_cast<long long>(a->num_rows), a->batch, a->max_q_rows);
+  if (!(a->temperature > 0.0f) || !std::isfinite(a->temperature))
+    return fail(SV_ERR_INVALID, "sampling: temperature must be finite and > 0 (greedy not built)");
+  if (!(a->top_p > 0.0f) || std::isnan(a->top_p))
+    return fail(SV_ERR_INVALID, "sampling: top_p must be > 0");
+  if (a->batch > 0) {
+    if (!a->cu_q || !a->target_logits || !a->kv_len || !a->num_accepted || !a->out_tokens)
+      return fail(SV_ERR_INVALID, "sampling: null device pointer");
+    if (a->num_rows > a->batch && (!a->draft_logits || !a->draft_tokens))
+      return fail(SV_ERR_INVALID, "sampling: null draft pointer");
+  }
+  return SV_OK;
+}
+
+struct Layout {
+  size_t cnt_attn, cnt_samp, stats, part_o, part_ml, total;
+  sv::AttnPlan plan;
+};
+
+// Workspace: [attention counters | sampler counters | row stats | partials].
+// The counter regions must be zero before a call and are left zero after it.
+Layout layout(const sv_attn_args *a, const sv_sample_args *s) {
+  Layout L{};
+  size_t off = 0;
+  if (a) {
+    L.cnt_attn = off;
+    off += round_up(static_cast<size_t>(a->batch) * a->num_kv_heads * 4);
+  }
+  if (s) {
+    L.cnt_samp = off;
+    off += round_up(static_cast<size_t>(s->batch) * 4);
+    L.stats = off;
+    off += round_up(sv::sampler_stats_bytes(*s));
+  }
+  if (a) {
+    // size the partials for the largest grid any device could get
+    sv_attn_args tmp = *a;
+    L.plan = sv::plan_attention(tmp, 0);
+    L.plan.grid = std::min<int64_t>(L.plan.tiles_bound, kMaxGrid);
+    const int64_t slots = (a->dtype == SV_BF16 ? L.plan.grid : 0) +
+                          static_cast<int64_t>(a->batch) * a->num_kv_heads;
+    const int64_t rows = static_cast<int64_t>(L.plan.m_tiles) * 16;
+    L.part_o = off;
+    off += round_up(a->dtype == SV_BF16 ? static_cast<size_t>(slots * rows * a->head_dim * 4) : 0);
+    L.part_ml = off;
+    off += round_up(a->dtype == SV_BF16 ? static_cast<size_t>(slots * rows * 8) : 0);
+  }
+  L.total = off;
+  return L;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+sv_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return SV_OK;
+  if (!ws) return fail(SV_ERR_WORKSPACE, "workspace: null (need %zu bytes)", need);
+  if (!aligned16(ws)) return fail(SV_ERR_WORKSPACE, "workspace: not 16-byte aligned");
+  if (ws_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "workspace: %zu bytes given, %zu needed", ws_bytes, need);
+  return SV_OK;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+sv_status run_attention(const sv_attn_args *a, const Layout &L, void *ws, bool pdl,
+                        cudaStream_t s) {
+  if (a->batch == 0) return SV_OK;
+  sv::AttnPlan plan = L.plan;
+  const int sms = num_sms_current();
+  if (sms <= 0) return fail(SV_ERR_CUDA, "no CUDA device");
+  sv::AttnPlan live = sv::plan_attention(*a, sms);
+  plan.grid = std::min<int64_t>(live.grid, L.plan.grid);
+  cudaError_t e = sv::launch_attention(*a, plan, at<float>(ws, L.part_o), at<float>(ws, L.part_ml),
+                                       at<uint32_t>(ws, L.cnt_attn), pdl, s);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SV_API size_t sv_workspace_bytes(const sv_attn_args *attn, const sv_sample_args *sample) {
+  if (!attn && !sample) return 0;
+  if (attn && check_attn(attn) != SV_OK) return 0;
+  if (sample && check_sample(sample) != SV_OK) return 0;
+  const size_t t = layout(attn, sample).total;
+  return t > 0 ? t : kAlign;
+}
+
+SV_API sv_status sv_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws || ws_bytes == 0) return fail(SV_ERR_WORKSPACE, "workspace_init: empty workspace");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace_init");
+  return SV_OK;
+}
+
+SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  sv_status st = check_attn(attn);
+  if (st != SV_OK) return st;
+  const Layout L = layout(attn, nullptr);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
+  return run_attention(attn, L, ws, false, static_cast<cudaStream_t>(stream));
+}
+
+SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,
+                                    void *stream) {
+  sv_status st = check_sample(sample);
+  if (st != SV_OK) return st;
+  const Layout L = layout(nullptr, sample);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
+  if (sample->batch == 0) return SV_OK;
+  sv::SamplerLaunch SL{};
+  SL.a = *sample;
+  SL.stats = at<sv::RowStats>(ws, L.stats);
+  SL.counters = at<uint32_t>(ws, L.cnt_samp);
+  SL.do_append = false;
+  SL.pdl_primary = false;
+  cudaError_t e = sv::launch_sampler(SL, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return SV_OK;
+}
+
+SV_API sv_status kv_append_ragged(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t dtype, int32_t max_q_rows, int64_t num_rows,
+                                  const int32_t *cu_q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, int64_t pool_rows,
+                                  const int64_t *kv_start, const int32_t *kv_len,
+                                  const int32_t *kv_cap, const int32_t *num_accepted,
+                                  int32_t *new_kv_len, uint32_t *dev_status, void *stream) {
+  if (batch < 0) return fail(SV_ERR_INVALID, "append: batch %d", batch);
+  if (num_kv_heads < 1 || head_dim < 1 || (dtype != SV_F32 && dtype != SV_BF16))
+    return fail(SV_ERR_INVALID, "append: bad shape or dtype");
+  const int esz = dtype == SV_F32 ? 4 : 2;
+  const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * esz;
+  if (row_bytes % 16 || row_bytes > (1 << 30))
+    return fail(SV_ERR_UNSUPPORTED, "append: row bytes %lld not a multiple of 16",
+                static_cast<long long>(row_bytes));
+  if (max_q_rows < 1 || max_q_rows > sv::kMaxQRows)
+    return fail(SV_ERR_INVALID, "append: max_q_rows %d", max_q_rows);
+  if (num_rows < batch || num_rows > static_cast<int64_t>(batch) * max_q_rows || pool_rows < 0)
+    return fail(SV_ERR_INVALID, "append: num_rows / pool_rows");
+  if (batch == 0) return SV_OK;
+  if (!cu_q || !k_new || !v_new || !k_cache || !v_cache || !kv_start || !kv_len || !kv_cap ||
+      !num_accepted || !new_kv_len)
+    return fail(SV_ERR_INVALID, "append: null device pointer");
+  if (new_kv_len == kv_len) return fail(SV_ERR_INVALID, "append: new_kv_len aliases kv_len");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(SV_ERR_INVALID, "append: tensors must be 16-byte aligned");
+  cudaError_t e = sv::launch_append(batch, static_cast<int32_t>(row_bytes), max_q_rows, num_rows,
+                                    cu_q, k_new, v_new, k_cache, v_cache, pool_rows, kv_start,
+                                    kv_len, kv_cap, num_accepted, new_kv_len, dev_status,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return SV_OK;
+}
+
+SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args *sample,
+                                  const int32_t *kv_cap, int32_t *new_kv_len, void *ws,
+                                  size_t ws_bytes, void *stream) {
+  sv_status st = check_attn(attn);
+  if (st != SV_OK) return st;
+  if ((st = check_sample(sample)) != SV_OK) return st;
+  if (attn->batch != sample->batch || attn->num_rows != sample->num_rows ||
+      attn->cu_q != sample->cu_q || attn->kv_len != sample->kv_len ||
+      attn->max_q_rows != sample->max_q_rows)
+    return fail(SV_ERR_INVALID, "step: attention and sampling describe different batches");
+  if (attn->batch > 0) {
+    if (!kv_cap || !new_kv_len) return fail(SV_ERR_INVALID, "step: null kv_cap / new_kv_len");
+    if (new_kv_len == attn->kv_len) return fail(SV_ERR_INVALID, "step: new_kv_len aliases kv_len");
+    if (!attn->k_cache || !attn->v_cache) return fail(SV_ERR_INVALID, "step: null cache");
+  }
+  const Layout L = layout(attn, sample);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
+  if (attn->batch == 0) return SV_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Sampling (with the append of accepted rows) is the primary launch; the
+  // attention launch may start while it runs and waits for it before exiting.
+  sv::SamplerLaunch SL{};
+  SL.a = *sample;
+  SL.stats = at<sv::RowStats>(ws, L.stats);
+  SL.counters = at<uint32_t>(ws, L.cnt_samp);
+  SL.do_append = true;
+  SL.pdl_primary = true;
+  const int esz = attn->dtype == SV_F32 ? 4 : 2;
+  SL.app.k_new = attn->k_new;
+  SL.app.v_new = attn->v_new;
+  SL.app.k_cache = const_cast<void *>(attn->k_cache);
+  SL.app.v_cache = const_cast<void *>(attn->v_cache);
+  SL.app.pool_rows = attn->pool_rows;
+  SL.app.kv_start = attn->kv_start;
+  SL.app.kv_cap = kv_cap;
+  SL.app.new_kv_len = new_kv_len;
+  SL.app.row_bytes = attn->num_kv_heads * attn->head_dim * esz;
+  if (SL.app.row_bytes % 16)
+    return fail(SV_ERR_UNSUPPORTED, "step: K/V row bytes not a multiple of 16");
+  cudaError_t e = sv::launch_sampler(SL, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return run_attention(attn, L, ws, true, s);
+}
+
+SV_API const char *sv_last_error(void) { return g_err.c_str(); }
+
+SV_API int32_t sv_abi_version(void) { return SV_ABI_VERSION; }
+
+SV_API size_t sv_struct_size(int32_t which) {
+  return which == 0 ? sizeof(sv_attn_args) : which == 1 ? sizeof(sv_sample_args) : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+"""The C-ABI library: it builds, loads without a GPU, exports exactly what
+include/*.h declares, and rejects bad host arguments synchronously (these
+calls launch nothing, so they run on a GPU-less host)."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from speculative_decoding_verify_09_gb300 import build
+    build()
+    from speculative_decoding_verify_09_gb300 import _binding
+    return _binding
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"SV_API\s+[\w\s\*]+?\b(\w+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_exactly_the_declared_symbols(binding):
+    decl = declared_symbols()
+    assert {"spec_verify_attn", "spec_reject_sample", "kv_append_ragged",
+            "spec_verify_step"} <= decl
+    for name in decl:
+        assert hasattr(binding.lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.split() and ln.split()[1] in "TW"}
+    exported = {e for e in exported if not e.startswith("_")}
+    assert exported == decl
+
+
+def test_struct_mirrors_and_version(binding):
+    assert binding.lib.sv_abi_version() == 1
+    assert binding.lib.sv_struct_size(0) == ctypes.sizeof(binding.AttnArgs)
+    assert binding.lib.sv_struct_size(1) == ctypes.sizeof(binding.SampleArgs)
+
+
+def _attn(b, **kw):
+    a = b.AttnArgs()
+    a.batch, a.num_q_heads, a.num_kv_heads, a.head_dim = 2, 8, 2, 128
+    a.dtype, a.max_q_rows, a.num_rows, a.kv_rows_bound, a.pool_rows = b.SV_BF16, 5, 10, 100, 200
+    for k in ("cu_q", "q", "k_new", "v_new", "k_cache", "v_cache", "kv_start", "kv_len", "out"):
+        setattr(a, k, 4096)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _sample(b, **kw):
+    s = b.SampleArgs()
+    s.batch, s.vocab, s.dtype, s.max_q_rows, s.num_rows = 2, 1000, b.SV_BF16, 5, 10
+    s.temperature, s.top_p, s.seed = 1.0, 1.0, 0
+    for k in ("cu_q", "target_logits", "draft_logits", "draft_tokens", "kv_len", "num_accepted",
+              "out_tokens"):
+        setattr(s, k, 4096)
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_kv_heads", 3, 1), ("head_dim", 96, 4), ("max_q_rows", 0, 1), ("max_q_rows", 17, 1),
+    ("num_rows", 11, 1), ("num_rows", 1, 1), ("dtype", 7, 1), ("q", 4097, 1), ("out", 0, 1),
+    ("num_groups", 1, 4), ("batch", 5000, 1),
+])
+def test_attention_host_validation(binding, field, value, status):
+    a = _attn(binding, **{field: value})
+    st = binding.lib.spec_verify_attn(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == status, binding.last_error()
+    assert binding.last_error()
+    assert binding.lib.sv_workspace_bytes(ctypes.byref(a), None) == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("temperature", 0.0, 1), ("temperature", float("inf"), 1), ("top_p", 0.0, 1),
+    ("vocab", 0, 4), ("vocab", 10 ** 7, 4), ("num_rows", 1, 1), ("target_logits", 0, 1),
+])
+def test_sampling_host_validation(binding, field, value, status):
+    s = _sample(binding, **{field: value})
+    st = binding.lib.spec_reject_sample(ctypes.byref(s), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == status, binding.last_error()
+
+
+def test_workspace_checks(binding):
+    a, s = _attn(binding), _sample(binding)
+    need = binding.lib.sv_workspace_bytes(ctypes.byref(a), ctypes.byref(s))
+    assert need > 0 and need % 256 == 0
+    assert binding.lib.sv_workspace_bytes(ctypes.byref(a), None) < need
+    st = binding.lib.spec_verify_step(ctypes.byref(a), ctypes.byref(s), ctypes.c_void_p(4096),
+                                      ctypes.c_void_p(8192), ctypes.c_void_p(4096), need - 1, None)
+    assert st == binding.SV_ERR_WORKSPACE
+    st = binding.lib.spec_verify_step(ctypes.byref(a), ctypes.byref(s), ctypes.c_void_p(4096),
+                                      ctypes.c_void_p(8192), ctypes.c_void_p(4104), need, None)
+    assert st == binding.SV_ERR_WORKSPACE          # misaligned
+
+
+def test_step_rejects_mismatched_batches_and_aliasing(binding):
+    a, s = _attn(binding), _sample(binding, cu_q=8192)
+    st = binding.lib.spec_verify_step(ctypes.byref(a), ctypes.byref(s), ctypes.c_void_p(4096),
+                                      ctypes.c_void_p(8192), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == binding.SV_ERR_INVALID
+    s = _sample(binding)
+    st = binding.lib.spec_verify_step(ctypes.byref(a), ctypes.byref(s), ctypes.c_void_p(4096),
+                                      ctypes.c_void_p(4096), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == binding.SV_ERR_INVALID            # new_kv_len aliases kv_len
+
+
+def test_append_host_validation(binding):
+    f = binding.lib.kv_append_ragged
+    p = ctypes.c_void_p(4096)
+    assert f(2, 1, 3, binding.SV_BF16, 5, 10, *([p] * 5), 100, p, p, p, p,
+             ctypes.c_void_p(8192), None, None) == binding.SV_ERR_UNSUPPORTED   # 6-byte rows
+    assert f(2, 8, 128, binding.SV_BF16, 5, 10, *([p] * 5), 100, p, p, p, p, p, None,
+             None) == binding.SV_ERR_INVALID      # new_kv_len aliases kv_len
+
+
+def test_binding_module_has_no_fallback():
+    src = open(os.path.join(ROOT, "speculative_decoding_verify_09_gb300", "_binding.py")).read()
+    assert "oracle" not in src and "import numpy" not in src
+    for f in glob.glob(os.path.join(ROOT, "speculative_decoding_verify_09_gb300", "*.py")):
+        assert "import oracle" not in open(f).read() and "from oracle" not in open(f).read()

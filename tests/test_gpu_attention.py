@@ -1,0 +1,169 @@
+"""GPU parity of spec_verify_attn against the CPU oracle.
+
+Tolerance (the benchmark spec): max-abs 2e-2 for bf16 K/V, 1e-4 for fp32.  Small
+cases compare every output; full-size workloads compare a seeded sample of
+(sequence, head, row) outputs computed one by one by the oracle.  Sources:
+"Accelerating Large Language Model Decoding with Speculative Sampling",
+section "Conditional scoring"; BASS and EMS-SD abstracts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import DeviceStep
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import speculative_decoding_verify_09_gb300 as pkg
+    pkg.build()
+    return pkg.load()
+
+
+def run_attn(api, inp):
+    d = DeviceStep({k: v for k, v in inp.items()
+                    if k not in ("target_logits", "draft_logits", "draft_tokens")}, api)
+    api.spec_verify_attn(d.attn, d.ws)
+    torch.cuda.synchronize()
+    return d
+
+
+def tol(inp):
+    return 1e-4 if inp["dtype"] == "f32" else 2e-2
+
+
+def full_check(api, inp):
+    d = run_attn(api, inp)
+    got = d.out.float().cpu().numpy()
+    ref = oracle.verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
+                                  inp["v_cache"], inp["cu_q"], inp["kv_start"], inp["kv_len"],
+                                  inp["num_kv_heads"])
+    err = np.max(np.abs(got - ref))
+    assert np.all(np.isfinite(got)) and err < tol(inp), err
+    assert d.status_bits() == 0
+    return err
+
+
+def sampled_check(api, inp, n=96, seed=0):
+    d = run_attn(api, inp)
+    got = d.out.float().cpu().numpy()
+    assert np.all(np.isfinite(got)), "unwritten or non-finite outputs"
+    rng = np.random.default_rng(seed)
+    cu = inp["cu_q"]
+    worst = 0.0
+    for _ in range(n):
+        i = int(rng.integers(0, inp["B"]))
+        j = int(rng.integers(0, cu[i + 1] - cu[i]))
+        h = int(rng.integers(0, inp["num_q_heads"]))
+        ref = oracle.attention_row(i, h, j, inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
+                                   inp["v_cache"], cu, inp["kv_start"], inp["kv_len"],
+                                   inp["num_kv_heads"])
+        worst = max(worst, float(np.max(np.abs(got[cu[i] + j, h] - ref))))
+    assert worst < tol(inp), worst
+    assert d.status_bits() == 0
+    return worst
+
+
+def attn_inputs(name, **kw):
+    return W.make_inputs(W.workload(name, **kw), with_logits=False)
+
+
+def test_tiny_fp32(api):
+    full_check(api, attn_inputs("tiny_f32"))
+
+
+def test_fp32_gqa_d128(api):
+    full_check(api, attn_inputs("tiny_f32", B=3, Hq=8, Hkv=2, D=128, L_dist="uniform",
+                                L_lo=0, L_hi=90, K_lo=0, K_hi=7, gen_seed=9))
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,K_hi", [
+    (128, 4, 4, 5),     # MHA, one m-tile
+    (64, 4, 4, 5),      # head_dim 64
+    (128, 8, 2, 7),     # GQA g=4, up to 32 packed rows (2 m-tiles)
+    (128, 8, 2, 8),     # 36 rows (3 m-tiles)
+    (64, 16, 2, 7),     # g=8, 64 rows (4 m-tiles)
+])
+def test_bf16_small_all_outputs(api, D, Hq, Hkv, K_hi):
+    inp = attn_inputs("bass_b8", B=5, Hq=Hq, Hkv=Hkv, D=D, L_lo=0, L_hi=700, K_lo=0,
+                      K_hi=K_hi, gen_seed=D + Hq + K_hi)
+    full_check(api, inp)
+
+
+def test_one_long_sequence_many_pieces(api):
+    """One (sequence, head) split across many CTAs: many partials merged."""
+    inp = attn_inputs("bass_b8", B=1, Hq=2, Hkv=1, L_lo=40000, L_hi=40000, K_lo=5, K_hi=5,
+                      gen_seed=3)
+    full_check(api, inp)
+
+
+def test_many_short_sequences(api):
+    inp = attn_inputs("ragged_gqa_b32", B=300, L_lo=1, L_hi=40, L_dist="uniform",
+                      Hq=8, Hkv=2, gen_seed=4)
+    full_check(api, inp)
+
+
+def test_zero_length_cache_rows_only_block(api):
+    inp = attn_inputs("bass_b8", B=4, Hq=4, Hkv=4, L_lo=0, L_hi=0, K_lo=0, K_hi=4, gen_seed=5)
+    full_check(api, inp)
+
+
+@pytest.mark.parametrize("name", ["bass_b8", "ragged_gqa_b32", "vocab128k_b64"])
+def test_full_size_sampled(api, name):
+    sampled_check(api, attn_inputs(name))
+
+
+def test_shared_prefix_arrangement_as_plain_cache(api):
+    """The shared-prefix workload run as plain per-sequence caches (prefix rows
+    copied in front of each sequence's own rows): same result as the
+    oracle's shared-prefix definition."""
+    inp = attn_inputs("shared_prefix_s32", B=6, prefix_len=700, gen_seed=6)
+    P = int(inp["prefix_len"][0])
+    ps = int(inp["prefix_start"][0])
+    Ls = inp["kv_len"].astype(np.int64)
+    starts = np.concatenate([[0], np.cumsum(P + Ls + 8)[:-1]]).astype(np.int64)
+    rows = int(starts[-1] + P + Ls[-1] + 8)
+    kc = np.zeros((rows,) + inp["k_cache"].shape[1:], dtype=inp["k_cache"].dtype)
+    vc = np.zeros_like(kc)
+    for i in range(inp["B"]):
+        for src, dst in ((inp["k_cache"], kc), (inp["v_cache"], vc)):
+            dst[starts[i]:starts[i] + P] = src[ps:ps + P]
+            a = int(inp["kv_start"][i])
+            dst[starts[i] + P:starts[i] + P + Ls[i]] = src[a:a + Ls[i]]
+    flat = dict(inp, k_cache=kc, v_cache=vc, kv_start=starts,
+                kv_len=(Ls + P).astype(np.int32), pool_rows=rows)
+    flat.pop("group")
+    d = run_attn(api, flat)
+    got = d.out.float().cpu().numpy()
+    ref = oracle.verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
+                                  inp["v_cache"], inp["cu_q"], inp["kv_start"], inp["kv_len"],
+                                  inp["num_kv_heads"],
+                                  prefix=(inp["group"], inp["prefix_start"], inp["prefix_len"]))
+    assert np.max(np.abs(got - ref)) < 2e-2
+
+
+def test_bad_lengths_set_status_and_skip(api):
+    inp = attn_inputs("bass_b8", B=3, Hq=4, Hkv=4, L_lo=10, L_hi=50, gen_seed=8)
+    inp["kv_len"] = inp["kv_len"].copy()
+    inp["kv_len"][1] = 10 ** 6                 # past the pool: skipped, flagged
+    d = DeviceStep({k: v for k, v in inp.items()}, api)
+    d.attn.kv_rows_bound = 10 ** 7
+    api.spec_verify_attn(d.attn, d.ws)
+    torch.cuda.synchronize()
+    assert d.status_bits() & oracle.DEV_BAD_LENGTH
+    got = d.out.float().cpu().numpy()
+    cu = inp["cu_q"]
+    assert np.all(np.isnan(got[cu[1]:cu[2]]))           # untouched
+    ok = np.concatenate([np.arange(cu[0], cu[1]), np.arange(cu[2], cu[3])])
+    assert np.all(np.isfinite(got[ok]))
+
+
+def test_deterministic(api):
+    inp = attn_inputs("ragged_gqa_b32", B=8, gen_seed=12)
+    a = run_attn(api, inp).out.clone()
+    b = run_attn(api, inp).out
+    assert torch.equal(a, b)

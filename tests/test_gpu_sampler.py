@@ -1,0 +1,145 @@
+"""GPU parity of spec_reject_sample against the CPU oracle.
+
+Tokens and accepted counts must match bit for bit outside the oracle's
+near-tie windows (|u - min(1,q/p)| < 1e-5, a drawn token's CDF interval end
+within 1e-5 of u, nucleus boundary mass within 2e-6 of top_p, residual mass
+below 1e-2); inside them the GPU must still agree up to the tied decision and
+draw a weighted neighbour.  Sources: "Accelerating Large Language Model
+Decoding with Speculative Sampling", section "Modified rejection sampling";
+EMS-SD abstract (ragged draft counts, no padding).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import DeviceStep, compare_sampling
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import speculative_decoding_verify_09_gb300 as pkg
+    pkg.build()
+    return pkg.load()
+
+
+def run_sampler(api, inp, seed=None):
+    d = DeviceStep({k: v for k, v in inp.items() if k not in ("q",)}, api, seed=seed)
+    api.spec_reject_sample(d.sample, d.ws)
+    torch.cuda.synchronize()
+    return d
+
+
+def oracle_sampler(inp, seed=None):
+    return oracle.reject_sample(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
+                                inp["cu_q"], inp["kv_len"], inp["temperature"], inp["top_p"],
+                                inp["seed"] if seed is None else seed, inp["seq_ids"])
+
+
+def check(api, inp, seed=None, expect_status=0):
+    d = run_sampler(api, inp, seed)
+    ref = oracle_sampler(inp, seed)
+    n, ties = compare_sampling(ref, d.num_accepted.cpu().numpy(), d.out_tokens.cpu().numpy(),
+                               inp["cu_q"])
+    assert d.status_bits() == (ref["status"] | expect_status), (d.status_bits(), ref["status"])
+    return d, ref, ties
+
+
+def sampler_inputs(name, **kw):
+    return W.make_inputs(W.workload(name, **kw), with_attention=False)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny_f32", {}),
+    ("bass_b8", {}),
+    ("ragged_gqa_b32", {}),
+    ("shared_prefix_s32", {}),
+    ("vocab128k_b64", {"draft_noise": 0.25}),
+    ("vocab128k_b64", {"draft_noise": 1.0}),
+    ("vocab128k_b64", {"draft_noise": 4.0}),
+])
+def test_full_size_workloads(api, name, kw):
+    inp = sampler_inputs(name, **kw)
+    _, ref, ties = check(api, inp)
+    print(f"{name} {kw}: mean accepted {np.mean(ref['num_accepted']):.2f}, tie sequences {ties}")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_many_seeds_gqa_shape(api, seed):
+    inp = sampler_inputs("ragged_gqa_b32", gen_seed=100 + seed)
+    check(api, inp, seed=seed * 7919)
+
+
+@pytest.mark.parametrize("V", [1, 7, 1001, 4099])
+def test_vocab_sizes_unaligned_rows(api, V):
+    """Odd vocabularies: bf16 rows not 16-byte aligned take the scalar loads."""
+    inp = sampler_inputs("ragged_gqa_b32", B=9, V=V, gen_seed=7)
+    check(api, inp)
+
+
+def test_fp32_logits_with_nucleus(api):
+    inp = sampler_inputs("tiny_f32", B=2, V=5000, temperature=0.6, top_p=0.8, gen_seed=3)
+    check(api, inp)
+
+
+def test_zero_drafts_and_max_drafts(api):
+    """K_i = 0 (bonus only) next to K_i = 15 (16 block rows)."""
+    inp = sampler_inputs("ragged_gqa_b32", B=12, K_lo=0, K_hi=15, V=3000, gen_seed=11)
+    assert (np.diff(inp["cu_q"]) - 1).min() == 0 and (np.diff(inp["cu_q"]) - 1).max() >= 12
+    check(api, inp)
+
+
+def test_p_equals_q_accepts_all(api):
+    inp = sampler_inputs("bass_b8", V=2000, gen_seed=5)
+    cu = inp["cu_q"]
+    for i in range(inp["B"]):
+        for j in range(cu[i + 1] - cu[i] - 1):
+            inp["draft_logits"][cu[i] - i + j] = inp["target_logits"][cu[i] + j]
+    d, ref, _ = check(api, inp)
+    assert np.all(d.num_accepted.cpu().numpy() == np.diff(cu) - 1)
+
+
+def test_tiny_top_p_and_tie_heavy_logits(api):
+    """Quantized logits (many exact ties) with several top_p values."""
+    rng = np.random.default_rng(0)
+    for top_p in (1e-6, 0.3, 0.9, 0.999):
+        inp = sampler_inputs("ragged_gqa_b32", B=6, V=700, gen_seed=13, top_p=top_p)
+        q = rng.integers(-8, 8, size=inp["target_logits"].shape).astype(np.float32) * 0.5
+        inp["target_logits"] = W.f32_to_bf16_bits(q)
+        inp["draft_logits"] = W.f32_to_bf16_bits(
+            q[np.concatenate([np.arange(inp["cu_q"][i], inp["cu_q"][i + 1] - 1)
+                              for i in range(inp["B"])])] +
+            rng.integers(-2, 3, size=inp["draft_logits"].shape).astype(np.float32) * 0.5)
+        check(api, inp)
+
+
+def test_bad_tokens_nonfinite_and_masked_rows(api):
+    inp = sampler_inputs("bass_b8", B=6, V=512, gen_seed=17, top_p=0.9)
+    cu = inp["cu_q"]
+    inp["draft_tokens"][cu[1] - 1 + 1] = 512          # seq 1, draft 2: out of range
+    inp["draft_tokens"][cu[2] - 2] = -3               # seq 2, draft 1: negative
+    nan_bits = np.uint16(0x7FC0)
+    inp["target_logits"][cu[3] + 2, 100] = nan_bits   # seq 3 fails
+    inp["draft_logits"][cu[4] - 4, 5] = np.uint16(0x7F80)   # +inf: seq 4 fails
+    inp["target_logits"][cu[5]:cu[6], :400] = np.uint16(0xFF80)   # -inf: masked tokens
+    d, ref, _ = check(api, inp, expect_status=0)
+    assert ref["status"] & oracle.DEV_BAD_TOKEN and ref["status"] & oracle.DEV_NONFINITE
+    na = d.num_accepted.cpu().numpy()
+    assert na[3] == -1 and na[4] == -1
+    toks = d.out_tokens.cpu().numpy()
+    assert np.all(toks[cu[5]:cu[6]][toks[cu[5]:cu[6]] >= 0] >= 400)
+
+
+def test_deterministic_and_seq_id_keyed(api):
+    inp = sampler_inputs("ragged_gqa_b32", B=16, V=2048, gen_seed=21)
+    a = run_sampler(api, inp)
+    b = run_sampler(api, inp)
+    assert torch.equal(a.out_tokens, b.out_tokens) and torch.equal(a.num_accepted, b.num_accepted)
+    # a different seq_id for sequence 0 changes only sequence 0's uniforms
+    inp2 = dict(inp)
+    inp2["seq_ids"] = inp["seq_ids"].copy()
+    inp2["seq_ids"][0] = 1 << 40
+    check(api, inp2)
