@@ -1,0 +1,348 @@
+"""Benchmark of the fused verify step (spec_verify_step) on the bass_b8 workload.
+
+Default: 1 GPU.  Under torchrun, one rank per GPU, each with its own batch of
+8 sequences (global sequence ids offset by rank): weak scaling, no data-path
+collective; the barrier and the max-over-ranks timing use torch.distributed.
+
+Prints one JSON line (rank 0).  `value` = verify steps/s of the whole job with
+inputs resident in HBM (CUDA-graph replays of the C-ABI call, three rotating
+input sets so every step reads ~176 MB > L2); `e2e` = the same metric through
+the C-ABI call with pinned host buffers copied in and results copied out every
+step; `roofline` = the attention kernel (the dominant one) timed alone;
+`cpu_baseline` = the CPU oracle timed on a bounded sample.
+`--impl reference` times the CPU oracle alone (the reference arm).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verify steps/s & accepted tok/s at B=8 7.8B-shape; achieved HBM GB/s vs peak"
+UNIT = "steps/s"
+WORKLOAD = "bass_b8"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_desc(w):
+    return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, KV len U[{w.L_lo},{w.L_hi}], "
+            f"K={w.K_lo}, V={w.V}, {w.dtype}, T={w.temperature}, top_p={w.top_p}")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_gb_s"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_src_sha):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for ln in open(p):
+        f = ln.split()
+        if len(f) == 4 and f[0] == "attention" and f[1] == WORKLOAD and f[2] == kernel_src_sha:
+            return float(f[3])
+    return None
+
+
+def src_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_09_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("attention") or f.endswith((".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_baseline(inp, budget_s=12.0):
+    """The oracle, as it stands, on whole bass_b8 steps until the budget is
+    used (at least one step)."""
+    import oracle
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify_step(inp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole {WORKLOAD} steps (attention + sampling + append), "
+                      f"{el:.1f} s, OMP/BLAS threads 1"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    w = W.workload(WORKLOAD)
+    inp = W.make_inputs(w)
+    import oracle
+    for _ in range(min(args.warmup, 1)):
+        oracle.verify_step(inp)
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.verify_step(inp)
+    el = time.perf_counter() - t0
+    v = steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * el / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(w)},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{steps} whole steps (the requested count, capped at 3)"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--sets", type=int, default=3, help="rotating input sets (L2 defeat)")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--attn-steps", type=int, default=3000,
+                    help="attention-only launches timed for the roofline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch directly (profiling)")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import speculative_decoding_verify_09_gb300 as pkg
+    pkg.build()
+    api = pkg.load()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    w = W.workload(WORKLOAD)
+    inp = W.make_inputs(w)
+    inp["seq_ids"] = inp["seq_ids"] + rank * w.B          # global sequence ids
+    from speculative_decoding_verify_09_gb300.buffers import StepBuffers
+    sets = [StepBuffers(inp, api) for _ in range(args.sets)]
+    nbytes = W.step_bytes(inp)
+    stream = torch.cuda.current_stream()
+
+    def step(d):
+        api.spec_verify_step(d.attn, d.sample, d.kv_cap, d.new_kv_len, d.ws)
+
+    def attn_only(d):
+        api.spec_verify_attn(d.attn, d.ws)
+
+    # warm-up (also settles the accepted counts used for the append bytes)
+    for k in range(max(args.warmup, 3)):
+        step(sets[k % len(sets)])
+    torch.cuda.synchronize()
+    n_acc = sets[0].num_accepted.cpu().numpy()
+    emitted = int(np.sum(n_acc + 1))
+    esz = 2
+    append_bytes = 2 * 2 * emitted * w.Hkv * w.D * esz        # K and V, read + write
+    step_total = nbytes["attention"] + nbytes["sampler"] + append_bytes
+
+    def timed(fn, n_launch):
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for d in sets:
+                    fn(d)
+            torch.cuda.synchronize()
+        reps = max(1, n_launch // len(sets))
+        for _ in range(2):
+            graph.replay() if graph else [fn(d) for d in sets]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            if graph:
+                graph.replay()
+            else:
+                for d in sets:
+                    fn(d)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        if dist:
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, reps * len(sets)
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
+    clk = Clocks(gpu_index)
+    time.sleep(0.3)
+    ms_step, n_steps = timed(step, args.steps)
+    clocks = clk.stop()
+    ms_attn, n_attn = timed(attn_only, args.attn_steps)
+
+    emitted_all = emitted
+    if dist:
+        t = torch.tensor([emitted], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t)
+        emitted_all = int(t.item())
+    per_step_ms = ms_step / n_steps
+    value = world * n_steps / (ms_step / 1e3)
+    attn_us = 1e3 * ms_attn / n_attn
+    peak, peak_kind = peaks()
+    achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
+    sha = src_sha()
+    traffic = traffic_record(sha)
+
+    # end to end through the C ABI with pinned host buffers
+    d = sets[0]
+    host_in = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
+               for k, v in (("q", inp["q"]), ("k_new", inp["k_new"]), ("v_new", inp["v_new"]),
+                            ("tgt", inp["target_logits"]), ("drf", inp["draft_logits"]),
+                            ("drafts", inp["draft_tokens"]), ("cu_q", inp["cu_q"]),
+                            ("kv_len", inp["kv_len"]), ("kv_start", inp["kv_start"]),
+                            ("kv_cap", inp["kv_cap"]), ("seq_ids", inp["seq_ids"]))}
+    dev_views = {"q": d.q.view(torch.int16), "k_new": d.k_new.view(torch.int16),
+                 "v_new": d.v_new.view(torch.int16), "tgt": d.tgt.view(torch.int16),
+                 "drf": d.drf.view(torch.int16), "drafts": d.drafts, "cu_q": d.cu_q,
+                 "kv_len": d.kv_len, "kv_start": d.kv_start, "kv_cap": d.kv_cap,
+                 "seq_ids": d.seq_ids}
+    outs = {"out": d.out.view(torch.int16), "num_accepted": d.num_accepted,
+            "out_tokens": d.out_tokens, "new_kv_len": d.new_kv_len}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    for it in range(3 + args.e2e_steps):
+        if it == 3:
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        for k, t in host_in.items():
+            dev_views[k].copy_(t, non_blocking=True)
+        step(d)
+        for k, t in outs.items():
+            host_out[k].copy_(t, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": per_step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; random-init tensors of the workload's shapes)",
+            "config": {"workload": workload_desc(w), "parallelism": f"dp{world} (sequence shards)",
+                       "global_batch": world * w.B,
+                       "l2": f"inputs larger than L2: {len(sets)} rotating input sets of "
+                             f"{step_total / 1e6:.0f} MB per step",
+                       "launch": "CUDA graph of the C-ABI call per input set" if not args.no_graph
+                       else "direct launches"},
+            "accepted_tok_s": emitted_all * n_steps / (ms_step / 1e3),
+            "mean_accepted_per_seq": float(np.mean(n_acc)),
+            "step_bytes": step_total,
+            "step_hbm_gbs": step_total / (per_step_ms * 1e-3) / 1e9,
+            "step_frac_of_peak": step_total / (per_step_ms * 1e-3) / 1e9 / peak,
+            "roofline": {"kernel": "attention (split-KV, stream-K)", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                         "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["attention"],
+                         "avg_launch_us": attn_us, "kernel_src": sha},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * n_steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

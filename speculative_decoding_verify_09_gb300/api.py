@@ -35,10 +35,13 @@ def _stream(stream):
 
 
 def attn_args(q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, *, max_q_rows,
-              kv_rows_bound, scale=0.0, dev_status=None):
+              kv_rows_bound, scale=0.0, dev_status=None, group=None, prefix_start=None,
+              prefix_len=None, prefix_rows_bound=0):
     """sv_attn_args for q [R, Hq, D], k_new / v_new [R, Hkv, D], caches
     [P, Hkv, D], cu_q [B+1] int32, kv_start [B] int64, kv_len [B] int32,
-    out [R, Hq, D]; max_q_rows / kv_rows_bound are host bounds."""
+    out [R, Hq, D]; max_q_rows / kv_rows_bound are host bounds.  Shared
+    prefixes: group [B] int32 (non-decreasing), prefix_start [G] int64,
+    prefix_len [G] int32 and the host bound prefix_rows_bound."""
     a = AttnArgs()
     R, Hq, D = q.shape
     a.batch = cu_q.shape[0] - 1
@@ -49,13 +52,15 @@ def attn_args(q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, *,
     a.kv_rows_bound = int(kv_rows_bound)
     a.pool_rows = k_cache.shape[0]
     a.scale = float(scale)
-    a.num_groups = 0
-    a.prefix_rows_bound = 0
+    a.num_groups = 0 if group is None else prefix_len.shape[0]
+    a.prefix_rows_bound = int(prefix_rows_bound)
     a.cu_q, a.q, a.k_new, a.v_new = _ptr(cu_q), _ptr(q), _ptr(k_new), _ptr(v_new)
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
     a.kv_start, a.kv_len, a.out = _ptr(kv_start), _ptr(kv_len), _ptr(out)
     a.dev_status = _ptr(dev_status)
-    a._keep = (q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, dev_status)
+    a.group, a.prefix_start, a.prefix_len = _ptr(group), _ptr(prefix_start), _ptr(prefix_len)
+    a._keep = (q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, dev_status,
+               group, prefix_start, prefix_len)
     return a
 
 

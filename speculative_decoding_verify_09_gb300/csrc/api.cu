@@ -28,7 +28,6 @@ sv_status cuda_fail(cudaError_t e, const char *what) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int64_t kMaxGrid = 2048;   // bound on persistent attention CTAs
 constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -59,8 +58,17 @@ sv_status check_attn(const sv_attn_args *a) {
     return fail(SV_ERR_INVALID, "attention: negative kv_rows_bound or pool_rows");
   if (!std::isfinite(a->scale) || a->scale < 0.0f)
     return fail(SV_ERR_INVALID, "attention: scale must be finite and >= 0");
-  if (a->num_groups != 0)
-    return fail(SV_ERR_UNSUPPORTED, "attention: shared-prefix groups not built in this library");
+  if (a->num_groups < 0 || a->num_groups > sv::attention_max_groups())
+    return fail(SV_ERR_INVALID, "attention: num_groups %d outside [0, %d]", a->num_groups,
+                sv::attention_max_groups());
+  if (a->num_groups > 0) {
+    if (a->dtype != SV_BF16)
+      return fail(SV_ERR_UNSUPPORTED, "attention: shared prefix built for bf16 only");
+    if (a->prefix_rows_bound < 0)
+      return fail(SV_ERR_INVALID, "attention: negative prefix_rows_bound");
+    if (a->batch > 0 && (!a->group || !a->prefix_start || !a->prefix_len))
+      return fail(SV_ERR_INVALID, "attention: null shared-prefix pointer");
+  }
   if (a->batch > 0) {
     if (!a->cu_q || !a->q || !a->k_new || !a->v_new || !a->kv_start || !a->kv_len || !a->out)
       return fail(SV_ERR_INVALID, "attention: null device pointer");
@@ -101,8 +109,10 @@ sv_status check_sample(const sv_sample_args *a) {
 }
 
 struct Layout {
-  size_t cnt_attn, cnt_samp, stats, part_o, part_ml, total;
+  size_t cnt_attn, row_cnt, seq_cnt1, seq_cnt2, stats, parts, draw_parts;
+  size_t part_o, part_ml, pre_o, pre_ml, total;
   sv::AttnPlan plan;
+  sv::SamplerPlan splan;
 };
 
 // Workspace: [attention counters | sampler counters | row stats | partials].
@@ -115,23 +125,36 @@ Layout layout(const sv_attn_args *a, const sv_sample_args *s) {
     off += round_up(static_cast<size_t>(a->batch) * a->num_kv_heads * 4);
   }
   if (s) {
-    L.cnt_samp = off;
+    const size_t rows = static_cast<size_t>(2 * s->num_rows - s->batch);
+    L.splan = sv::plan_sampler(*s);
+    L.row_cnt = off;                      // counters first: zeroed once, left zero
+    off += round_up(rows * 4);
+    L.seq_cnt1 = off;
+    off += round_up(static_cast<size_t>(s->batch) * 4);
+    L.seq_cnt2 = off;
     off += round_up(static_cast<size_t>(s->batch) * 4);
     L.stats = off;
-    off += round_up(sv::sampler_stats_bytes(*s));
+    off += round_up(rows * sizeof(sv::RowStats));
+    L.parts = off;
+    off += round_up(rows * L.splan.stat_chunks * sizeof(sv::ChunkPart));
+    L.draw_parts = off;
+    off += round_up(static_cast<size_t>(s->batch) * L.splan.draw_chunks * 8);
   }
   if (a) {
-    // size the partials for the largest grid any device could get
-    sv_attn_args tmp = *a;
-    L.plan = sv::plan_attention(tmp, 0);
-    L.plan.grid = std::min<int64_t>(L.plan.tiles_bound, kMaxGrid);
-    const int64_t slots = (a->dtype == SV_BF16 ? L.plan.grid : 0) +
-                          static_cast<int64_t>(a->batch) * a->num_kv_heads;
-    const int64_t rows = static_cast<int64_t>(L.plan.m_tiles) * 16;
+    // size the partials for the largest grids any device could get
+    L.plan = sv::plan_attention(*a, 0);
+    const bool bf = a->dtype == SV_BF16;
+    const int64_t slots = L.plan.grid + static_cast<int64_t>(a->batch) * a->num_kv_heads;
+    const int64_t rows = sv::attention_slot_rows(L.plan);
     L.part_o = off;
-    off += round_up(a->dtype == SV_BF16 ? static_cast<size_t>(slots * rows * a->head_dim * 4) : 0);
+    off += round_up(bf ? static_cast<size_t>(slots * rows * a->head_dim * 4) : 0);
     L.part_ml = off;
-    off += round_up(a->dtype == SV_BF16 ? static_cast<size_t>(slots * rows * 8) : 0);
+    off += round_up(bf ? static_cast<size_t>(slots * rows * 8) : 0);
+    const int64_t prows = sv::attention_prefix_rows();
+    L.pre_o = off;
+    off += round_up(L.plan.prefix ? static_cast<size_t>(L.plan.pre_slots * prows * a->head_dim * 4) : 0);
+    L.pre_ml = off;
+    off += round_up(L.plan.prefix ? static_cast<size_t>(L.plan.pre_slots * prows * 8) : 0);
   }
   L.total = off;
   return L;
@@ -166,15 +189,31 @@ T *at(void *ws, size_t off) {
 sv_status run_attention(const sv_attn_args *a, const Layout &L, void *ws, bool pdl,
                         cudaStream_t s) {
   if (a->batch == 0) return SV_OK;
-  sv::AttnPlan plan = L.plan;
   const int sms = num_sms_current();
   if (sms <= 0) return fail(SV_ERR_CUDA, "no CUDA device");
-  sv::AttnPlan live = sv::plan_attention(*a, sms);
-  plan.grid = std::min<int64_t>(live.grid, L.plan.grid);
-  cudaError_t e = sv::launch_attention(*a, plan, at<float>(ws, L.part_o), at<float>(ws, L.part_ml),
-                                       at<uint32_t>(ws, L.cnt_attn), pdl, s);
+  sv::AttnPlan plan = sv::plan_attention(*a, sms);   // grids never exceed the sized ones
+  sv::AttnWs w;
+  w.counters = at<uint32_t>(ws, L.cnt_attn);
+  w.dec_o = at<float>(ws, L.part_o);
+  w.dec_ml = at<float>(ws, L.part_ml);
+  w.pre_o = at<float>(ws, L.pre_o);
+  w.pre_ml = at<float>(ws, L.pre_ml);
+  cudaError_t e = sv::launch_attention(*a, plan, w, pdl, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
+}
+
+sv::SamplerLaunch sampler_launch(const sv_sample_args *sample, const Layout &L, void *ws) {
+  sv::SamplerLaunch SL{};
+  SL.a = *sample;
+  SL.plan = L.splan;
+  SL.ws.stats = at<sv::RowStats>(ws, L.stats);
+  SL.ws.row_cnt = at<uint32_t>(ws, L.row_cnt);
+  SL.ws.seq_cnt1 = at<uint32_t>(ws, L.seq_cnt1);
+  SL.ws.seq_cnt2 = at<uint32_t>(ws, L.seq_cnt2);
+  SL.ws.parts = at<sv::ChunkPart>(ws, L.parts);
+  SL.ws.draw_parts = at<unsigned long long>(ws, L.draw_parts);
+  return SL;
 }
 
 }  // namespace
@@ -212,10 +251,7 @@ SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size
   const Layout L = layout(nullptr, sample);
   if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
   if (sample->batch == 0) return SV_OK;
-  sv::SamplerLaunch SL{};
-  SL.a = *sample;
-  SL.stats = at<sv::RowStats>(ws, L.stats);
-  SL.counters = at<uint32_t>(ws, L.cnt_samp);
+  sv::SamplerLaunch SL = sampler_launch(sample, L, ws);
   SL.do_append = false;
   SL.pdl_primary = false;
   cudaError_t e = sv::launch_sampler(SL, static_cast<cudaStream_t>(stream));
@@ -278,10 +314,7 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Sampling (with the append of accepted rows) is the primary launch; the
   // attention launch may start while it runs and waits for it before exiting.
-  sv::SamplerLaunch SL{};
-  SL.a = *sample;
-  SL.stats = at<sv::RowStats>(ws, L.stats);
-  SL.counters = at<uint32_t>(ws, L.cnt_samp);
+  sv::SamplerLaunch SL = sampler_launch(sample, L, ws);
   SL.do_append = true;
   SL.pdl_primary = true;
   const int esz = attn->dtype == SV_F32 ? 4 : 2;

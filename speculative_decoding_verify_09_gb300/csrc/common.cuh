@@ -121,6 +121,62 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan_u64(
   return base + inc - v;
 }
 
+// ---------------------------------------------------------------- float-float sums
+// Unevaluated sum hi + lo of two floats (about 48 significant bits), added with
+// Knuth's two-sum.  Used for block reductions instead of fp64, which runs at a
+// small fraction of the fp32 rate on this GPU.
+struct FF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_make(float x) { return FF{x, 0.0f}; }
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bv = __fsub_rn(s, a.hi);
+  const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bv)), __fsub_rn(b.hi, bv));
+  const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
+  const float hi = __fadd_rn(s, lo);
+  return FF{hi, __fsub_rn(lo, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF t;
+    t.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+    t.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+    v = ff_add(v, t);
+  }
+  return v;
+}
+
+// a >= b for normalized float-float values.
+__device__ __forceinline__ bool ff_ge(FF a, FF b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo >= b.lo);
+}
+
+__device__ __forceinline__ FF ff_from_double(double x) {
+  const float hi = static_cast<float>(x);
+  return FF{hi, static_cast<float>(x - static_cast<double>(hi))};
+}
+
+__device__ __forceinline__ double ff_to_double(FF a) {
+  return static_cast<double>(a.hi) + static_cast<double>(a.lo);
+}
+
+// floor(r * 2^52) for a float r in [0, 2), computed with integer operations
+// only (exact: the float's 24-bit significand shifted into place).
+__device__ __forceinline__ unsigned long long fix52(float r) {
+  const uint32_t b = __float_as_uint(r);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;                                   // zero / subnormal (< 2^-126)
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;  // value = m * 2^(e - 150)
+  const int sh = e - 98;                                     // * 2^52
+  if (sh >= 0) return m << sh;
+  return -sh < 32 ? (m >> (-sh)) : 0ull;
+}
+
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -158,6 +214,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one 32-bit pair per lane (row lane/4,
+// columns 2*(lane%4) and +1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

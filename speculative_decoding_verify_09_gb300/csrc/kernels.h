@@ -12,13 +12,38 @@ namespace sv {
 constexpr int kMaxQRows = 16;   // bound on K_i + 1 block rows per sequence
 constexpr int kMaxRowsM = 64;   // bound on (K_i + 1) * (Hq / Hkv) packed query rows
 
-// Per logits row statistics written by the sampler's row pass.
+// Per logits row statistics written by the sampler's first phase.
 struct RowStats {
   float lmax;         // largest logit of the row
   uint32_t tau_key;   // nucleus threshold as an order-preserving key (0: keep all)
   uint32_t valid;     // 0: NaN / +inf / only -inf in the row
+  float inv_hi;       // 1 / ssum as a float-float pair
+  float inv_lo;
   uint32_t pad;
   double ssum;        // sum over the kept set of exp((l - lmax) / T)
+};
+
+// Partial (max, sum) of one chunk of a row (chunked statistics).
+struct ChunkPart {
+  float m;            // chunk max
+  float s_hi, s_lo;   // sum of exp((l - m) / T) over the chunk, float-float
+  uint32_t bad;       // NaN / +inf seen
+};
+
+// Sampler workspace regions (device pointers).
+struct SamplerWs {
+  RowStats *stats;          // [2R - B]
+  uint32_t *row_cnt;        // [2R - B] chunk arrivals per row (zero between calls)
+  uint32_t *seq_cnt1;       // [B] row arrivals per sequence (zero between calls)
+  uint32_t *seq_cnt2;       // [B] draw-chunk arrivals per sequence (zero between calls)
+  ChunkPart *parts;         // [(2R - B) * stat_chunks]
+  unsigned long long *draw_parts;   // [B * draw_chunks]
+};
+
+struct SamplerPlan {
+  int stat_chunks;          // CTAs per row in the statistics phase (1: nucleus path)
+  int draw_chunks;          // CTAs per sequence in the draw phase
+  bool cluster;             // one CTA cluster per sequence (no nucleus, rows fit in smem)
 };
 
 struct AppendView {   // what the fused step's append needs (all device pointers)
@@ -33,15 +58,14 @@ struct AppendView {   // what the fused step's append needs (all device pointers
 
 struct SamplerLaunch {
   sv_sample_args a;
-  RowStats *stats;          // [2R - B]
-  uint32_t *counters;       // [B], zero between calls
+  SamplerWs ws;
+  SamplerPlan plan;
   bool do_append;
   AppendView app;
   bool pdl_primary;         // trigger dependent launch at kernel start
 };
 
-// Sizes of the sampler's workspace parts.
-size_t sampler_stats_bytes(const sv_sample_args &a);
+SamplerPlan plan_sampler(const sv_sample_args &a);
 int sampler_max_vocab(int dtype);
 cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s);
 
@@ -55,16 +79,30 @@ cudaError_t launch_append(int32_t B, int32_t row_bytes, int32_t max_q_rows, int6
 // Attention split plan: chosen on the host from the bounds.
 struct AttnPlan {
   int rows_m;           // packed query rows per (sequence, KV head): max_q_rows * Hq/Hkv
-  int m_tiles;          // ceil(rows_m / 16)
+  int row_cfg;          // kernel row configuration (rows per CTA: 8, 16, 32, 48, 64)
+  int m_tiles;          // partial-slot rows / 16
   int64_t grid;         // persistent CTAs (bf16 path)
   int64_t tiles_bound;  // bound on the global count of 64-key tiles
+  // shared-prefix arrangement (num_groups > 0)
+  bool prefix;
+  int spb;              // whole sequences per prefix row-block
+  int64_t pre_grid, pre_tiles_bound, pre_slots;
 };
 
+// Device regions of the attention workspace.
+struct AttnWs {
+  uint32_t *counters;   // [B * Hkv]
+  float *dec_o, *dec_ml;      // decode partials
+  float *pre_o, *pre_ml;      // prefix partials
+};
+
+// num_sms = 0: device-independent plan (grids at their upper bound).
 AttnPlan plan_attention(const sv_attn_args &a, int num_sms);
-size_t attention_partials_bytes(const sv_attn_args &a, const AttnPlan &p);
 int attention_max_batch();
-cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, float *part_o,
-                             float *part_ml, uint32_t *counters, bool pdl_secondary,
-                             cudaStream_t s);
+int attention_max_groups();
+int attention_slot_rows(const AttnPlan &p);   // rows per decode partial slot
+int attention_prefix_rows();                  // rows per prefix partial slot
+cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const AttnWs &ws,
+                             bool pdl_secondary, cudaStream_t s);
 
 }  // namespace sv

@@ -19,6 +19,8 @@
 // fp64 across threads; the accept test is evaluated in fp64; the inverse-CDF
 // draw accumulates exact 64-bit fixed-point values (2^-52 units), so the
 // chosen index does not depend on the summation order.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,7 +32,6 @@ constexpr int kSampNT = 512;          // threads per sampler CTA
 constexpr int kSampNW = kSampNT / 32;
 constexpr int kMaxTiles = 64;         // vectors per thread per row (bounds V)
 constexpr int kCandCap = 4096;        // nucleus candidates held in shared memory
-constexpr float kFix = 4503599627370496.0f;  // 2^52
 
 template <typename T> struct LT;
 template <> struct LT<float> {
@@ -39,6 +40,7 @@ template <> struct LT<float> {
   static constexpr uint32_t NEG_INF_BITS = 0xFF800000u;
   __device__ static float val(uint32_t b) { return __uint_as_float(b); }
   __device__ static uint32_t key(uint32_t b) { return key_of_f32(b); }
+  __device__ static uint32_t bits(float x) { return __float_as_uint(x); }
 };
 template <> struct LT<uint16_t> {
   static constexpr int EPV = 8;
@@ -46,31 +48,133 @@ template <> struct LT<uint16_t> {
   static constexpr uint32_t NEG_INF_BITS = 0xFF80u;
   __device__ static float val(uint32_t b) { return bf16_bits_to_f32(b); }
   __device__ static uint32_t key(uint32_t b) { return key_of_bf16(b); }
+  __device__ static uint32_t bits(uint16_t x) { return x; }
 };
 
-// Raw bits of the EPV elements of vector v (elements v*EPV ..); past-the-end
-// elements read as -inf (weight 0, lowest key).
+// One 16-byte vector v (elements v*EPV ..) of a row as raw bits; elements past
+// V read as -inf (weight 0, lowest key).  Unaligned rows use scalar loads.
+template <typename T>
+__device__ __forceinline__ uint4 load_vec(const T *row, int V, int v, bool aligned) {
+  constexpr int EPV = LT<T>::EPV;
+  const int e0 = v * EPV;
+  if (aligned && e0 + EPV <= V) return __ldg(reinterpret_cast<const uint4 *>(row + e0));
+  uint32_t b[EPV];
+#pragma unroll
+  for (int i = 0; i < EPV; ++i)
+    b[i] = (e0 + i < V) ? LT<T>::bits(__ldg(row + e0 + i)) : LT<T>::NEG_INF_BITS;
+  if constexpr (EPV == 4) {
+    return make_uint4(b[0], b[1], b[2], b[3]);
+  } else {
+    return make_uint4(b[0] | (b[1] << 16), b[2] | (b[3] << 16), b[4] | (b[5] << 16),
+                      b[6] | (b[7] << 16));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 raw, uint32_t (&b)[LT<T>::EPV]) {
+  if constexpr (LT<T>::EPV == 4) {
+    b[0] = raw.x; b[1] = raw.y; b[2] = raw.z; b[3] = raw.w;
+  } else {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      b[2 * i] = w[i] & 0xFFFFu;
+      b[2 * i + 1] = w[i] >> 16;
+    }
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void load_bits(const T *row, int V, int v, bool aligned,
                                           uint32_t (&b)[LT<T>::EPV]) {
-  constexpr int EPV = LT<T>::EPV;
-  const int e0 = v * EPV;
-  if (aligned && e0 + EPV <= V) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(row + e0));
-    if constexpr (EPV == 4) {
-      b[0] = raw.x; b[1] = raw.y; b[2] = raw.z; b[3] = raw.w;
+  unpack<T>(load_vec<T>(row, V, v, aligned), b);
+}
+
+constexpr int kRowSmemBytes = 64 * 1024;  // a row up to this size is cached in smem
+constexpr int kStream = 4;                 // vectors per thread loaded together when streaming
+constexpr int kDrawBatch = 4;              // vectors per thread loaded together by the draw
+
+// A logits row as seen by one CTA: vector v = k * kSampNT + tid for k = 0..
+// A row of at most kRowSmemBytes is copied once from HBM into shared memory
+// (cp.async, all copies in flight together) and every pass reads it there;
+// a longer row is streamed from L2 on every pass in unrolled batches.
+template <typename T>
+struct RowPass {
+  const T *row;
+  const uint4 *srow;   // shared-memory copy (cached rows)
+  int V, NV;
+  bool aligned, cached;
+
+  __device__ __forceinline__ void init(const T *r, int v_, uint4 *smem_row) {
+    row = r;
+    V = v_;
+    NV = (V + LT<T>::EPV - 1) / LT<T>::EPV;
+    aligned = (reinterpret_cast<uintptr_t>(r) & 15) == 0;
+    cached = NV * 16 <= kRowSmemBytes;
+    srow = smem_row;
+    if (cached) {
+      for (int v = threadIdx.x; v < NV; v += kSampNT) {
+        if (aligned && (v + 1) * LT<T>::EPV <= V)
+          cp_async16(smem_u32(smem_row + v), row + v * LT<T>::EPV, 16);
+        else
+          smem_row[v] = load_vec<T>(row, V, v, aligned);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+    }
+  }
+
+  // f(bits[EPV]) for every vector this thread owns, in increasing v.
+  template <typename F>
+  __device__ __forceinline__ void each(F &&f) const {
+    constexpr int EPV = LT<T>::EPV;
+    if (cached) {
+      for (int v = threadIdx.x; v < NV; v += kSampNT) {
+        uint32_t b[EPV];
+        unpack<T>(srow[v], b);
+        f(b);
+      }
     } else {
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int base = 0; base < NV; base += kStream * kSampNT) {
+        uint4 tmp[kStream];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        b[2 * i] = w[i] & 0xFFFFu;
-        b[2 * i + 1] = w[i] >> 16;
+        for (int k = 0; k < kStream; ++k) {
+          const int v = base + k * kSampNT + threadIdx.x;
+          if (v < NV) tmp[k] = load_vec<T>(row, V, v, aligned);
+        }
+#pragma unroll
+        for (int k = 0; k < kStream; ++k) {
+          if (base + k * kSampNT + static_cast<int>(threadIdx.x) < NV) {
+            uint32_t b[EPV];
+            unpack<T>(tmp[k], b);
+            f(b);
+          }
+        }
       }
     }
-  } else {
+  }
+};
+
+// Block-wide float-float sums of N values per thread in one pass: every
+// thread adds the per-warp partials in the same order, so all get the same
+// result (one barrier; `red` must not be reused before the next barrier).
+template <int N>
+__device__ __forceinline__ void block_sum_ff(FF (&v)[N], FF *red) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < EPV; ++i)
-      b[i] = (e0 + i < V) ? static_cast<uint32_t>(__ldg(row + e0 + i)) : LT<T>::NEG_INF_BITS;
+  for (int k = 0; k < N; ++k) v[k] = warp_sum_ff(v[k]);
+  if (l == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) red[k * kSampNW + w] = v[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    FF t = red[k * kSampNW];
+#pragma unroll
+    for (int i = 1; i < kSampNW; ++i) t = ff_add(t, red[k * kSampNW + i]);
+    v[k] = t;
   }
 }
 
@@ -87,26 +191,24 @@ struct WeightFn {
 
 struct SampParams {
   sv_sample_args a;
-  RowStats *stats;
-  uint32_t *counters;
+  SamplerWs ws;
+  SamplerPlan plan;
   int do_append;
   AppendView app;
   float c_hi, c_lo;   // log2(e)/T as two floats
-  double inv_T;
   int pdl_primary;
 };
 
 struct SampSmem {
-  double red[32];
+  FF red[2][8 * kSampNW];     // double-buffered float-float partials
   float redf[32];
   unsigned long long red64[32];
-  unsigned long long wsum[kMaxTiles][kSampNW];
-  unsigned long long tile_tot[kMaxTiles];
-  unsigned long long bcast64[4];
   int bcast[8];
   uint32_t cand_key[kCandCap];
   float cand_w[kCandCap];
 };
+
+constexpr size_t kSmemRowOff = (sizeof(SampSmem) + 127) / 128 * 128;
 
 // Validity of sequence i's row bookkeeping against the host bounds.
 __device__ __forceinline__ bool seq_rows_ok(const sv_sample_args &a, int i) {
@@ -142,108 +244,119 @@ __device__ __forceinline__ int seq_of_draft_row(const int32_t *cu_q, int B, int 
 // many, over the whole row).
 // --------------------------------------------------------------------------
 template <typename T>
-__device__ void nucleus_cut(const T *row, int V, bool aligned, const WeightFn &wf, double S,
-                            float top_p, SampSmem &sm, uint32_t &tau_out, double &ssum_out) {
+__device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, float top_p,
+                            SampSmem &sm, uint32_t &tau_out, double &ssum_out) {
   constexpr int EPV = LT<T>::EPV;
-  const int NV = (V + EPV - 1) / EPV;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   const double target = static_cast<double>(top_p) * S;
 
   // coarse bins: bin b = min((127 - biased_exp(w)) / 4, 7)
   float acc[8];
 #pragma unroll
   for (int b = 0; b < 8; ++b) acc[b] = 0.0f;
-  for (int v = tid; v < NV; v += kSampNT) {
-    uint32_t bits[EPV];
-    load_bits<T>(row, V, v, aligned, bits);
+  rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
-      const float w = wf(LT<T>::val(bits[e]));
-      const int ex = 127 - static_cast<int>((__float_as_uint(w) >> 23) & 0xFFu);
+      const float x = wf(LT<T>::val(bits[e]));
+      const int ex = 127 - static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);
       const int b = min(max(ex, 0) >> 2, 7);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] += (b == k) ? w : 0.0f;
+      for (int k = 0; k < 8; ++k) acc[k] += (b == k) ? x : 0.0f;
     }
-  }
-  double cum = 0.0;
+  });
+  FF bins[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) bins[k] = ff_make(acc[k]);
+  block_sum_ff<8>(bins, sm.red[0]);
+  const FF tgt_safe = ff_from_double(target * (1.0 + 1e-5));
+  FF cum = ff_make(0.0f);
   int kb = 7;
-  for (int k = 0; k < 8; ++k) {
-    cum += block_sum_d<kSampNT>(static_cast<double>(acc[k]), sm.red);
-    if (kb == 7 && k < 7 && cum >= target * (1.0 + 1e-5)) kb = k;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    cum = ff_add(cum, bins[k]);
+    if (kb == 7 && ff_ge(cum, tgt_safe)) kb = k;
   }
-  // candidates: bin <= kb (all elements when kb == 7)
-  auto is_cand = [&](float w) {
+  // candidates: bin <= kb (every element when kb == 7)
+  auto is_cand = [&](float x) {
     if (kb == 7) return true;
-    const int ex = 127 - static_cast<int>((__float_as_uint(w) >> 23) & 0xFFu);
+    const int ex = 127 - static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);
     return (max(ex, 0) >> 2) <= kb;
   };
   int mine = 0;
-  for (int v = tid; v < NV; v += kSampNT) {
-    uint32_t bits[EPV];
-    load_bits<T>(row, V, v, aligned, bits);
+  rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) mine += is_cand(wf(LT<T>::val(bits[e]))) ? 1 : 0;
-  }
+  });
   unsigned long long total = 0;
   const unsigned long long off =
       block_exclusive_scan_u64<kSampNT>(static_cast<unsigned long long>(mine), sm.red64, &total);
   const bool in_smem = total <= static_cast<unsigned long long>(kCandCap);
   if (in_smem) {
     int o = static_cast<int>(off);
-    for (int v = tid; v < NV; v += kSampNT) {
-      uint32_t bits[EPV];
-      load_bits<T>(row, V, v, aligned, bits);
+    rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float w = wf(LT<T>::val(bits[e]));
-        if (is_cand(w)) {
+        const float x = wf(LT<T>::val(bits[e]));
+        if (is_cand(x)) {
           sm.cand_key[o] = LT<T>::key(bits[e]);
-          sm.cand_w[o] = w;
+          sm.cand_w[o] = x;
           ++o;
         }
       }
-    }
+    });
   }
   __syncthreads();
   const int C = static_cast<int>(total);
-  // partial weight of {key >= cand} held by this thread
+  // this thread's part of the weight of {key >= cand}
   auto partial = [&](uint32_t cand) {
-    float s = 0.0f;
+    float sum = 0.0f;
     if (in_smem) {
       for (int c = tid; c < C; c += kSampNT)
-        if (sm.cand_key[c] >= cand) s += sm.cand_w[c];
+        if (sm.cand_key[c] >= cand) sum += sm.cand_w[c];
     } else {
-      for (int v = tid; v < NV; v += kSampNT) {
-        uint32_t bits[EPV];
-        load_bits<T>(row, V, v, aligned, bits);
+      rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
-          if (LT<T>::key(bits[e]) >= cand) s += wf(LT<T>::val(bits[e]));
-      }
+          if (LT<T>::key(bits[e]) >= cand) sum += wf(LT<T>::val(bits[e]));
+      });
     }
-    return s;
+    return sum;
   };
+  // bitwise search, one barrier per bit (double-buffered partial sums)
+  const FF tgt = ff_from_double(target);
   uint32_t tau = 0;
+  int buf = 1;
   for (int bit = LT<T>::KEY_BITS - 1; bit >= 0; --bit) {
     const uint32_t cand = tau | (1u << bit);
-    const double W = block_sum_d<kSampNT>(static_cast<double>(partial(cand)), sm.red);
-    if (W >= target) tau = cand;
+    FF W[1] = {ff_make(partial(cand))};
+    block_sum_ff<1>(W, sm.red[buf]);
+    if (ff_ge(W[0], tgt)) tau = cand;
+    buf ^= 1;
   }
-  ssum_out = block_sum_d<kSampNT>(static_cast<double>(partial(tau)), sm.red);
+  FF ss[1] = {ff_make(partial(tau))};
+  block_sum_ff<1>(ss, sm.red[buf]);
+  ssum_out = ff_to_double(ss[0]);
   tau_out = tau;
 }
 
 // --------------------------------------------------------------------------
-// Inverse-CDF draw over one vocabulary row (block-wide).  mode 0: residual
-// max(0, q_hat - p_hat) of (trow, drow); mode 1: q_hat of trow.  Returns the
-// first index x with C(x) * 2^24 > k * Z (C, Z in 2^-52 fixed point), or -1
-// when Z == 0.
+// Probabilities.  q_hat(l) = [key(l) >= tau] * w(l) / S with w(l) = exp((l -
+// lmax)/T) in fp32 and 1/S held as a float-float pair (no per-thread fp64).
 // --------------------------------------------------------------------------
-struct RowProb {      // q_hat(l) = [key(l) >= tau] * w(l) / S, w(l) = exp((l-lmax)/T)
+struct RowProb {
   WeightFn wf;
   uint32_t tau;
-  float inv_hi, inv_lo;  // 1/S as two floats
+  float inv_hi, inv_lo;
 };
+
+__device__ __forceinline__ RowProb rowprob_of(const RowStats *st, float c_hi, float c_lo) {
+  RowProb r;
+  r.wf = WeightFn{__ldcg(&st->lmax), c_hi, c_lo};
+  r.tau = __ldcg(&st->tau_key);
+  r.inv_hi = __ldcg(&st->inv_hi);
+  r.inv_lo = __ldcg(&st->inv_lo);
+  return r;
+}
 
 template <typename T>
 __device__ __forceinline__ float row_prob(const RowProb &rp, uint32_t bits) {
@@ -252,292 +365,300 @@ __device__ __forceinline__ float row_prob(const RowProb &rp, uint32_t bits) {
   return __fmaf_rn(w, rp.inv_hi, __fmul_rn(w, rp.inv_lo));
 }
 
+// Fixed-point (2^-52) draw weight of one vector: mode 0 the residual
+// max(0, q_hat - p_hat), mode 1 q_hat.  Element e of the vector is `e`.
 template <typename T>
-__device__ __forceinline__ unsigned long long vec_fix_sum(const T *trow, const T *drow, int V,
-                                                          bool al_t, bool al_d, int v,
-                                                          const RowProb &pq, const RowProb &pp,
-                                                          int mode) {
-  constexpr int EPV = LT<T>::EPV;
-  uint32_t bq[EPV], bp[EPV];
-  load_bits<T>(trow, V, v, al_t, bq);
-  if (mode == 0) load_bits<T>(drow, V, v, al_d, bp);
-  unsigned long long s = 0;
-#pragma unroll
-  for (int e = 0; e < EPV; ++e) {
-    float r = row_prob<T>(pq, bq[e]);
-    if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp[e])), 0.0f);
-    s += __float2ull_rz(__fmul_rn(r, kFix));
-  }
-  return s;
+__device__ __forceinline__ unsigned long long fix_weight(const RowProb &pq, const RowProb &pp,
+                                                         int mode, uint32_t bq, uint32_t bp) {
+  float r = row_prob<T>(pq, bq);
+  if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp)), 0.0f);
+  return fix52(r);
 }
 
-template <typename T>
-__device__ int block_draw(const T *trow, const T *drow, int V, const RowProb &pq,
-                          const RowProb &pp, int mode, uint32_t k24, SampSmem &sm) {
-  constexpr int EPV = LT<T>::EPV;
-  const int NV = (V + EPV - 1) / EPV;
-  const int NK = (NV + kSampNT - 1) / kSampNT;
-  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-  const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
-  const bool al_d = mode == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
-  for (int k = 0; k < NK; ++k) {
-    const int v = k * kSampNT + tid;
-    unsigned long long s = v < NV ? vec_fix_sum<T>(trow, drow, V, al_t, al_d, v, pq, pp, mode) : 0;
-    s = warp_sum_u64(s);
-    if (l == 0) sm.wsum[k][w] = s;
-  }
-  __syncthreads();
-  if (tid < NK) {
-    unsigned long long t = 0;
-    for (int i = 0; i < kSampNW; ++i) t += sm.wsum[tid][i];
-    sm.tile_tot[tid] = t;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long Z = 0;
-    for (int k = 0; k < NK; ++k) Z += sm.tile_tot[k];
-    int kstar = -1;
-    unsigned long long tgt = 0, base = 0;
-    if (Z > 0) {
-      const unsigned long long ku = k24;
-      const unsigned long long lo = ku * Z, hi = __umul64hi(ku, Z);
-      tgt = (hi << 40) | (lo >> 24);            // floor(k * Z / 2^24) < Z
-      unsigned long long cum = 0;
-      for (int k = 0; k < NK; ++k) {
-        if (tgt < cum + sm.tile_tot[k]) { kstar = k; base = cum; break; }
-        cum += sm.tile_tot[k];
-      }
-    }
-    sm.bcast[0] = kstar;
-    sm.bcast[1] = -1;
-    sm.bcast64[0] = tgt;
-    sm.bcast64[1] = base;
-  }
-  __syncthreads();
-  const int kstar = sm.bcast[0];
-  if (kstar < 0) return -1;
-  const unsigned long long tgt = sm.bcast64[0], base = sm.bcast64[1];
-  const int v = kstar * kSampNT + tid;
-  const unsigned long long s = v < NV ? vec_fix_sum<T>(trow, drow, V, al_t, al_d, v, pq, pp, mode) : 0;
-  unsigned long long dummy;
-  const unsigned long long ex = block_exclusive_scan_u64<kSampNT>(s, sm.red64, &dummy);
-  const unsigned long long lo_c = base + ex;
-  if (s > 0 && lo_c <= tgt && tgt < lo_c + s) {
-    // owner: walk the vector element by element with the same arithmetic
-    uint32_t bq[EPV], bp[EPV];
-    load_bits<T>(trow, V, v, al_t, bq);
-    if (mode == 0) load_bits<T>(drow, V, v, al_d, bp);
-    unsigned long long c = lo_c;
-    int x = v * EPV + EPV - 1;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      float r = row_prob<T>(pq, bq[e]);
-      if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp[e])), 0.0f);
-      c += __float2ull_rz(__fmul_rn(r, kFix));
-      if (c > tgt) { x = v * EPV + e; break; }
-    }
-    sm.bcast[1] = x;
-  }
-  __syncthreads();
-  return sm.bcast[1];
-}
-
-__device__ __forceinline__ RowProb make_rowprob(const RowStats &st, float c_hi, float c_lo) {
-  RowProb r;
-  r.wf = WeightFn{st.lmax, c_hi, c_lo};
-  r.tau = st.tau_key;
-  const double inv = 1.0 / st.ssum;
-  r.inv_hi = static_cast<float>(inv);
-  r.inv_lo = static_cast<float>(inv - static_cast<double>(r.inv_hi));
-  return r;
-}
-
-// Copy block rows 0..n of sequence i to pool rows kv_start + L .. (fused step).
-__device__ void append_seq(const SampParams &P, int i, int r0, int n, int L, uint32_t *status) {
-  const AppendView &A = P.app;
-  int32_t new_len = L;
-  const int64_t start = A.kv_start[i];
-  if (L + n + 1 > A.kv_cap[i]) {
-    if (threadIdx.x == 0) set_status(status, SV_DEV_CAPACITY);
-  } else if (start < 0 || start + L + n + 1 > A.pool_rows) {
-    if (threadIdx.x == 0) set_status(status, SV_DEV_BAD_LENGTH);
-  } else {
-    const int64_t nvec = static_cast<int64_t>(n + 1) * A.row_bytes / 16;
-    const uint4 *sk = reinterpret_cast<const uint4 *>(static_cast<const char *>(A.k_new) +
-                                                      static_cast<int64_t>(r0) * A.row_bytes);
-    const uint4 *sv_ = reinterpret_cast<const uint4 *>(static_cast<const char *>(A.v_new) +
-                                                       static_cast<int64_t>(r0) * A.row_bytes);
-    uint4 *dk = reinterpret_cast<uint4 *>(static_cast<char *>(A.k_cache) +
-                                          (start + L) * A.row_bytes);
-    uint4 *dv = reinterpret_cast<uint4 *>(static_cast<char *>(A.v_cache) +
-                                          (start + L) * A.row_bytes);
-    for (int64_t v = threadIdx.x; v < nvec; v += kSampNT) {
-      dk[v] = __ldcg(sk + v);
-      dv[v] = __ldcg(sv_ + v);
-    }
-    new_len = L + n + 1;
-  }
-  if (threadIdx.x == 0) A.new_kv_len[i] = new_len;
+// Finish a row's statistics (one thread): ssum and its float-float inverse.
+__device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t tau, bool valid,
+                                            double ssum) {
+  RowStats o;
+  o.lmax = lmax;
+  o.tau_key = tau;
+  o.valid = valid ? 1u : 0u;
+  const double inv = valid && ssum > 0.0 ? 1.0 / ssum : 0.0;
+  o.inv_hi = static_cast<float>(inv);
+  o.inv_lo = static_cast<float>(inv - static_cast<double>(o.inv_hi));
+  o.pad = 0;
+  o.ssum = ssum;
+  *st = o;
 }
 
 // --------------------------------------------------------------------------
-// Decision for sequence i, run by the last row CTA of i to finish.
+// Accept tests of sequence i (warp 0 of the CTA that completed its rows):
+// lane j tests draft j+1 against target row j and draft row j with the
+// acceptance uniform of token index L_i + j + 1.  Writes num_accepted, the
+// accepted drafts and -1 elsewhere (the drawn token comes in the draw phase).
 // --------------------------------------------------------------------------
 template <typename T>
-__device__ void decide_sequence(const SampParams &P, int i, SampSmem &sm) {
+__device__ void accept_sequence(const SampParams &P, int i) {
   const sv_sample_args &a = P.a;
+  const int lane = threadIdx.x & 31;
   const int V = a.vocab, R = static_cast<int>(a.num_rows);
   const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
   const int L = a.kv_len[i];
-  const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
-  const int tid = threadIdx.x;
-  const T *tgt = static_cast<const T *>(a.target_logits);
-  const T *drf = static_cast<const T *>(a.draft_logits);
-
-  // all rows valid?
+  const RowStats *st = P.ws.stats;
   int ok = 1;
-  if (tid <= K) ok = __ldcg(&P.stats[r0 + tid].valid) != 0;
-  if (tid < K) ok = ok && (__ldcg(&P.stats[R + p0 + tid].valid) != 0);
-  ok = __syncthreads_and(ok);
-  if (!ok || L < 0) {
-    if (tid <= K) a.out_tokens[r0 + tid] = -1;
-    if (tid == 0) {
+  if (lane <= K) ok = __ldcg(&st[r0 + lane].valid) != 0;
+  if (lane < K) ok = ok && (__ldcg(&st[R + p0 + lane].valid) != 0);
+  ok = __all_sync(0xffffffffu, ok) && L >= 0;
+  if (!ok) {
+    if (lane <= K) a.out_tokens[r0 + lane] = -1;
+    if (lane == 0) {
       a.num_accepted[i] = -1;
       set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
-      if (P.do_append) P.app.new_kv_len[i] = L;
     }
     return;
   }
+  const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
   const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
   const uint32_t sid_lo = static_cast<uint32_t>(static_cast<unsigned long long>(sid));
   const uint32_t sid_hi = static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32);
-
-  // accept tests, one lane per draft row (K <= 15)
-  if (tid < 32) {
-    bool rej = false, bad = false;
-    if (tid < K) {
-      const int d = a.draft_tokens[p0 + tid];
-      if (d < 0 || d >= V) {
-        rej = bad = true;
-      } else {
-        RowStats sq, sp;
-        sq.lmax = __ldcg(&P.stats[r0 + tid].lmax);
-        sq.tau_key = __ldcg(&P.stats[r0 + tid].tau_key);
-        sq.ssum = __ldcg(&P.stats[r0 + tid].ssum);
-        sp.lmax = __ldcg(&P.stats[R + p0 + tid].lmax);
-        sp.tau_key = __ldcg(&P.stats[R + p0 + tid].tau_key);
-        sp.ssum = __ldcg(&P.stats[R + p0 + tid].ssum);
-        const uint32_t bq = static_cast<uint32_t>(tgt[static_cast<int64_t>(r0 + tid) * V + d]);
-        const uint32_t bp = static_cast<uint32_t>(drf[static_cast<int64_t>(p0 + tid) * V + d]);
-        const double lq = LT<T>::val(bq), lp = LT<T>::val(bp);
-        const double qh = LT<T>::key(bq) >= sq.tau_key
-                              ? exp((lq - static_cast<double>(sq.lmax)) * P.inv_T) / sq.ssum
-                              : 0.0;
-        const double ph = LT<T>::key(bp) >= sp.tau_key
-                              ? exp((lp - static_cast<double>(sp.lmax)) * P.inv_T) / sp.ssum
-                              : 0.0;
-        const U4 w = philox4x32_10(U4{static_cast<uint32_t>(L + tid + 1), sid_lo, sid_hi, 0u}, k0, k1);
-        const double u = static_cast<double>(u24(w.x)) * 0x1p-24;
-        rej = !(u * ph < qh);
-      }
-    }
-    const unsigned rm = __ballot_sync(0xffffffffu, rej);
-    const unsigned bm = __ballot_sync(0xffffffffu, bad);
-    if (tid == 0) {
-      const int n = rm ? (__ffs(rm) - 1) : K;
-      sm.bcast[2] = n;
-      if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
+  bool rej = false, bad = false;
+  int d = 0;
+  if (lane < K) {
+    d = a.draft_tokens[p0 + lane];
+    if (d < 0 || d >= V) {
+      rej = bad = true;
+    } else {
+      const T *tgt = static_cast<const T *>(a.target_logits);
+      const T *drf = static_cast<const T *>(a.draft_logits);
+      const RowProb pq = rowprob_of(&st[r0 + lane], P.c_hi, P.c_lo);
+      const RowProb pp = rowprob_of(&st[R + p0 + lane], P.c_hi, P.c_lo);
+      const float qh = row_prob<T>(pq, LT<T>::bits(tgt[static_cast<int64_t>(r0 + lane) * V + d]));
+      const float ph = row_prob<T>(pp, LT<T>::bits(drf[static_cast<int64_t>(p0 + lane) * V + d]));
+      const U4 w = philox4x32_10(U4{static_cast<uint32_t>(L + lane + 1), sid_lo, sid_hi, 0u}, k0, k1);
+      const float u = static_cast<float>(u24(w.x)) * 0x1p-24f;          // exact
+      rej = !(__fmul_rn(u, ph) < qh);
     }
   }
-  __syncthreads();
-  const int n = sm.bcast[2];
-
-  // draw at row n: residual (n < K) or bonus (n == K)
-  const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1), sid_lo, sid_hi, 0u}, k0, k1);
-  const uint32_t ks = u24(wv.y);
-  RowStats sq;
-  sq.lmax = __ldcg(&P.stats[r0 + n].lmax);
-  sq.tau_key = __ldcg(&P.stats[r0 + n].tau_key);
-  sq.ssum = __ldcg(&P.stats[r0 + n].ssum);
-  const RowProb pq = make_rowprob(sq, P.c_hi, P.c_lo);
-  const T *trow = tgt + static_cast<int64_t>(r0 + n) * V;
-  int x;
-  if (n < K) {
-    RowStats sp;
-    sp.lmax = __ldcg(&P.stats[R + p0 + n].lmax);
-    sp.tau_key = __ldcg(&P.stats[R + p0 + n].tau_key);
-    sp.ssum = __ldcg(&P.stats[R + p0 + n].ssum);
-    const RowProb pp = make_rowprob(sp, P.c_hi, P.c_lo);
-    x = block_draw<T>(trow, drf + static_cast<int64_t>(p0 + n) * V, V, pq, pp, 0, ks, sm);
-    if (x < 0) {
-      if (tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
-      x = block_draw<T>(trow, trow, V, pq, pq, 1, ks, sm);
-    }
-  } else {
-    x = block_draw<T>(trow, trow, V, pq, pq, 1, ks, sm);
+  const unsigned rm = __ballot_sync(0xffffffffu, rej);
+  const unsigned bm = __ballot_sync(0xffffffffu, bad);
+  const int n = rm ? (__ffs(rm) - 1) : K;
+  if (lane <= K) a.out_tokens[r0 + lane] = lane < n ? d : -1;
+  if (lane == 0) {
+    a.num_accepted[i] = n;
+    if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
   }
-  if (tid <= K) {
-    int tok = -1;
-    if (tid < n) tok = a.draft_tokens[p0 + tid];
-    else if (tid == n) tok = x;
-    a.out_tokens[r0 + tid] = tok;
-  }
-  if (tid == 0) a.num_accepted[i] = n;
-  if (P.do_append) append_seq(P, i, r0, n, L, a.dev_status);
 }
 
+// The CTA that finished the last row of sequence i runs its accept tests.
 template <typename T>
-__global__ void __launch_bounds__(kSampNT) sampler_kernel(const SampParams P) {
-  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SampSmem &sm = *reinterpret_cast<SampSmem *>(smem_raw);
-  const sv_sample_args &a = P.a;
-  const int V = a.vocab, R = static_cast<int>(a.num_rows), B = a.batch;
-  const int r = blockIdx.x;
-  const int tid = threadIdx.x;
-
-  int i;
-  const T *row;
-  if (r < R) {
-    i = seq_of_target_row(a.cu_q, B, r);
-    row = static_cast<const T *>(a.target_logits) + static_cast<int64_t>(r) * V;
-  } else {
-    i = seq_of_draft_row(a.cu_q, B, r - R);
-    row = static_cast<const T *>(a.draft_logits) + static_cast<int64_t>(r - R) * V;
+__device__ __forceinline__ void arrive_sequence(const SampParams &P, int i, int *flag) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int nrows = 2 * (P.a.cu_q[i + 1] - P.a.cu_q[i]) - 1;
+    const unsigned old = atomicInc(&P.ws.seq_cnt1[i], static_cast<unsigned>(nrows - 1));
+    *flag = old == static_cast<unsigned>(nrows - 1) ? 1 : 0;
   }
+  __syncthreads();
+  if (*flag && threadIdx.x < 32) {
+    __threadfence();
+    accept_sequence<T>(P, i);
+  }
+}
+
+__device__ __forceinline__ int row_seq(const sv_sample_args &a, int r, const void *&base,
+                                       int64_t &row_off) {
+  const int R = static_cast<int>(a.num_rows);
+  if (r < R) {
+    row_off = static_cast<int64_t>(r) * a.vocab;
+    base = a.target_logits;
+    return seq_of_target_row(a.cu_q, a.batch, r);
+  }
+  row_off = static_cast<int64_t>(r - R) * a.vocab;
+  base = a.draft_logits;
+  return seq_of_draft_row(a.cu_q, a.batch, r - R);
+}
+
+// --------------------------------------------------------------------------
+// Phase 1a (no nucleus): CTA (row, chunk) computes the chunk's max and the sum
+// of exp((l - m_chunk)/T); the last chunk of a row merges them, the last row
+// of a sequence runs the accept tests.
+// --------------------------------------------------------------------------
+constexpr int kStatNT = 256;
+constexpr int kStatVec = 4;          // vectors per thread per chunk
+
+template <typename T>
+__global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P) {
+  constexpr int EPV = LT<T>::EPV;
+  constexpr int NW = kStatNT / 32;
+  __shared__ float redf[NW];
+  __shared__ FF redff[NW];
+  __shared__ int flag[2];
+  const sv_sample_args &a = P.a;
+  const int NCH = P.plan.stat_chunks;
+  const int r = blockIdx.x / NCH, c = blockIdx.x - r * NCH;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const void *base;
+  int64_t off;
+  const int i = row_seq(a, r, base, off);
   if (!seq_rows_ok(a, i)) {
     if (tid == 0) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
     return;
   }
-  constexpr int EPV = LT<T>::EPV;
-  const int NV = (V + EPV - 1) / EPV;
+  const T *row = static_cast<const T *>(base) + off;
+  const int V = a.vocab, NV = (V + EPV - 1) / EPV;
+  const int per = (NV + NCH - 1) / NCH;
+  const int v0 = c * per, v1 = min(NV, v0 + per);
   const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-
-  // pass 1: max and finiteness (streams the row from HBM)
+  uint4 vec[kStatVec];
+#pragma unroll
+  for (int k = 0; k < kStatVec; ++k) {
+    const int v = v0 + k * kStatNT + tid;
+    if (v < v1) vec[k] = load_vec<T>(row, V, v, aligned);
+  }
   float mx = -INFINITY;
   int bad = 0;
-  for (int v = tid; v < NV; v += kSampNT) {
-    uint32_t bits[EPV];
-    load_bits<T>(row, V, v, aligned, bits);
+#pragma unroll
+  for (int k = 0; k < kStatVec; ++k) {
+    if (v0 + k * kStatNT + tid < v1) {
+      uint32_t b[EPV];
+      unpack<T>(vec[k], b);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = LT<T>::val(b[e]);
+        bad |= (x != x) || (x == INFINITY);
+        mx = fmaxf(mx, x);
+      }
+    }
+  }
+  // chunks longer than kStatVec * kStatNT vectors stream the rest
+  for (int v = v0 + kStatVec * kStatNT + tid; v < v1; v += kStatNT) {
+    uint32_t b[EPV];
+    load_bits<T>(row, V, v, aligned, b);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const float x = LT<T>::val(b[e]);
+      bad |= (x != x) || (x == INFINITY);
+      mx = fmaxf(mx, x);
+    }
+  }
+  bad = __syncthreads_or(bad);
+  mx = warp_max(mx);
+  if (l == 0) redf[w] = mx;
+  __syncthreads();
+  mx = redf[0];
+#pragma unroll
+  for (int k = 1; k < NW; ++k) mx = fmaxf(mx, redf[k]);
+  // chunk sum of exp((l - mx)/T), Kahan per thread, float-float across threads
+  const WeightFn wf{mx, P.c_hi, P.c_lo};
+  float sum = 0.0f, comp = 0.0f;
+  auto kahan = [&](const uint32_t (&b)[EPV]) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const float y = __fsub_rn(wf(LT<T>::val(b[e])), comp);
+      const float t = __fadd_rn(sum, y);
+      comp = __fsub_rn(__fsub_rn(t, sum), y);
+      sum = t;
+    }
+  };
+  if (mx > -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kStatVec; ++k) {
+      if (v0 + k * kStatNT + tid < v1) {
+        uint32_t b[EPV];
+        unpack<T>(vec[k], b);
+        kahan(b);
+      }
+    }
+    for (int v = v0 + kStatVec * kStatNT + tid; v < v1; v += kStatNT) {
+      uint32_t b[EPV];
+      load_bits<T>(row, V, v, aligned, b);
+      kahan(b);
+    }
+  }
+  FF f = warp_sum_ff(FF{sum, -comp});
+  if (l == 0) redff[w] = f;
+  __syncthreads();
+  if (tid == 0) {
+    FF t = redff[0];
+    for (int k = 1; k < NW; ++k) t = ff_add(t, redff[k]);
+    ChunkPart cp;
+    cp.m = mx;
+    cp.s_hi = t.hi;
+    cp.s_lo = t.lo;
+    cp.bad = bad ? 1u : 0u;
+    P.ws.parts[static_cast<int64_t>(r) * NCH + c] = cp;
+    __threadfence();
+    const unsigned old = atomicInc(&P.ws.row_cnt[r], static_cast<unsigned>(NCH - 1));
+    flag[0] = old == static_cast<unsigned>(NCH - 1) ? 1 : 0;
+    if (flag[0]) {          // last chunk of the row: merge (max, sum) online
+      __threadfence();
+      float M = -INFINITY;
+      uint32_t anybad = 0;
+      const ChunkPart *parts = P.ws.parts + static_cast<int64_t>(r) * NCH;
+      for (int k = 0; k < NCH; ++k) {
+        M = fmaxf(M, __ldcg(&parts[k].m));
+        anybad |= __ldcg(&parts[k].bad);
+      }
+      FF S = ff_make(0.0f);
+      if (M > -INFINITY) {
+        const WeightFn sc{M, P.c_hi, P.c_lo};
+        for (int k = 0; k < NCH; ++k) {
+          const float qm = __ldcg(&parts[k].m);
+          if (qm == -INFINITY) continue;
+          const float f = sc(qm);                        // exp((m_k - M)/T)
+          S = ff_add(S, ff_add(FF{__fmul_rn(__ldcg(&parts[k].s_hi), f), 0.0f},
+                               FF{__fmul_rn(__ldcg(&parts[k].s_lo), f), 0.0f}));
+        }
+      }
+      const bool valid = !anybad && M > -INFINITY;
+      write_stats(&P.ws.stats[r], M, 0u, valid, ff_to_double(S));
+    }
+  }
+  __syncthreads();
+  if (flag[0]) arrive_sequence<T>(P, i, &flag[1]);
+}
+
+// --------------------------------------------------------------------------
+// Phase 1b (nucleus): one CTA per row.  The row is read once from HBM into
+// shared memory (or streamed from L2 when longer than 64 KB), then max, sum,
+// and the nucleus cut run on chip.
+// --------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SampSmem &sm = *reinterpret_cast<SampSmem *>(smem_raw);
+  const sv_sample_args &a = P.a;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const void *base;
+  int64_t off;
+  const int i = row_seq(a, r, base, off);
+  if (!seq_rows_ok(a, i)) {
+    if (tid == 0) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+    return;
+  }
+  const T *row = static_cast<const T *>(base) + off;
+  constexpr int EPV = LT<T>::EPV;
+  RowPass<T> rp;
+  rp.init(row, a.vocab, reinterpret_cast<uint4 *>(smem_raw + kSmemRowOff));  // the one HBM read
+  float mx = -INFINITY;
+  int bad = 0;
+  rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
       const float x = LT<T>::val(bits[e]);
       bad |= (x != x) || (x == INFINITY);
       mx = fmaxf(mx, x);
     }
-  }
+  });
   bad = __syncthreads_or(bad);
   mx = block_max_f<kSampNT>(mx, sm.redf);
   const bool valid = !bad && mx > -INFINITY;
   uint32_t tau = 0;
-  double ssum = 1.0;
+  double ssum = 0.0;
   if (valid) {
     const WeightFn wf{mx, P.c_hi, P.c_lo};
-    // pass 2: sum of weights (Kahan per thread, fp64 across threads)
     float s = 0.0f, comp = 0.0f;
-    for (int v = tid; v < NV; v += kSampNT) {
-      uint32_t bits[EPV];
-      load_bits<T>(row, V, v, aligned, bits);
+    rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         const float y = __fsub_rn(wf(LT<T>::val(bits[e])), comp);
@@ -545,72 +666,725 @@ __global__ void __launch_bounds__(kSampNT) sampler_kernel(const SampParams P) {
         comp = __fsub_rn(__fsub_rn(t, s), y);
         s = t;
       }
+    });
+    FF S[1] = {FF{s, -comp}};
+    block_sum_ff<1>(S, sm.red[1]);
+    nucleus_cut<T>(rp, wf, ff_to_double(S[0]), a.top_p, sm, tau, ssum);
+  }
+  if (tid == 0) write_stats(&P.ws.stats[r], mx, tau, valid, ssum);
+  arrive_sequence<T>(P, i, &sm.bcast[3]);
+}
+
+// --------------------------------------------------------------------------
+// Phase 2: draw and append.  CTA (sequence i, chunk c): fixed-point sum of the
+// draw weights of its chunk of row n_i (residual of target/draft row n_i, or
+// the bonus target row); the last chunk to finish scans the chunk sums, finds
+// the chunk holding the crossing and walks it.  Every chunk CTA also copies its
+// slice of block rows 0..n_i to the KV pool (fused step).
+// --------------------------------------------------------------------------
+constexpr int kDrawNT = 256;
+constexpr int kDrawVec = 2;          // contiguous vectors per thread in the walk
+
+struct DrawSmem {
+  unsigned long long red[kDrawNT / 32];
+  unsigned long long bc64[2];
+  int bc[4];
+};
+
+// Sum of the chunk's fixed-point weights (block-wide, all threads get it).
+template <typename T>
+__device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int v0, int v1,
+                                        const RowProb &pq, const RowProb &pp, int mode,
+                                        DrawSmem &sm) {
+  constexpr int EPV = LT<T>::EPV;
+  const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
+  const bool al_d = mode == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  unsigned long long s = 0;
+  for (int vb = v0; vb < v1; vb += kDrawVec * kDrawNT) {
+    uint4 q[kDrawVec], d[kDrawVec];
+#pragma unroll
+    for (int k = 0; k < kDrawVec; ++k) {
+      const int v = vb + k * kDrawNT + threadIdx.x;
+      if (v < v1) {
+        q[k] = load_vec<T>(trow, V, v, al_t);
+        if (mode == 0) d[k] = load_vec<T>(drow, V, v, al_d);
+      }
     }
-    const double S = block_sum_d<kSampNT>(static_cast<double>(s) - static_cast<double>(comp), sm.red);
-    if (a.top_p < 1.0f) {
-      nucleus_cut<T>(row, V, aligned, wf, S, a.top_p, sm, tau, ssum);
-    } else {
-      ssum = S;
+#pragma unroll
+    for (int k = 0; k < kDrawVec; ++k) {
+      const int v = vb + k * kDrawNT + threadIdx.x;
+      if (v < v1) {
+        uint32_t bq[EPV], bd[EPV];
+        unpack<T>(q[k], bq);
+        if (mode == 0) unpack<T>(d[k], bd);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
+      }
     }
   }
+  s = warp_sum_u64(s);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red[w] = s;
+  __syncthreads();
+  unsigned long long t = 0;
+#pragma unroll
+  for (int k = 0; k < kDrawNT / 32; ++k) t += sm.red[k];
+  return t;
+}
+
+// Index of the first element of vectors [v0, v1) whose running weight sum,
+// starting at 0, exceeds `tgt` (requires the chunk total > tgt).  Thread t
+// owns kDrawVec contiguous vectors, so thread order is vocabulary order.
+template <typename T>
+__device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
+                          const RowProb &pq, const RowProb &pp, int mode,
+                          unsigned long long tgt, DrawSmem &sm, unsigned long long *scan_red) {
+  constexpr int EPV = LT<T>::EPV;
+  const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
+  const bool al_d = mode == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  const int tid = threadIdx.x;
+  int result = -1;
+  if (tid == 0) sm.bc[0] = -1;
+  unsigned long long base = 0;
+  for (int vb = v0; vb < v1; vb += kDrawVec * kDrawNT) {
+    const int va = vb + tid * kDrawVec;
+    uint32_t bq[kDrawVec][EPV], bd[kDrawVec][EPV];
+    unsigned long long s = 0;
+#pragma unroll
+    for (int k = 0; k < kDrawVec; ++k) {
+      if (va + k < v1) {
+        unpack<T>(load_vec<T>(trow, V, va + k, al_t), bq[k]);
+        if (mode == 0) unpack<T>(load_vec<T>(drow, V, va + k, al_d), bd[k]);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u);
+      }
+    }
+    unsigned long long total;
+    const unsigned long long ex = block_exclusive_scan_u64<kDrawNT>(s, scan_red, &total);
+    const unsigned long long lo = base + ex;
+    if (s > 0 && lo <= tgt && tgt < lo + s) {
+      unsigned long long c = lo;
+      int x = (va + kDrawVec) * EPV - 1;
+      bool found = false;
+#pragma unroll
+      for (int k = 0; k < kDrawVec; ++k)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (!found && va + k < v1) {
+            c += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u);
+            if (c > tgt) { x = (va + k) * EPV + e; found = true; }
+          }
+        }
+      sm.bc[0] = x;
+    }
+    __syncthreads();
+    result = sm.bc[0];
+    if (result >= 0) break;
+    base += total;
+  }
+  return result;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
+  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
+  __shared__ DrawSmem sm;
+  __shared__ unsigned long long scan_red[kDrawNT / 32];
+  const sv_sample_args &a = P.a;
+  const int NCH = P.plan.draw_chunks;
+  const int i = blockIdx.x / NCH, c = blockIdx.x - i * NCH;
+  const int tid = threadIdx.x;
+  if (!seq_rows_ok(a, i)) return;                 // flagged in phase 1
+  const int V = a.vocab, R = static_cast<int>(a.num_rows);
+  const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
+  const int L = a.kv_len[i];
+  const int n = a.num_accepted[i];
+  if (n < 0 || n > K) {                           // failed sequence: nothing to draw
+    if (P.do_append && c == 0 && tid == 0) P.app.new_kv_len[i] = L;
+    return;
+  }
+  // ---- append this chunk's slice of block rows 0..n (fused step)
+  if (P.do_append) {
+    const AppendView &A = P.app;
+    const int64_t start = A.kv_start[i];
+    const bool cap_ok = L + n + 1 <= A.kv_cap[i];
+    const bool pool_ok = start >= 0 && start + L + n + 1 <= A.pool_rows;
+    if (cap_ok && pool_ok) {
+      const int64_t nvec = static_cast<int64_t>(n + 1) * A.row_bytes / 16;
+      const int64_t a0 = nvec * c / NCH, a1 = nvec * (c + 1) / NCH;
+      const uint4 *__restrict__ sk = reinterpret_cast<const uint4 *>(
+          static_cast<const char *>(A.k_new) + static_cast<int64_t>(r0) * A.row_bytes);
+      const uint4 *__restrict__ svv = reinterpret_cast<const uint4 *>(
+          static_cast<const char *>(A.v_new) + static_cast<int64_t>(r0) * A.row_bytes);
+      uint4 *__restrict__ dk = reinterpret_cast<uint4 *>(static_cast<char *>(A.k_cache) +
+                                                         (start + L) * A.row_bytes);
+      uint4 *__restrict__ dv = reinterpret_cast<uint4 *>(static_cast<char *>(A.v_cache) +
+                                                         (start + L) * A.row_bytes);
+      constexpr int U = 4;
+      for (int64_t b = a0; b < a1; b += U * kDrawNT) {
+        uint4 x[U], y[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int64_t v = b + k * kDrawNT + tid;
+          if (v < a1) { x[k] = __ldcg(sk + v); y[k] = __ldcg(svv + v); }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int64_t v = b + k * kDrawNT + tid;
+          if (v < a1) { dk[v] = x[k]; dv[v] = y[k]; }
+        }
+      }
+    }
+    if (c == 0 && tid == 0) {
+      if (!cap_ok) set_status(a.dev_status, SV_DEV_CAPACITY);
+      else if (!pool_ok) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+      A.new_kv_len[i] = cap_ok && pool_ok ? L + n + 1 : L;
+    }
+  }
+  // ---- chunk sum of the draw weights
+  constexpr int EPV = LT<T>::EPV;
+  const int mode = n < K ? 0 : 1;
+  const T *trow = static_cast<const T *>(a.target_logits) + static_cast<int64_t>(r0 + n) * V;
+  const T *drow = mode == 0 ? static_cast<const T *>(a.draft_logits) + static_cast<int64_t>(p0 + n) * V
+                            : trow;
+  const RowProb pq = rowprob_of(&P.ws.stats[r0 + n], P.c_hi, P.c_lo);
+  const RowProb pp = mode == 0 ? rowprob_of(&P.ws.stats[R + p0 + n], P.c_hi, P.c_lo) : pq;
+  const int NV = (V + EPV - 1) / EPV;
+  const int per = (NV + NCH - 1) / NCH;
+  const int v0 = min(NV, c * per), v1 = min(NV, v0 + per);
+  const unsigned long long cs = chunk_sum<T>(trow, drow, V, v0, v1, pq, pp, mode, sm);
   if (tid == 0) {
-    RowStats st;
-    st.lmax = mx;
-    st.tau_key = tau;
-    st.valid = valid ? 1u : 0u;
-    st.pad = 0;
-    st.ssum = ssum;
-    P.stats[r] = st;
+    P.ws.draw_parts[static_cast<int64_t>(i) * NCH + c] = cs;
     __threadfence();
-    const int nrows = 2 * (a.cu_q[i + 1] - a.cu_q[i]) - 1;
-    const unsigned old = atomicInc(&P.counters[i], static_cast<unsigned>(nrows - 1));
-    sm.bcast[3] = (old == static_cast<unsigned>(nrows - 1)) ? 1 : 0;
+    const unsigned old = atomicInc(&P.ws.seq_cnt2[i], static_cast<unsigned>(NCH - 1));
+    sm.bc[1] = old == static_cast<unsigned>(NCH - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (sm.bcast[3]) {
-    __threadfence();
-    decide_sequence<T>(P, i, sm);
+  if (!sm.bc[1]) return;
+  // ---- last chunk: find the crossing chunk, walk it
+  __threadfence();
+  const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+  const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
+                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                              static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+  const unsigned long long ku = u24(wv.y);
+  int use_mode = mode;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (tid == 0) {
+      unsigned long long Z = 0;
+      if (attempt == 0) {
+        for (int k = 0; k < NCH; ++k) Z += __ldcg(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
+      }
+      sm.bc64[0] = Z;
+    }
+    __syncthreads();
+    unsigned long long Z = sm.bc64[0];
+    if (attempt == 1) {            // fallback: q_hat of row n, chunk sums computed here
+      Z = 0;
+      for (int k = 0; k < NCH; ++k) {
+        const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
+        Z += chunk_sum<T>(trow, trow, V, a0, a1, pq, pq, 1, sm);
+      }
+    }
+    if (Z == 0) {
+      if (attempt == 0 && mode == 0) {
+        if (tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+        use_mode = 1;
+        continue;
+      }
+      if (tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: cannot happen for a valid row
+      return;
+    }
+    const unsigned long long tgt = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);   // floor(k*Z/2^24)
+    // locate the chunk (chunk sums recomputed in the fallback)
+    unsigned long long cum = 0;
+    int cstar = NCH - 1;
+    for (int k = 0; k < NCH; ++k) {
+      unsigned long long zk;
+      if (use_mode == mode) {
+        zk = __ldcg(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
+      } else {
+        const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
+        zk = chunk_sum<T>(trow, trow, V, a0, a1, pq, pq, 1, sm);
+      }
+      if (tgt < cum + zk) { cstar = k; break; }
+      cum += zk;
+    }
+    const int a0 = min(NV, cstar * per), a1 = min(NV, a0 + per);
+    const int x = use_mode == mode
+                      ? chunk_walk<T>(trow, drow, V, a0, a1, pq, pp, mode, tgt - cum, sm, scan_red)
+                      : chunk_walk<T>(trow, trow, V, a0, a1, pq, pq, 1, tgt - cum, sm, scan_red);
+    if (tid == 0) a.out_tokens[r0 + n] = x;
+    return;
+  }
+}
+
+// --------------------------------------------------------------------------
+// Cluster path (no nucleus): one thread-block cluster of kClusterN CTAs per
+// sequence.  Everything between the phases goes through distributed shared
+// memory and cluster barriers: no global atomics, no fences, no second launch.
+//   A  CTA k copies slice k of every row of the sequence into its shared
+//      memory (one cp.async round trip) and computes per-row slice (max, sum).
+//   M  CTA (q mod C) merges row q from the C slices; with the prefetched logit
+//      at the draft token it computes that row's probability of the draft.
+//   B  CTA 0, warp 0: accept tests; n is broadcast through CTA 0's memory.
+//   C  every CTA: exact fixed-point sums of its slice of row n (one run of
+//      vpt vectors per thread) and its slice of the append.
+//   D  CTA 0 scans the C * 256 run sums in vocabulary order (CTA-major) and
+//      walks the one run holding the crossing.
+// --------------------------------------------------------------------------
+constexpr int kClusterN = 16;
+constexpr int kClNT = 256;
+constexpr int kClNW = kClNT / 32;
+constexpr int kMaxRows = 2 * kMaxQRows - 1;          // 2K+1 rows per sequence
+constexpr int kClSmemRows = 96 * 1024;               // row slices cached in smem
+
+struct ClusterSmem {
+  // phase A results of this CTA, per row
+  float pm[kMaxRows];
+  float ps_hi[kMaxRows], ps_lo[kMaxRows];
+  uint32_t pbad[kMaxRows];
+  // merged rows (valid in CTA 0)
+  float st_m[kMaxRows], st_ihi[kMaxRows], st_ilo[kMaxRows];
+  uint32_t st_ok[kMaxRows];
+  float pdraft[kMaxRows];                          // probability of the draft token
+  // decision (valid in CTA 0)
+  int n, redo, fail;
+  // reductions
+  float redf[kMaxRows][kClNW];
+  FF redff[kMaxRows][kClNW];
+  unsigned long long run_sum[kClNT];               // phase C
+  unsigned long long scan_red[kClNW];
+  unsigned long long bc64[2];
+  int bc[4];
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Generic address of `p` in the shared memory of cluster CTA `rank`.
+template <typename X>
+__device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<X *>(r);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams P) {
+  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
+  extern __shared__ __align__(16) unsigned char csm_raw[];
+  ClusterSmem &sm = *reinterpret_cast<ClusterSmem *>(csm_raw);
+  uint4 *slice = reinterpret_cast<uint4 *>(csm_raw + (sizeof(ClusterSmem) + 127) / 128 * 128);
+  constexpr int EPV = LT<T>::EPV;
+  constexpr int C = kClusterN;
+  const sv_sample_args &a = P.a;
+  const uint32_t k = cluster_rank<T>();
+  const int i = blockIdx.x / C;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  if (!seq_rows_ok(a, i)) {            // uniform over the cluster: all CTAs leave
+    if (k == 0 && tid == 0) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+    return;
+  }
+  const int V = a.vocab, R = static_cast<int>(a.num_rows);
+  const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
+  const int nrows = 2 * K + 1;
+  const int L = a.kv_len[i];
+  const T *tgt = static_cast<const T *>(a.target_logits);
+  const T *drf = static_cast<const T *>(a.draft_logits);
+  auto row_ptr = [&](int q) -> const T * {
+    return q <= K ? tgt + static_cast<int64_t>(r0 + q) * V
+                  : drf + static_cast<int64_t>(p0 + q - K - 1) * V;
+  };
+  const int NV = (V + EPV - 1) / EPV;
+  const int per = (NV + C - 1) / C;                  // vectors per CTA slice
+  const int v0 = min(NV, static_cast<int>(k) * per), v1 = min(NV, v0 + per);
+  const int nv = v1 - v0;
+  const bool in_smem = nrows * nv * 16 <= kClSmemRows;
+
+  // ---- prefetch: the logit at the draft token of each row this CTA merges
+  uint32_t dbits = 0;
+  int dtok = -1;
+  const int myq = static_cast<int>(k) + (tid / 32) * C;       // row merged by lane 0 of warp tid/32
+  if (l == 0 && myq < nrows && myq != K) {
+    const int j = myq < K ? myq : myq - K - 1;
+    dtok = a.draft_tokens[p0 + j];
+    if (dtok >= 0 && dtok < V) dbits = LT<T>::bits(row_ptr(myq)[dtok]);
+  }
+  // ---- phase A: copy slice k of every row, per-row slice max and sum
+  auto vec_at = [&](int q, int v) -> uint4 {       // v relative to the slice
+    if (in_smem) return slice[q * nv + v];
+    const T *rp = row_ptr(q);
+    return load_vec<T>(rp, V, v0 + v, (reinterpret_cast<uintptr_t>(rp) & 15) == 0);
+  };
+  if (in_smem) {
+    for (int q = 0; q < nrows; ++q) {
+      const T *rp = row_ptr(q);
+      const bool al = (reinterpret_cast<uintptr_t>(rp) & 15) == 0;
+      for (int v = tid; v < nv; v += kClNT) {
+        if (al && (v0 + v + 1) * EPV <= V)
+          cp_async16(smem_u32(slice + q * nv + v), rp + (v0 + v) * EPV, 16);
+        else
+          slice[q * nv + v] = load_vec<T>(rp, V, v0 + v, al);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+  }
+  if (tid < nrows) sm.pbad[tid] = 0;
+  __syncthreads();
+  // max per row (thread partials -> warp -> smem)
+  for (int q = 0; q < nrows; ++q) {
+    float mx = -INFINITY;
+    int bad = 0;
+    for (int v = tid; v < nv; v += kClNT) {
+      uint32_t b[EPV];
+      unpack<T>(vec_at(q, v), b);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = LT<T>::val(b[e]);
+        bad |= (x != x) || (x == INFINITY);
+        mx = fmaxf(mx, x);
+      }
+    }
+    mx = warp_max(mx);
+    bad = __any_sync(0xffffffffu, bad);
+    if (l == 0) {
+      sm.redf[q][w] = mx;
+      if (bad) atomicOr(&sm.pbad[q], 1u);
+    }
+  }
+  __syncthreads();
+  if (tid < nrows) {
+    float mx = sm.redf[tid][0];
+#pragma unroll
+    for (int x = 1; x < kClNW; ++x) mx = fmaxf(mx, sm.redf[tid][x]);
+    sm.pm[tid] = mx;
+  }
+  __syncthreads();
+  // sum per row of exp((l - m_slice)/T): 8-element tree per vector, Kahan across
+  for (int q = 0; q < nrows; ++q) {
+    const float mq = sm.pm[q];
+    const WeightFn wf{mq, P.c_hi, P.c_lo};
+    float s = 0.0f, comp = 0.0f;
+    if (mq > -INFINITY) {
+      for (int v = tid; v < nv; v += kClNT) {
+        uint32_t b[EPV];
+        unpack<T>(vec_at(q, v), b);
+        float t8[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t8[e] = wf(LT<T>::val(b[e]));
+#pragma unroll
+        for (int st = EPV / 2; st > 0; st >>= 1)
+#pragma unroll
+          for (int e = 0; e < st; ++e) t8[e] = __fadd_rn(t8[e], t8[e + st]);
+        const float y = __fsub_rn(t8[0], comp);
+        const float t = __fadd_rn(s, y);
+        comp = __fsub_rn(__fsub_rn(t, s), y);
+        s = t;
+      }
+    }
+    const FF f = warp_sum_ff(FF{s, -comp});
+    if (l == 0) sm.redff[q][w] = f;
+  }
+  __syncthreads();
+  if (tid < nrows) {
+    FF t = sm.redff[tid][0];
+#pragma unroll
+    for (int x = 1; x < kClNW; ++x) t = ff_add(t, sm.redff[tid][x]);
+    sm.ps_hi[tid] = t.hi;
+    sm.ps_lo[tid] = t.lo;
+  }
+  cluster_sync_all();                              // slices of all rows done
+
+  // ---- phase M: lane 0 of warp x merges row q = k + x*C
+  if (l == 0 && myq < nrows) {
+    float M = -INFINITY;
+    uint32_t anybad = 0;
+    for (int c = 0; c < C; ++c) {
+      M = fmaxf(M, *dsmem(&sm.pm[myq], c));
+      anybad |= *dsmem(&sm.pbad[myq], c);
+    }
+    FF S = ff_make(0.0f);
+    if (M > -INFINITY) {
+      const WeightFn sc{M, P.c_hi, P.c_lo};
+      for (int c = 0; c < C; ++c) {
+        const float mc = *dsmem(&sm.pm[myq], c);
+        if (mc == -INFINITY) continue;
+        const float f = sc(mc);
+        S = ff_add(S, ff_add(FF{__fmul_rn(*dsmem(&sm.ps_hi[myq], c), f), 0.0f},
+                             FF{__fmul_rn(*dsmem(&sm.ps_lo[myq], c), f), 0.0f}));
+      }
+    }
+    const bool ok = !anybad && M > -INFINITY && S.hi > 0.0f;
+    // 1/S as a float-float: r = 1/hi, corrected by the residual 1 - S*r
+    const float rh = ok ? __frcp_rn(S.hi) : 0.0f;
+    const float res = ok ? __fmaf_rn(-S.hi, rh, 1.0f) - S.lo * rh : 0.0f;
+    const float rl = rh * res;
+    float pd = 0.0f;
+    if (ok && dtok >= 0 && dtok < V) {
+      const float wv = WeightFn{M, P.c_hi, P.c_lo}(LT<T>::val(dbits));
+      pd = __fmaf_rn(wv, rh, __fmul_rn(wv, rl));
+    }
+    *dsmem(&sm.st_m[myq], 0) = M;
+    *dsmem(&sm.st_ihi[myq], 0) = rh;
+    *dsmem(&sm.st_ilo[myq], 0) = rl;
+    *dsmem(&sm.st_ok[myq], 0) = ok ? 1u : 0u;
+    *dsmem(&sm.pdraft[myq], 0) = pd;
+  }
+  cluster_sync_all();                              // merged rows in CTA 0
+
+  // ---- phase B: accept tests (CTA 0, warp 0)
+  if (k == 0 && w == 0) {
+    int okall = 1;
+    for (int q = l; q < nrows; q += 32) okall &= sm.st_ok[q] != 0;
+    okall = __all_sync(0xffffffffu, okall) && L >= 0;
+    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+    bool rej = false, bad = false;
+    int d = 0;
+    if (okall && l < K) {
+      d = a.draft_tokens[p0 + l];
+      if (d < 0 || d >= V) {
+        rej = bad = true;
+      } else {
+        const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
+                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                    static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+        const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;
+        rej = !(__fmul_rn(u, sm.pdraft[K + 1 + l]) < sm.pdraft[l]);
+      }
+    }
+    const unsigned rm = __ballot_sync(0xffffffffu, rej);
+    const unsigned bm = __ballot_sync(0xffffffffu, bad);
+    const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
+    if (l <= K) a.out_tokens[r0 + l] = (n >= 0 && l < n) ? d : -1;
+    if (l == 0) {
+      a.num_accepted[i] = n;
+      sm.n = n;
+      if (!okall) set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
+      else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
+    }
+  }
+  cluster_sync_all();                              // n known
+  const int n = *dsmem(&sm.n, 0);
+
+  // ---- append slice k of block rows 0..n
+  if (P.do_append) {
+    const AppendView &A = P.app;
+    if (n < 0) {
+      if (k == 0 && tid == 0) A.new_kv_len[i] = L;
+    } else {
+      const int64_t start = A.kv_start[i];
+      const bool cap_ok = L + n + 1 <= A.kv_cap[i];
+      const bool pool_ok = start >= 0 && start + L + n + 1 <= A.pool_rows;
+      if (cap_ok && pool_ok) {
+        const int64_t nvec = static_cast<int64_t>(n + 1) * A.row_bytes / 16;
+        const int64_t a0 = nvec * k / C, a1 = nvec * (k + 1) / C;
+        const uint4 *sk = reinterpret_cast<const uint4 *>(static_cast<const char *>(A.k_new) +
+                                                          static_cast<int64_t>(r0) * A.row_bytes);
+        const uint4 *svv = reinterpret_cast<const uint4 *>(static_cast<const char *>(A.v_new) +
+                                                           static_cast<int64_t>(r0) * A.row_bytes);
+        uint4 *dk = reinterpret_cast<uint4 *>(static_cast<char *>(A.k_cache) + (start + L) * A.row_bytes);
+        uint4 *dv = reinterpret_cast<uint4 *>(static_cast<char *>(A.v_cache) + (start + L) * A.row_bytes);
+        for (int64_t v = a0 + tid; v < a1; v += kClNT) {
+          const uint4 x = __ldcg(sk + v), y = __ldcg(svv + v);
+          dk[v] = x;
+          dv[v] = y;
+        }
+      }
+      if (k == 0 && tid == 0) {
+        if (!cap_ok) set_status(a.dev_status, SV_DEV_CAPACITY);
+        else if (!pool_ok) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+        A.new_kv_len[i] = cap_ok && pool_ok ? L + n + 1 : L;
+      }
+    }
+  }
+  if (n < 0) {
+    cluster_sync_all();
+    return;
+  }
+  // ---- phases C and D (a second round draws from q_hat if the residual is empty)
+  const int vpt = (per + kClNT - 1) / kClNT;        // vectors per run
+  const int ra = v0 + tid * vpt, rb_ = min(v1, ra + vpt);
+  const int qn = n;                                 // target row n (row index q = n)
+  const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+  const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
+                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                              static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+  const unsigned long long ku = u24(wv.y);
+  int mode = n < K ? 0 : 1;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    RowProb pq, pp;
+    pq.wf = WeightFn{*dsmem(&sm.st_m[qn], 0), P.c_hi, P.c_lo};
+    pq.tau = 0;
+    pq.inv_hi = *dsmem(&sm.st_ihi[qn], 0);
+    pq.inv_lo = *dsmem(&sm.st_ilo[qn], 0);
+    pp = pq;
+    if (mode == 0) {
+      const int qd = K + 1 + n;
+      pp.wf = WeightFn{*dsmem(&sm.st_m[qd], 0), P.c_hi, P.c_lo};
+      pp.inv_hi = *dsmem(&sm.st_ihi[qd], 0);
+      pp.inv_lo = *dsmem(&sm.st_ilo[qd], 0);
+    }
+    const int qrow_t = n, qrow_d = K + 1 + n;
+    unsigned long long s = 0;
+    for (int v = ra; v < rb_; ++v) {
+      uint32_t bq[EPV], bd[EPV];
+      unpack<T>(vec_at(qrow_t, v - v0), bq);
+      if (mode == 0) unpack<T>(vec_at(qrow_d, v - v0), bd);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
+    }
+    sm.run_sum[tid] = s;
+    cluster_sync_all();                            // all run sums visible
+    if (k == 0) {
+      // thread t owns global runs g = t*C .. t*C+C-1 (g = cta * 256 + run)
+      unsigned long long mine = 0;
+      for (int u = 0; u < C; ++u) {
+        const int g = tid * C + u;
+        mine += *dsmem(&sm.run_sum[g % kClNT], g / kClNT);
+      }
+      unsigned long long Z;
+      const unsigned long long ex = block_exclusive_scan_u64<kClNT>(mine, sm.scan_red, &Z);
+      if (tid == 0) {
+        sm.redo = (Z == 0 && mode == 0) ? 1 : 0;
+        sm.fail = (Z == 0 && mode == 1) ? 1 : 0;
+        if (sm.redo) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+        if (sm.fail) a.out_tokens[r0 + n] = -1;
+        sm.bc64[0] = Z == 0 ? 0 : (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);
+      }
+      __syncthreads();
+      const unsigned long long tg = sm.bc64[0];
+      if (Z > 0 && ex <= tg && tg < ex + mine) {
+        // owner: find the run, then walk its elements
+        unsigned long long c = ex;
+        int g = tid * C;
+        for (int u = 0; u < C; ++u) {
+          const unsigned long long rs = *dsmem(&sm.run_sum[(tid * C + u) % kClNT], (tid * C + u) / kClNT);
+          if (tg < c + rs) { g = tid * C + u; break; }
+          c += rs;
+        }
+        const int cta = g / kClNT, run = g % kClNT;
+        const int va = min(NV, cta * per) + run * vpt;
+        const int vb = min(min(NV, cta * per + per), va + vpt);
+        int x = -1;
+        for (int v = va; v < vb && x < 0; ++v) {
+          const T *tr = row_ptr(qrow_t);
+          const T *dr = row_ptr(qrow_d < nrows ? qrow_d : qrow_t);
+          uint32_t bq[EPV], bd[EPV];
+          unpack<T>(load_vec<T>(tr, V, v, (reinterpret_cast<uintptr_t>(tr) & 15) == 0), bq);
+          if (mode == 0) unpack<T>(load_vec<T>(dr, V, v, (reinterpret_cast<uintptr_t>(dr) & 15) == 0), bd);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            if (x < 0) {
+              c += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
+              if (c > tg) x = v * EPV + e;
+            }
+          }
+        }
+        a.out_tokens[r0 + n] = x;
+      }
+    }
+    cluster_sync_all();                            // decision of this round visible
+    const int redo = *dsmem(&sm.redo, 0);
+    cluster_sync_all();                            // CTA 0's flag read by all: safe to exit
+    if (!redo) break;
+    mode = 1;
   }
 }
 
 }  // namespace
 
-size_t sampler_stats_bytes(const sv_sample_args &a) {
-  return static_cast<size_t>(2 * a.num_rows - a.batch) * sizeof(RowStats);
+SamplerPlan plan_sampler(const sv_sample_args &a) {
+  SamplerPlan p;
+  const int epv = a.dtype == SV_BF16 ? 8 : 4;
+  const int nv = (a.vocab + epv - 1) / epv;
+  p.stat_chunks = a.top_p < 1.0f ? 1 : std::max(1, std::min(32, (nv + 1023) / 1024));
+  p.draw_chunks = std::max(1, std::min(64, (nv + 511) / 512));
+  // one cluster per sequence when there is no nucleus and the rows' slices fit
+  const int per = (nv + kClusterN - 1) / kClusterN;
+  p.cluster = a.top_p >= 1.0f && (2 * a.max_q_rows - 1) * per * 16 <= kClSmemRows;
+  return p;
 }
 
 int sampler_max_vocab(int dtype) {
   return kMaxTiles * kSampNT * (dtype == SV_BF16 ? 8 : 4);
 }
 
+template <typename T>
+static cudaError_t launch_cluster(const SampParams &P, cudaStream_t s) {
+  auto kern = sampler_cluster_kernel<T>;
+  const int smem = static_cast<int>((sizeof(ClusterSmem) + 127) / 128 * 128) + kClSmemRows;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.a.batch * kClusterN);
+  cfg.blockDim = dim3(kClNT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterN;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+template <typename T>
+static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
+  const int rows = static_cast<int>(2 * P.a.num_rows - P.a.batch);
+  cudaError_t e;
+  if (P.plan.cluster) {
+    e = launch_cluster<T>(P, s);
+    if (e == cudaSuccess) return e;
+    (void)cudaGetLastError();          // no room for a cluster: two-kernel path
+  }
+  if (P.plan.stat_chunks > 1 || P.a.top_p >= 1.0f) {
+    stats_chunk_kernel<T><<<rows * P.plan.stat_chunks, kStatNT, 0, s>>>(P);
+  } else {
+    const size_t smem = kSmemRowOff + kRowSmemBytes;
+    e = cudaFuncSetAttribute(stats_row_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    stats_row_kernel<T><<<rows, kSampNT, smem, s>>>(P);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  draw_kernel<T><<<P.a.batch * P.plan.draw_chunks, kDrawNT, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s) {
   SampParams P;
   P.a = L.a;
-  P.stats = L.stats;
-  P.counters = L.counters;
+  P.ws = L.ws;
+  P.plan = L.plan;
   P.do_append = L.do_append ? 1 : 0;
   P.app = L.app;
   const double c = 1.4426950408889634 / static_cast<double>(L.a.temperature);
   P.c_hi = static_cast<float>(c);
   P.c_lo = static_cast<float>(c - static_cast<double>(P.c_hi));
-  P.inv_T = 1.0 / static_cast<double>(L.a.temperature);
   P.pdl_primary = L.pdl_primary ? 1 : 0;
-  const int grid = static_cast<int>(2 * L.a.num_rows - L.a.batch);
-  if (grid <= 0) return cudaSuccess;
-  const size_t smem = sizeof(SampSmem);
-  cudaError_t e;
-  if (L.a.dtype == SV_BF16) {
-    e = cudaFuncSetAttribute(sampler_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    sampler_kernel<uint16_t><<<grid, kSampNT, smem, s>>>(P);
-  } else {
-    e = cudaFuncSetAttribute(sampler_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    sampler_kernel<float><<<grid, kSampNT, smem, s>>>(P);
-  }
-  return cudaGetLastError();
+  if (2 * L.a.num_rows - L.a.batch <= 0) return cudaSuccess;
+  return L.a.dtype == SV_BF16 ? launch_t<uint16_t>(P, s) : launch_t<float>(P, s);
 }
 
 }  // namespace sv

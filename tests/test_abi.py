@@ -75,14 +75,24 @@ def _sample(b, **kw):
 @pytest.mark.parametrize("field,value,status", [
     ("num_kv_heads", 3, 1), ("head_dim", 96, 4), ("max_q_rows", 0, 1), ("max_q_rows", 17, 1),
     ("num_rows", 11, 1), ("num_rows", 1, 1), ("dtype", 7, 1), ("q", 4097, 1), ("out", 0, 1),
-    ("num_groups", 1, 4), ("batch", 5000, 1),
+    ("num_groups", 1, 1), ("num_groups", 300, 1), ("prefix_rows_bound", -1, 1),
+    ("batch", 5000, 1),
 ])
 def test_attention_host_validation(binding, field, value, status):
     a = _attn(binding, **{field: value})
+    if field == "prefix_rows_bound":
+        a.num_groups, a.group, a.prefix_start, a.prefix_len = 1, 4096, 4096, 4096
     st = binding.lib.spec_verify_attn(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
     assert st == status, binding.last_error()
     assert binding.last_error()
     assert binding.lib.sv_workspace_bytes(ctypes.byref(a), None) == 0
+
+
+def test_shared_prefix_needs_bf16(binding):
+    a = _attn(binding, dtype=binding.SV_F32, num_groups=1, group=4096, prefix_start=4096,
+              prefix_len=4096)
+    st = binding.lib.spec_verify_attn(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == binding.SV_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("field,value,status", [

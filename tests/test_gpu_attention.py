@@ -36,12 +36,18 @@ def tol(inp):
     return 1e-4 if inp["dtype"] == "f32" else 2e-2
 
 
+def prefix_of(inp):
+    if inp.get("group") is None:
+        return None
+    return (inp["group"], inp["prefix_start"], inp["prefix_len"])
+
+
 def full_check(api, inp):
     d = run_attn(api, inp)
     got = d.out.float().cpu().numpy()
     ref = oracle.verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
                                   inp["v_cache"], inp["cu_q"], inp["kv_start"], inp["kv_len"],
-                                  inp["num_kv_heads"])
+                                  inp["num_kv_heads"], prefix=prefix_of(inp))
     err = np.max(np.abs(got - ref))
     assert np.all(np.isfinite(got)) and err < tol(inp), err
     assert d.status_bits() == 0
@@ -61,7 +67,7 @@ def sampled_check(api, inp, n=96, seed=0):
         h = int(rng.integers(0, inp["num_q_heads"]))
         ref = oracle.attention_row(i, h, j, inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
                                    inp["v_cache"], cu, inp["kv_start"], inp["kv_len"],
-                                   inp["num_kv_heads"])
+                                   inp["num_kv_heads"], prefix=prefix_of(inp))
         worst = max(worst, float(np.max(np.abs(got[cu[i] + j, h] - ref))))
     assert worst < tol(inp), worst
     assert d.status_bits() == 0
@@ -112,7 +118,8 @@ def test_zero_length_cache_rows_only_block(api):
     full_check(api, inp)
 
 
-@pytest.mark.parametrize("name", ["bass_b8", "ragged_gqa_b32", "vocab128k_b64"])
+@pytest.mark.parametrize("name", ["bass_b8", "ragged_gqa_b32", "vocab128k_b64",
+                                  "shared_prefix_s32"])
 def test_full_size_sampled(api, name):
     sampled_check(api, attn_inputs(name))
 
@@ -144,6 +151,29 @@ def test_shared_prefix_arrangement_as_plain_cache(api):
                                   inp["num_kv_heads"],
                                   prefix=(inp["group"], inp["prefix_start"], inp["prefix_len"]))
     assert np.max(np.abs(got - ref)) < 2e-2
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=7, groups=3, prefix_lens=(300, 0, 130), Hq=4, Hkv=4, K_lo=0, K_hi=6, L_hi=200),
+    dict(B=9, groups=2, prefix_lens=(777, 64), Hq=8, Hkv=2, K_lo=1, K_hi=7, L_hi=100),
+    dict(B=13, groups=1, prefix_len=1000, Hq=4, Hkv=4, K_lo=4, K_hi=4, L_lo=0, L_hi=0),
+    dict(B=5, groups=5, prefix_len=65, D=64, Hq=16, Hkv=2, K_lo=0, K_hi=7, L_hi=70),
+])
+def test_shared_prefix_all_outputs(api, kw):
+    """Bifurcated mode: prefix row-blocks + decode segments + merge equal
+    attention over [prefix ++ own cache ++ block] (bifurcated attention
+    abstract: the split is precise)."""
+    full_check(api, attn_inputs("shared_prefix_s32", gen_seed=sum(kw.get("prefix_lens", (1,))),
+                                **kw))
+
+
+def test_shared_prefix_bad_group_order_flagged(api):
+    inp = attn_inputs("shared_prefix_s32", B=4, groups=2, prefix_len=100, Hq=4, Hkv=4, L_hi=50,
+                      gen_seed=2)
+    inp["group"] = np.array([0, 1, 0, 1], dtype=np.int32)    # not contiguous
+    d = run_attn(api, inp)
+    assert d.status_bits() & oracle.DEV_BAD_LENGTH
+    assert np.all(np.isnan(d.out.float().cpu().numpy()))        # nothing written
 
 
 def test_bad_lengths_set_status_and_skip(api):

@@ -87,8 +87,9 @@ def test_fp32_logits_with_nucleus(api):
 
 def test_zero_drafts_and_max_drafts(api):
     """K_i = 0 (bonus only) next to K_i = 15 (16 block rows)."""
-    inp = sampler_inputs("ragged_gqa_b32", B=12, K_lo=0, K_hi=15, V=3000, gen_seed=11)
-    assert (np.diff(inp["cu_q"]) - 1).min() == 0 and (np.diff(inp["cu_q"]) - 1).max() >= 12
+    Ks = (0, 15, 0, 3, 15, 1, 0, 7, 15, 2, 0, 9)
+    inp = sampler_inputs("ragged_gqa_b32", B=12, K_fixed=Ks, V=3000, gen_seed=11)
+    assert list(np.diff(inp["cu_q"]) - 1) == list(Ks)
     check(api, inp)
 
 

@@ -53,10 +53,13 @@ def check_step(api, inp, attn_rows=None):
     tol = 1e-4 if inp["dtype"] == "f32" else 2e-2
     cu = inp["cu_q"]
     rng = np.random.default_rng(0)
+    prefix = None
+    if inp.get("group") is not None:
+        prefix = (inp["group"], inp["prefix_start"], inp["prefix_len"])
     if attn_rows is None:
         ref = oracle.verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
                                       inp["v_cache"], cu, inp["kv_start"], inp["kv_len"],
-                                      inp["num_kv_heads"])
+                                      inp["num_kv_heads"], prefix=prefix)
         err = np.max(np.abs(got - ref))
     else:
         err = 0.0
@@ -66,7 +69,7 @@ def check_step(api, inp, attn_rows=None):
             h = int(rng.integers(0, inp["num_q_heads"]))
             ref = oracle.attention_row(i, h, j, inp["q"], inp["k_new"], inp["v_new"],
                                        inp["k_cache"], inp["v_cache"], cu, inp["kv_start"],
-                                       inp["kv_len"], inp["num_kv_heads"])
+                                       inp["kv_len"], inp["num_kv_heads"], prefix=prefix)
             err = max(err, float(np.max(np.abs(got[cu[i] + j, h] - ref))))
     assert err < tol, err
     return d, ties
@@ -81,10 +84,17 @@ def test_small_bf16_step_all_outputs(api):
                                              gen_seed=31)))
 
 
-@pytest.mark.parametrize("name", ["bass_b8", "ragged_gqa_b32", "vocab128k_b64"])
+@pytest.mark.parametrize("name", ["bass_b8", "ragged_gqa_b32", "vocab128k_b64",
+                                  "shared_prefix_s32"])
 def test_full_size_step(api, name):
     d, ties = check_step(api, W.make_inputs(W.workload(name)), attn_rows=64)
     print(name, "accepted", d.num_accepted.tolist()[:16], "tie sequences", ties)
+
+
+def test_small_shared_prefix_step_all_outputs(api):
+    check_step(api, W.make_inputs(W.workload("shared_prefix_s32", B=6, groups=2,
+                                             prefix_lens=(200, 90), V=900, L_hi=100,
+                                             gen_seed=33)))
 
 
 def test_capacity_overflow_in_step(api):

@@ -43,12 +43,15 @@ class Workload:
     L_fixed: tuple = ()
     K_lo: int = 4              # drafts per sequence, lower bound
     K_hi: int = 4              # ... upper bound (inclusive)
+    K_fixed: tuple = ()        # explicit per-sequence draft counts (overrides K_lo/K_hi)
     logit_std: float = 3.0
     draft_noise: float = 1.0
     temperature: float = 1.0
     top_p: float = 1.0
     philox_seed: int = 0
-    prefix_len: int = 0        # > 0: one shared prefix of this length (bifurcated)
+    prefix_len: int = 0        # > 0: shared prefixes of this length (bifurcated)
+    groups: int = 1            # shared-prefix groups (contiguous runs of sequences)
+    prefix_lens: tuple = ()    # per-group prefix lengths (overrides prefix_len)
     cap_slack: int = 0         # extra pool rows per sequence beyond L + K + 1
     gen_seed: int = 0
 
@@ -112,6 +115,8 @@ def draw_lengths(w, rng):
     else:
         L = rng.integers(w.L_lo, w.L_hi + 1, size=w.B)
     K = rng.integers(w.K_lo, w.K_hi + 1, size=w.B)
+    if w.K_fixed:
+        K = np.array(w.K_fixed, dtype=np.int64)
     return L.astype(np.int64), K.astype(np.int64)
 
 
@@ -124,12 +129,15 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
     cu_q[1:] = np.cumsum(R_i)
     R = int(cu_q[-1])
     cap = L + R_i + w.cap_slack
-    # pool: guard | prefix | seq0 region | seq1 region | ... | guard
+    # pool: guard | prefixes | seq0 region | seq1 region | ... | guard
     prefix_start = None
     base = guard_rows
-    if w.prefix_len > 0:
-        prefix_start = np.array([base], dtype=np.int64)
-        base += w.prefix_len
+    shared = w.prefix_len > 0 or len(w.prefix_lens) > 0
+    if shared:
+        plen = np.array(w.prefix_lens if w.prefix_lens else [w.prefix_len] * w.groups,
+                        dtype=np.int64)
+        prefix_start = base + np.concatenate([[0], np.cumsum(plen)[:-1]]).astype(np.int64)
+        base += int(plen.sum())
     kv_start = np.zeros(w.B, dtype=np.int64)
     kv_start[0] = base
     kv_start[1:] = base + np.cumsum(cap)[:-1]
@@ -140,9 +148,10 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
                seq_ids=np.arange(w.B, dtype=np.int64),
                temperature=w.temperature, top_p=w.top_p, seed=w.philox_seed,
                scale=0.0, pool_rows=P)
-    if w.prefix_len > 0:
-        inp.update(group=np.zeros(w.B, dtype=np.int32), prefix_start=prefix_start,
-                   prefix_len=np.array([w.prefix_len], dtype=np.int32))
+    if shared:
+        G = len(plen)
+        inp.update(group=(np.arange(w.B) * G // w.B).astype(np.int32), prefix_start=prefix_start,
+                   prefix_len=plen.astype(np.int32))
     if with_attention:
         inp["q"] = _normal(rng, (R, w.Hq, w.D), 1.0, w.dtype)
         inp["k_new"] = _normal(rng, (R, w.Hkv, w.D), 1.0, w.dtype)
