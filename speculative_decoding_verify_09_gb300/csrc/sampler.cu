@@ -926,43 +926,42 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
 // sequence.  Everything between the phases goes through distributed shared
 // memory and cluster barriers: no global atomics, no fences, no second launch.
 //   A  CTA k copies slice k of every row of the sequence into its shared
-//      memory (one cp.async round trip) and computes per-row slice (max, sum).
-//   M  CTA (q mod C) merges row q from the C slices; with the prefetched logit
-//      at the draft token it computes that row's probability of the draft.
-//   B  CTA 0, warp 0: accept tests; n is broadcast through CTA 0's memory.
-//   C  every CTA: exact fixed-point sums of its slice of row n (one run of
-//      vpt vectors per thread) and its slice of the append.
+//      memory (one cp.async round trip) and computes each row's slice max and
+//      slice sum of exp((l - m)/T); rows are handled 8 at a time so their
+//      reductions overlap.
+//   B  CTA 0 merges every row from the C slices (one DSMEM load per thread),
+//      evaluates the probability of each draft token and runs the accept
+//      tests; n is published in CTA 0's shared memory.
+//   C  every CTA: exact fixed-point sums of its slice of row n, one run of
+//      vpt vectors per thread, for the residual and for q_hat (fallback),
+//      plus its slice of the append.
 //   D  CTA 0 scans the C * 256 run sums in vocabulary order (CTA-major) and
-//      walks the one run holding the crossing.
+//      walks the one run holding the crossing in the owner CTA's slice.
 // --------------------------------------------------------------------------
 constexpr int kClusterN = 16;
 constexpr int kClNT = 256;
 constexpr int kClNW = kClNT / 32;
 constexpr int kMaxRows = 2 * kMaxQRows - 1;          // 2K+1 rows per sequence
+constexpr int kRowGroup = 8;                         // rows reduced together
+constexpr int kClVPT = 2;                            // vectors per thread per row slice
 constexpr int kClSmemRows = 96 * 1024;               // row slices cached in smem
 
 struct ClusterSmem {
-  // phase A results of this CTA, per row
-  float pm[kMaxRows];
-  float ps_hi[kMaxRows], ps_lo[kMaxRows];
+  float pm[kMaxRows];                                // slice max per row
+  float ps_hi[kMaxRows], ps_lo[kMaxRows];            // slice sum per row
   uint32_t pbad[kMaxRows];
-  // merged rows (valid in CTA 0)
-  float st_m[kMaxRows], st_ihi[kMaxRows], st_ilo[kMaxRows];
-  uint32_t st_ok[kMaxRows];
-  float pdraft[kMaxRows];                          // probability of the draft token
-  // decision (valid in CTA 0)
-  int n, redo, fail;
-  // reductions
+  float st_m[kMaxRows], st_ihi[kMaxRows], st_ilo[kMaxRows];   // merged (CTA 0)
+  int n;                                             // decision (CTA 0)
   float redf[kMaxRows][kClNW];
   FF redff[kMaxRows][kClNW];
-  unsigned long long run_sum[kClNT];               // phase C
+  uint32_t redb[kMaxRows][kClNW];
+  unsigned long long run0[kClNT], run1[kClNT];       // residual / q_hat run sums
   unsigned long long scan_red[kClNW];
   unsigned long long bc64[2];
   int bc[4];
 };
 
-template <typename T>
-__device__ __forceinline__ uint32_t cluster_rank() {
+__device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
@@ -982,7 +981,7 @@ __device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams P) {
+__global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampParams P) {
   if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
   extern __shared__ __align__(16) unsigned char csm_raw[];
   ClusterSmem &sm = *reinterpret_cast<ClusterSmem *>(csm_raw);
@@ -990,7 +989,7 @@ __global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams
   constexpr int EPV = LT<T>::EPV;
   constexpr int C = kClusterN;
   const sv_sample_args &a = P.a;
-  const uint32_t k = cluster_rank<T>();
+  const uint32_t k = cluster_ctarank();
   const int i = blockIdx.x / C;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   if (!seq_rows_ok(a, i)) {            // uniform over the cluster: all CTAs leave
@@ -1011,93 +1010,128 @@ __global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams
   const int per = (NV + C - 1) / C;                  // vectors per CTA slice
   const int v0 = min(NV, static_cast<int>(k) * per), v1 = min(NV, v0 + per);
   const int nv = v1 - v0;
-  const bool in_smem = nrows * nv * 16 <= kClSmemRows;
 
-  // ---- prefetch: the logit at the draft token of each row this CTA merges
-  uint32_t dbits = 0;
-  int dtok = -1;
-  const int myq = static_cast<int>(k) + (tid / 32) * C;       // row merged by lane 0 of warp tid/32
-  if (l == 0 && myq < nrows && myq != K) {
-    const int j = myq < K ? myq : myq - K - 1;
-    dtok = a.draft_tokens[p0 + j];
-    if (dtok >= 0 && dtok < V) dbits = LT<T>::bits(row_ptr(myq)[dtok]);
-  }
-  // ---- phase A: copy slice k of every row, per-row slice max and sum
-  auto vec_at = [&](int q, int v) -> uint4 {       // v relative to the slice
-    if (in_smem) return slice[q * nv + v];
-    const T *rp = row_ptr(q);
-    return load_vec<T>(rp, V, v0 + v, (reinterpret_cast<uintptr_t>(rp) & 15) == 0);
-  };
-  if (in_smem) {
-    for (int q = 0; q < nrows; ++q) {
-      const T *rp = row_ptr(q);
-      const bool al = (reinterpret_cast<uintptr_t>(rp) & 15) == 0;
-      for (int v = tid; v < nv; v += kClNT) {
-        if (al && (v0 + v + 1) * EPV <= V)
-          cp_async16(smem_u32(slice + q * nv + v), rp + (v0 + v) * EPV, 16);
-        else
-          slice[q * nv + v] = load_vec<T>(rp, V, v0 + v, al);
-      }
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-  }
-  if (tid < nrows) sm.pbad[tid] = 0;
-  __syncthreads();
-  // max per row (thread partials -> warp -> smem)
-  for (int q = 0; q < nrows; ++q) {
-    float mx = -INFINITY;
-    int bad = 0;
-    for (int v = tid; v < nv; v += kClNT) {
-      uint32_t b[EPV];
-      unpack<T>(vec_at(q, v), b);
+  // ---- CTA 0 prefetches the logit at the draft token of rows mq and mq + 16
+  const int mq = tid / C, mc = tid % C;             // row and slice merged by this thread
+  uint32_t dbits[2] = {0u, 0u};
+  int dtok[2] = {-1, -1};
+  if (k == 0 && mc == 0) {
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const float x = LT<T>::val(b[e]);
-        bad |= (x != x) || (x == INFINITY);
-        mx = fmaxf(mx, x);
+    for (int pass = 0; pass < 2; ++pass) {
+      const int q = mq + pass * (kClNT / C);
+      if (q < nrows && q != K) {
+        const int j = q < K ? q : q - K - 1;
+        dtok[pass] = a.draft_tokens[p0 + j];
+        if (dtok[pass] >= 0 && dtok[pass] < V) dbits[pass] = LT<T>::bits(row_ptr(q)[dtok[pass]]);
       }
     }
-    mx = warp_max(mx);
-    bad = __any_sync(0xffffffffu, bad);
+  }
+  // ---- phase A: slice k of every row into shared memory
+  for (int q = 0; q < nrows; ++q) {
+    const T *rp = row_ptr(q);
+    const bool al = (reinterpret_cast<uintptr_t>(rp) & 15) == 0;
+    for (int v = tid; v < nv; v += kClNT) {
+      if (al && (v0 + v + 1) * EPV <= V)
+        cp_async16(smem_u32(slice + q * nv + v), rp + (v0 + v) * EPV, 16);
+      else
+        slice[q * nv + v] = load_vec<T>(rp, V, v0 + v, al);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  // slice max per row, kRowGroup rows at a time (compile-time bounds, so the
+  // rows' chains interleave)
+  for (int g0 = 0; g0 < nrows; g0 += kRowGroup) {
+    float mx[kRowGroup];
+    uint32_t bad[kRowGroup];
+#pragma unroll
+    for (int u = 0; u < kRowGroup; ++u) {
+      mx[u] = -INFINITY;
+      bad[u] = 0;
+#pragma unroll
+      for (int j = 0; j < kClVPT; ++j) {
+        const int v = tid + j * kClNT;
+        if (g0 + u < nrows && v < nv) {
+          uint32_t b[EPV];
+          unpack<T>(slice[(g0 + u) * nv + v], b);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float x = LT<T>::val(b[e]);
+            bad[u] |= (x != x) || (x == INFINITY);
+            mx[u] = fmaxf(mx[u], x);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < kRowGroup; ++u) {
+        mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], o));
+        bad[u] |= __shfl_xor_sync(0xffffffffu, bad[u], o);
+      }
     if (l == 0) {
-      sm.redf[q][w] = mx;
-      if (bad) atomicOr(&sm.pbad[q], 1u);
+#pragma unroll
+      for (int u = 0; u < kRowGroup; ++u)
+        if (g0 + u < nrows) {
+          sm.redf[g0 + u][w] = mx[u];
+          sm.redb[g0 + u][w] = bad[u];
+        }
     }
   }
   __syncthreads();
   if (tid < nrows) {
     float mx = sm.redf[tid][0];
+    uint32_t bd = sm.redb[tid][0];
 #pragma unroll
-    for (int x = 1; x < kClNW; ++x) mx = fmaxf(mx, sm.redf[tid][x]);
+    for (int x = 1; x < kClNW; ++x) {
+      mx = fmaxf(mx, sm.redf[tid][x]);
+      bd |= sm.redb[tid][x];
+    }
     sm.pm[tid] = mx;
+    sm.pbad[tid] = bd;
   }
   __syncthreads();
-  // sum per row of exp((l - m_slice)/T): 8-element tree per vector, Kahan across
-  for (int q = 0; q < nrows; ++q) {
-    const float mq = sm.pm[q];
-    const WeightFn wf{mq, P.c_hi, P.c_lo};
-    float s = 0.0f, comp = 0.0f;
-    if (mq > -INFINITY) {
-      for (int v = tid; v < nv; v += kClNT) {
-        uint32_t b[EPV];
-        unpack<T>(vec_at(q, v), b);
-        float t8[EPV];
+  // slice sum per row of exp((l - m_slice)/T): 8-element tree, float-float
+  for (int g0 = 0; g0 < nrows; g0 += kRowGroup) {
+    FF acc[kRowGroup];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) t8[e] = wf(LT<T>::val(b[e]));
+    for (int u = 0; u < kRowGroup; ++u) {
+      acc[u] = ff_make(0.0f);
+      const float mq_ = g0 + u < nrows ? sm.pm[g0 + u] : -INFINITY;
+      const WeightFn wf{mq_, P.c_hi, P.c_lo};
 #pragma unroll
-        for (int st = EPV / 2; st > 0; st >>= 1)
+      for (int j = 0; j < kClVPT; ++j) {
+        const int v = tid + j * kClNT;
+        if (mq_ > -INFINITY && v < nv) {
+          uint32_t b[EPV];
+          unpack<T>(slice[(g0 + u) * nv + v], b);
+          float t8[EPV];
 #pragma unroll
-          for (int e = 0; e < st; ++e) t8[e] = __fadd_rn(t8[e], t8[e + st]);
-        const float y = __fsub_rn(t8[0], comp);
-        const float t = __fadd_rn(s, y);
-        comp = __fsub_rn(__fsub_rn(t, s), y);
-        s = t;
+          for (int e = 0; e < EPV; ++e) t8[e] = wf(LT<T>::val(b[e]));
+#pragma unroll
+          for (int st = EPV / 2; st > 0; st >>= 1)
+#pragma unroll
+            for (int e = 0; e < st; ++e) t8[e] = __fadd_rn(t8[e], t8[e + st]);
+          acc[u] = ff_add(acc[u], ff_make(t8[0]));
+        }
       }
     }
-    const FF f = warp_sum_ff(FF{s, -comp});
-    if (l == 0) sm.redff[q][w] = f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < kRowGroup; ++u) {
+        FF t;
+        t.hi = __shfl_xor_sync(0xffffffffu, acc[u].hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, acc[u].lo, o);
+        acc[u] = ff_add(acc[u], t);
+      }
+    if (l == 0) {
+#pragma unroll
+      for (int u = 0; u < kRowGroup; ++u)
+        if (g0 + u < nrows) sm.redff[g0 + u][w] = acc[u];
+    }
   }
   __syncthreads();
   if (tid < nrows) {
@@ -1107,81 +1141,104 @@ __global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams
     sm.ps_hi[tid] = t.hi;
     sm.ps_lo[tid] = t.lo;
   }
-  cluster_sync_all();                              // slices of all rows done
+  cluster_sync_all();                              // (1) slices of all rows done
 
-  // ---- phase M: lane 0 of warp x merges row q = k + x*C
-  if (l == 0 && myq < nrows) {
-    float M = -INFINITY;
-    uint32_t anybad = 0;
-    for (int c = 0; c < C; ++c) {
-      M = fmaxf(M, *dsmem(&sm.pm[myq], c));
-      anybad |= *dsmem(&sm.pbad[myq], c);
-    }
-    FF S = ff_make(0.0f);
-    if (M > -INFINITY) {
-      const WeightFn sc{M, P.c_hi, P.c_lo};
-      for (int c = 0; c < C; ++c) {
-        const float mc = *dsmem(&sm.pm[myq], c);
-        if (mc == -INFINITY) continue;
-        const float f = sc(mc);
-        S = ff_add(S, ff_add(FF{__fmul_rn(*dsmem(&sm.ps_hi[myq], c), f), 0.0f},
-                             FF{__fmul_rn(*dsmem(&sm.ps_lo[myq], c), f), 0.0f}));
+  // ---- phase B (CTA 0): merge row mq from slice mc, 16 lanes per row
+  if (k == 0) {
+    static_assert(kClNT / C * 2 >= kMaxRows, "rows merged two per 16-lane group pass");
+    for (int pass = 0; pass < 2; ++pass) {
+      const int q = mq + pass * (kClNT / C);
+      const bool live = q < nrows;
+      float m = -INFINITY, shi = 0.0f, slo = 0.0f;
+      uint32_t bd = 0;
+      if (live) {
+        m = *dsmem(&sm.pm[q], mc);
+        shi = *dsmem(&sm.ps_hi[q], mc);
+        slo = *dsmem(&sm.ps_lo[q], mc);
+        bd = *dsmem(&sm.pbad[q], mc);
+      }
+      float M = m;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        bd |= __shfl_xor_sync(0xffffffffu, bd, o);
+      }
+      FF S = ff_make(0.0f);
+      if (m > -INFINITY) {
+        const float f = WeightFn{M, P.c_hi, P.c_lo}(m);     // exp((m_c - M)/T)
+        S = ff_add(FF{__fmul_rn(shi, f), 0.0f}, FF{__fmul_rn(slo, f), 0.0f});
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        FF t;
+        t.hi = __shfl_xor_sync(0xffffffffu, S.hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, S.lo, o);
+        S = ff_add(S, t);
+      }
+      if (live && mc == 0) {
+        const bool ok = !bd && M > -INFINITY && S.hi > 0.0f;
+        const float rh = ok ? __frcp_rn(S.hi) : 0.0f;    // 1/S as float-float
+        const float res = ok ? __fmaf_rn(-S.hi, rh, 1.0f) - S.lo * rh : 0.0f;
+        sm.st_m[q] = M;
+        sm.st_ihi[q] = rh;
+        sm.st_ilo[q] = ok ? rh * res : 0.0f;
+        sm.pbad[q] = ok ? 0u : 1u;                 // reused: 1 = row unusable
       }
     }
-    const bool ok = !anybad && M > -INFINITY && S.hi > 0.0f;
-    // 1/S as a float-float: r = 1/hi, corrected by the residual 1 - S*r
-    const float rh = ok ? __frcp_rn(S.hi) : 0.0f;
-    const float res = ok ? __fmaf_rn(-S.hi, rh, 1.0f) - S.lo * rh : 0.0f;
-    const float rl = rh * res;
-    float pd = 0.0f;
-    if (ok && dtok >= 0 && dtok < V) {
-      const float wv = WeightFn{M, P.c_hi, P.c_lo}(LT<T>::val(dbits));
-      pd = __fmaf_rn(wv, rh, __fmul_rn(wv, rl));
-    }
-    *dsmem(&sm.st_m[myq], 0) = M;
-    *dsmem(&sm.st_ihi[myq], 0) = rh;
-    *dsmem(&sm.st_ilo[myq], 0) = rl;
-    *dsmem(&sm.st_ok[myq], 0) = ok ? 1u : 0u;
-    *dsmem(&sm.pdraft[myq], 0) = pd;
-  }
-  cluster_sync_all();                              // merged rows in CTA 0
-
-  // ---- phase B: accept tests (CTA 0, warp 0)
-  if (k == 0 && w == 0) {
-    int okall = 1;
-    for (int q = l; q < nrows; q += 32) okall &= sm.st_ok[q] != 0;
-    okall = __all_sync(0xffffffffu, okall) && L >= 0;
-    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
-    bool rej = false, bad = false;
-    int d = 0;
-    if (okall && l < K) {
-      d = a.draft_tokens[p0 + l];
-      if (d < 0 || d >= V) {
-        rej = bad = true;
-      } else {
-        const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
-                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
-                                    static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
-        const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;
-        rej = !(__fmul_rn(u, sm.pdraft[K + 1 + l]) < sm.pdraft[l]);
+    __syncthreads();
+    // probability of the draft token in rows mq and mq + 16 (prefetched logits)
+    if (mc == 0) {
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        const int q = mq + pass * (kClNT / C);
+        if (q < nrows && q != K) {
+          float pd = 0.0f;
+          if (sm.pbad[q] == 0 && dtok[pass] >= 0 && dtok[pass] < V) {
+            const float wv = WeightFn{sm.st_m[q], P.c_hi, P.c_lo}(LT<T>::val(dbits[pass]));
+            pd = __fmaf_rn(wv, sm.st_ihi[q], __fmul_rn(wv, sm.st_ilo[q]));
+          }
+          sm.ps_hi[q] = pd;                        // reused: draft probability
+        }
       }
     }
-    const unsigned rm = __ballot_sync(0xffffffffu, rej);
-    const unsigned bm = __ballot_sync(0xffffffffu, bad);
-    const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
-    if (l <= K) a.out_tokens[r0 + l] = (n >= 0 && l < n) ? d : -1;
-    if (l == 0) {
-      a.num_accepted[i] = n;
-      sm.n = n;
-      if (!okall) set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
-      else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
+    __syncthreads();
+    // accept tests, lane j for draft j+1
+    if (w == 0) {
+      int okall = 1;
+      for (int q = l; q < nrows; q += 32) okall &= sm.pbad[q] == 0;
+      okall = __all_sync(0xffffffffu, okall) && L >= 0;
+      const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+      bool rej = false, bad = false;
+      int d = 0;
+      if (okall && l < K) {
+        d = a.draft_tokens[p0 + l];
+        if (d < 0 || d >= V) {
+          rej = bad = true;
+        } else {
+          const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
+                                         static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                         static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                      static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+          const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;     // exact
+          rej = !(__fmul_rn(u, sm.ps_hi[K + 1 + l]) < sm.ps_hi[l]);
+        }
+      }
+      const unsigned rm = __ballot_sync(0xffffffffu, rej);
+      const unsigned bm = __ballot_sync(0xffffffffu, bad);
+      const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
+      if (l <= K) a.out_tokens[r0 + l] = (n >= 0 && l < n) ? d : -1;
+      if (l == 0) {
+        a.num_accepted[i] = n;
+        sm.n = n;
+        if (!okall) set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
+        else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
+      }
     }
   }
-  cluster_sync_all();                              // n known
+  cluster_sync_all();                              // (2) n and merged rows in CTA 0
   const int n = *dsmem(&sm.n, 0);
 
-  // ---- append slice k of block rows 0..n
+  // ---- phase C: append slice k of block rows 0..n, run sums of row n
   if (P.do_append) {
     const AppendView &A = P.app;
     if (n < 0) {
@@ -1216,95 +1273,102 @@ __global__ void __launch_bounds__(kClNT) sampler_cluster_kernel(const SampParams
     cluster_sync_all();
     return;
   }
-  // ---- phases C and D (a second round draws from q_hat if the residual is empty)
+  const int mode = n < K ? 0 : 1;
+  const int qt = n, qd = K + 1 + n;                 // target row n, draft row n
+  RowProb pq, pp;
+  pq.wf = WeightFn{*dsmem(&sm.st_m[qt], 0), P.c_hi, P.c_lo};
+  pq.tau = 0;
+  pq.inv_hi = *dsmem(&sm.st_ihi[qt], 0);
+  pq.inv_lo = *dsmem(&sm.st_ilo[qt], 0);
+  pp = pq;
+  if (mode == 0) {
+    pp.wf = WeightFn{*dsmem(&sm.st_m[qd], 0), P.c_hi, P.c_lo};
+    pp.inv_hi = *dsmem(&sm.st_ihi[qd], 0);
+    pp.inv_lo = *dsmem(&sm.st_ilo[qd], 0);
+  }
   const int vpt = (per + kClNT - 1) / kClNT;        // vectors per run
-  const int ra = v0 + tid * vpt, rb_ = min(v1, ra + vpt);
-  const int qn = n;                                 // target row n (row index q = n)
-  const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
-  const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
-                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
-                              static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
-  const unsigned long long ku = u24(wv.y);
-  int mode = n < K ? 0 : 1;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    RowProb pq, pp;
-    pq.wf = WeightFn{*dsmem(&sm.st_m[qn], 0), P.c_hi, P.c_lo};
-    pq.tau = 0;
-    pq.inv_hi = *dsmem(&sm.st_ihi[qn], 0);
-    pq.inv_lo = *dsmem(&sm.st_ilo[qn], 0);
-    pp = pq;
-    if (mode == 0) {
-      const int qd = K + 1 + n;
-      pp.wf = WeightFn{*dsmem(&sm.st_m[qd], 0), P.c_hi, P.c_lo};
-      pp.inv_hi = *dsmem(&sm.st_ihi[qd], 0);
-      pp.inv_lo = *dsmem(&sm.st_ilo[qd], 0);
-    }
-    const int qrow_t = n, qrow_d = K + 1 + n;
-    unsigned long long s = 0;
+  {
+    unsigned long long s0 = 0, s1 = 0;
+    const int ra = tid * vpt, rb_ = min(nv, ra + vpt);
     for (int v = ra; v < rb_; ++v) {
       uint32_t bq[EPV], bd[EPV];
-      unpack<T>(vec_at(qrow_t, v - v0), bq);
-      if (mode == 0) unpack<T>(vec_at(qrow_d, v - v0), bd);
+      unpack<T>(slice[qt * nv + v], bq);
+      if (mode == 0) unpack<T>(slice[qd * nv + v], bd);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
+      for (int e = 0; e < EPV; ++e) {
+        const float qh = row_prob<T>(pq, bq[e]);
+        s1 += fix52(qh);
+        if (mode == 0) s0 += fix52(fmaxf(__fsub_rn(qh, row_prob<T>(pp, bd[e])), 0.0f));
+      }
     }
-    sm.run_sum[tid] = s;
-    cluster_sync_all();                            // all run sums visible
-    if (k == 0) {
-      // thread t owns global runs g = t*C .. t*C+C-1 (g = cta * 256 + run)
-      unsigned long long mine = 0;
+    sm.run0[tid] = mode == 0 ? s0 : s1;
+    sm.run1[tid] = s1;
+  }
+  cluster_sync_all();                              // (3) all run sums visible
+
+  // ---- phase D (CTA 0): scan the run sums, walk the owner run
+  if (k == 0) {
+    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+    const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
+                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+    const unsigned long long ku = u24(wv.y);
+    unsigned long long rs[C];                        // global runs g = tid*C + u
+    for (int round = 0; round < 2; ++round) {
+      const int use = round == 0 ? mode : 1;
+#pragma unroll
       for (int u = 0; u < C; ++u) {
         const int g = tid * C + u;
-        mine += *dsmem(&sm.run_sum[g % kClNT], g / kClNT);
+        rs[u] = use == 0 ? *dsmem(&sm.run0[g % kClNT], g / kClNT)
+                         : *dsmem(&sm.run1[g % kClNT], g / kClNT);
       }
+      unsigned long long mine = 0;
+#pragma unroll
+      for (int u = 0; u < C; ++u) mine += rs[u];
       unsigned long long Z;
       const unsigned long long ex = block_exclusive_scan_u64<kClNT>(mine, sm.scan_red, &Z);
-      if (tid == 0) {
-        sm.redo = (Z == 0 && mode == 0) ? 1 : 0;
-        sm.fail = (Z == 0 && mode == 1) ? 1 : 0;
-        if (sm.redo) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
-        if (sm.fail) a.out_tokens[r0 + n] = -1;
-        sm.bc64[0] = Z == 0 ? 0 : (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);
+      if (Z == 0) {
+        if (use == 0) {                            // rejected, empty residual: draw from q_hat
+          if (tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+          continue;
+        }
+        if (tid == 0) a.out_tokens[r0 + n] = -1;
+        break;
       }
-      __syncthreads();
-      const unsigned long long tg = sm.bc64[0];
-      if (Z > 0 && ex <= tg && tg < ex + mine) {
-        // owner: find the run, then walk its elements
+      const unsigned long long tg = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);
+      if (ex <= tg && tg < ex + mine) {
         unsigned long long c = ex;
         int g = tid * C;
+#pragma unroll
         for (int u = 0; u < C; ++u) {
-          const unsigned long long rs = *dsmem(&sm.run_sum[(tid * C + u) % kClNT], (tid * C + u) / kClNT);
-          if (tg < c + rs) { g = tid * C + u; break; }
-          c += rs;
+          if (c + rs[u] > tg) { g = tid * C + u; break; }
+          c += rs[u];
         }
         const int cta = g / kClNT, run = g % kClNT;
-        const int va = min(NV, cta * per) + run * vpt;
-        const int vb = min(min(NV, cta * per + per), va + vpt);
+        const int cnv = min(NV, cta * per + per) - min(NV, cta * per);    // slice length of cta
+        const int va = run * vpt, vb = min(cnv, va + vpt);
+        const uint4 *rslice = dsmem(slice, cta);
         int x = -1;
         for (int v = va; v < vb && x < 0; ++v) {
-          const T *tr = row_ptr(qrow_t);
-          const T *dr = row_ptr(qrow_d < nrows ? qrow_d : qrow_t);
           uint32_t bq[EPV], bd[EPV];
-          unpack<T>(load_vec<T>(tr, V, v, (reinterpret_cast<uintptr_t>(tr) & 15) == 0), bq);
-          if (mode == 0) unpack<T>(load_vec<T>(dr, V, v, (reinterpret_cast<uintptr_t>(dr) & 15) == 0), bd);
+          unpack<T>(rslice[qt * cnv + v], bq);
+          if (use == 0) unpack<T>(rslice[qd * cnv + v], bd);
 #pragma unroll
           for (int e = 0; e < EPV; ++e) {
             if (x < 0) {
-              c += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
-              if (c > tg) x = v * EPV + e;
+              const float qh = row_prob<T>(pq, bq[e]);
+              c += use == 0 ? fix52(fmaxf(__fsub_rn(qh, row_prob<T>(pp, bd[e])), 0.0f)) : fix52(qh);
+              if (c > tg) x = (min(NV, cta * per) + v) * EPV + e;
             }
           }
         }
         a.out_tokens[r0 + n] = x;
       }
+      break;
     }
-    cluster_sync_all();                            // decision of this round visible
-    const int redo = *dsmem(&sm.redo, 0);
-    cluster_sync_all();                            // CTA 0's flag read by all: safe to exit
-    if (!redo) break;
-    mode = 1;
   }
+  cluster_sync_all();                              // (4) CTA 0 done reading remote slices
 }
 
 }  // namespace
@@ -1317,7 +1381,8 @@ SamplerPlan plan_sampler(const sv_sample_args &a) {
   p.draw_chunks = std::max(1, std::min(64, (nv + 511) / 512));
   // one cluster per sequence when there is no nucleus and the rows' slices fit
   const int per = (nv + kClusterN - 1) / kClusterN;
-  p.cluster = a.top_p >= 1.0f && (2 * a.max_q_rows - 1) * per * 16 <= kClSmemRows;
+  p.cluster = a.top_p >= 1.0f && (2 * a.max_q_rows - 1) * per * 16 <= kClSmemRows &&
+              per <= kClVPT * kClNT;
   return p;
 }
 
