@@ -153,6 +153,34 @@ SV_API sv_status sv_workspace_init(void *ws, size_t ws_bytes, void *stream);
 SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_bytes,
                                   void *stream);
 
+/* Bytes of the static scratch array behind spec_verify_attn_static. */
+#define SV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* spec_verify_attn without a caller workspace, allocating nothing.  The
+ * speculative-sampling and verify-attention papers have no counterpart of
+ * this call: it serves callers that may not allocate device memory when they
+ * call (an embedder whose device memory belongs to another allocator, a
+ * serving runtime that forbids allocation once it has started) and so cannot
+ * supply the workspace spec_verify_attn takes.  The split-KV partials and
+ * merge counters live instead in a fixed SV_STATIC_SCRATCH_BYTES array inside
+ * the library's device image, one per device, held until the process exits.
+ *   - Setup: the first call on a device (the current one) looks the array up
+ *     and clears it to zero, synchronizing the device; make that first call
+ *     before any stream capture and outside code that must not synchronize.
+ *     Later calls only launch kernels on `stream`.
+ *   - Limits: the first 64 KiB hold only the merge counters (batch *
+ *     num_kv_heads <= 16384); the scratch of the call
+ *     (sv_workspace_bytes(attn, NULL)) plus those 64 KiB must fit in
+ *     SV_STATIC_SCRATCH_BYTES.  A call beyond either limit returns
+ *     SV_ERR_WORKSPACE and launches nothing.
+ *   - Zero state: the merge counters must be zero when a call starts; setup
+ *     zeroes them and every call that runs to completion leaves them zero.
+ *   - Concurrency: all calls on one device share the array, so calls that can
+ *     overlap on the GPU (other streams, other host threads without ordering)
+ *     race and corrupt each other's partials; order them on one stream.
+ * Results are those of spec_verify_attn on the same arguments. */
+SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream);
+
 /* Rejection sampling only: writes num_accepted and out_tokens. */
 SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,
                                     void *stream);

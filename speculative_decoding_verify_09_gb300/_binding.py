@@ -58,6 +58,8 @@ def _load():
     lib.sv_workspace_init.restype = ctypes.c_int
     lib.spec_verify_attn.argtypes = [P(AttnArgs), _p, ctypes.c_size_t, _p]
     lib.spec_verify_attn.restype = ctypes.c_int
+    lib.spec_verify_attn_static.argtypes = [P(AttnArgs), _p]
+    lib.spec_verify_attn_static.restype = ctypes.c_int
     lib.spec_reject_sample.argtypes = [P(SampleArgs), _p, ctypes.c_size_t, _p]
     lib.spec_reject_sample.restype = ctypes.c_int
     lib.kv_append_ragged.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64] + [_p] * 5 + \

@@ -119,6 +119,13 @@ def spec_verify_attn(attn, ws, stream=None):
                                 _stream(stream)))
 
 
+def spec_verify_attn_static(attn, stream=None):
+    """spec_verify_attn with the library's static device scratch instead of a
+    workspace, for callers that may not allocate device memory; nothing is
+    allocated (the first call on a device sets the scratch up)."""
+    _check(lib.spec_verify_attn_static(ctypes.byref(attn), _stream(stream)))
+
+
 def spec_reject_sample(sample, ws, stream=None):
     _check(lib.spec_reject_sample(ctypes.byref(sample), ctypes.c_void_p(ws.ptr), ws.nbytes,
                                   _stream(stream)))

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "kernels.h"
@@ -218,6 +219,46 @@ sv::SamplerLaunch sampler_launch(const sv_sample_args *sample, const Layout &L, 
 
 }  // namespace
 
+// Scratch of spec_verify_attn_static: a fixed array in the library's own device
+// image instead of a caller workspace.  It exists for callers that may not
+// allocate device memory at call time -- an embedder whose device memory is
+// owned by another allocator, or a serving runtime that forbids allocation once
+// it has started -- and so cannot supply the workspace the other entry points
+// take.  One copy per device (per CUDA context that loads the library).
+static __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Front zone of g_static_scratch that holds only merge counters (B * Hkv words).
+constexpr size_t kStaticCounterBytes = 64 * 1024;
+
+std::mutex g_static_mu;
+void *g_static_ptr[64] = {};
+
+// Device address of g_static_scratch on the current device.  The first call on
+// each device looks the symbol up and clears the array (synchronously, before
+// returning); later calls only read the cached address.
+sv_status static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SV_ERR_CUDA, "static scratch: device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch: cudaGetSymbolAddress");
+    e = cudaMemset(p, 0, SV_STATIC_SCRATCH_BYTES);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch: clearing");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return SV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 SV_API size_t sv_workspace_bytes(const sv_attn_args *attn, const sv_sample_args *sample) {
@@ -241,6 +282,35 @@ SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_
   if (st != SV_OK) return st;
   const Layout L = layout(attn, nullptr);
   if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
+  return run_attention(attn, L, ws, false, static_cast<cudaStream_t>(stream));
+}
+
+SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream) {
+  sv_status st = check_attn(attn);
+  if (st != SV_OK) return st;
+  // The merge counters keep a fixed zone at the front of the array that no call
+  // uses for anything else: the workspace layout puts partials right after the
+  // counters of *this* call's shape, so without the zone a smaller earlier
+  // call's partials would sit where a larger later call expects zeroed counters.
+  Layout L = layout(attn, nullptr);
+  const size_t counters = L.part_o - L.cnt_attn;
+  if (counters > kStaticCounterBytes)
+    return fail(SV_ERR_WORKSPACE,
+                "spec_verify_attn_static: %zu bytes of merge counters (batch x kv heads x 4), "
+                "the static array reserves %zu",
+                counters, kStaticCounterBytes);
+  L.part_o += kStaticCounterBytes;
+  L.part_ml += kStaticCounterBytes;
+  L.pre_o += kStaticCounterBytes;
+  L.pre_ml += kStaticCounterBytes;
+  L.total += kStaticCounterBytes;
+  if (L.total > SV_STATIC_SCRATCH_BYTES)
+    return fail(SV_ERR_WORKSPACE,
+                "spec_verify_attn_static: needs %zu bytes of scratch, the static array holds %zu "
+                "(use spec_verify_attn with a workspace)",
+                L.total, static_cast<size_t>(SV_STATIC_SCRATCH_BYTES));
+  void *ws = nullptr;
+  if ((st = static_scratch(&ws)) != SV_OK) return st;
   return run_attention(attn, L, ws, false, static_cast<cudaStream_t>(stream));
 }
 
