@@ -77,9 +77,12 @@ enum {
                                   out_tokens stay -1, no append) */
   SV_DEV_EMPTY_RESIDUAL = 8u,  /* rejected but max(0, q-p) sums to 0: the
                                   token is drawn from the target row instead */
-  SV_DEV_BAD_LENGTH = 16u      /* cu_q / kv_len / kv_start / prefix values
+  SV_DEV_BAD_LENGTH = 16u,     /* cu_q / kv_len / kv_start / prefix values
                                   inconsistent with the host bounds or the
                                   pool: that sequence is skipped */
+  SV_DEV_TIMEOUT = 32u         /* an internal wait of the attention pipeline
+                                  gave up (not expected; outputs of the
+                                  affected CTA are left unwritten) */
 };
 
 /* Verify attention (a1, a1b).  scale * q.k softmax over keys

@@ -1,5 +1,6 @@
 // C ABI of the verify step: argument checks, workspace layout, launches.
 // See include/spec_verify.h for the contract of every entry point.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -187,8 +188,45 @@ T *at(void *ws, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
-sv_status run_attention(const sv_attn_args *a, const Layout &L, void *ws, bool pdl,
-                        cudaStream_t s) {
+// Per-device shared-memory facts used to size the attention ring.
+struct SmemFacts {
+  int per_sm;          // shared memory of one SM
+  int reserved;        // shared memory the system keeps per CTA
+};
+
+SmemFacts smem_facts() {
+  static SmemFacts cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SmemFacts{0, 0};
+  if (cache[dev].per_sm == 0) {
+    int a = 0, b = 0;
+    if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&b, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+      return SmemFacts{0, 0};
+    cache[dev] = SmemFacts{a, b};
+  }
+  return cache[dev];
+}
+
+// Attention alone: two persistent CTAs per SM (two independent load streams
+// and twice the consumer warps to hide MMA latency), each with the deepest
+// ring that fits half an SM.
+sv::AttnLaunchOpts opts_alone() {
+  const SmemFacts f = smem_facts();
+  const int half = f.per_sm > 0 ? f.per_sm / 2 - f.reserved : sv::kSmemMax;
+  return sv::AttnLaunchOpts{false, std::min(half, sv::kSmemMax), 0, num_sms_current()};
+}
+
+// Attention ahead of the sampler in the fused step: launched the same way, and
+// lets the sampling launch start early (it runs on the SMs as they free up).
+sv::AttnLaunchOpts opts_step() {
+  sv::AttnLaunchOpts o = opts_alone();
+  o.pdl_primary = true;
+  return o;
+}
+
+sv_status run_attention(const sv_attn_args *a, const Layout &L, void *ws,
+                        const sv::AttnLaunchOpts &opts, cudaStream_t s) {
   if (a->batch == 0) return SV_OK;
   const int sms = num_sms_current();
   if (sms <= 0) return fail(SV_ERR_CUDA, "no CUDA device");
@@ -199,7 +237,7 @@ sv_status run_attention(const sv_attn_args *a, const Layout &L, void *ws, bool p
   w.dec_ml = at<float>(ws, L.part_ml);
   w.pre_o = at<float>(ws, L.pre_o);
   w.pre_ml = at<float>(ws, L.pre_ml);
-  cudaError_t e = sv::launch_attention(*a, plan, w, pdl, s);
+  cudaError_t e = sv::launch_attention(*a, plan, w, opts, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return SV_OK;
 }
@@ -282,7 +320,7 @@ SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_
   if (st != SV_OK) return st;
   const Layout L = layout(attn, nullptr);
   if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
-  return run_attention(attn, L, ws, false, static_cast<cudaStream_t>(stream));
+  return run_attention(attn, L, ws, opts_alone(), static_cast<cudaStream_t>(stream));
 }
 
 SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream) {
@@ -311,7 +349,7 @@ SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream)
                 L.total, static_cast<size_t>(SV_STATIC_SCRATCH_BYTES));
   void *ws = nullptr;
   if ((st = static_scratch(&ws)) != SV_OK) return st;
-  return run_attention(attn, L, ws, false, static_cast<cudaStream_t>(stream));
+  return run_attention(attn, L, ws, opts_alone(), static_cast<cudaStream_t>(stream));
 }
 
 SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,
@@ -323,7 +361,7 @@ SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size
   if (sample->batch == 0) return SV_OK;
   sv::SamplerLaunch SL = sampler_launch(sample, L, ws);
   SL.do_append = false;
-  SL.pdl_primary = false;
+  SL.pdl_secondary = false;
   cudaError_t e = sv::launch_sampler(SL, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
   return SV_OK;
@@ -382,11 +420,13 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   if ((st = check_ws(ws, ws_bytes, L.total)) != SV_OK) return st;
   if (attn->batch == 0) return SV_OK;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Sampling (with the append of accepted rows) is the primary launch; the
-  // attention launch may start while it runs and waits for it before exiting.
+  // The attention launches first and lets the sampling launch (with the append
+  // of accepted rows) start at once beside it; the sampling waits for the
+  // attention before it exits.  The append writes pool rows at or beyond
+  // kv_len[i], which the attention never reads.
   sv::SamplerLaunch SL = sampler_launch(sample, L, ws);
   SL.do_append = true;
-  SL.pdl_primary = true;
+  SL.pdl_secondary = true;
   const int esz = attn->dtype == SV_F32 ? 4 : 2;
   SL.app.k_new = attn->k_new;
   SL.app.v_new = attn->v_new;
@@ -399,9 +439,10 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   SL.app.row_bytes = attn->num_kv_heads * attn->head_dim * esz;
   if (SL.app.row_bytes % 16)
     return fail(SV_ERR_UNSUPPORTED, "step: K/V row bytes not a multiple of 16");
+  if ((st = run_attention(attn, L, ws, opts_step(), s)) != SV_OK) return st;
   cudaError_t e = sv::launch_sampler(SL, s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
-  return run_attention(attn, L, ws, true, s);
+  return SV_OK;
 }
 
 SV_API const char *sv_last_error(void) { return g_err.c_str(); }

@@ -11,20 +11,29 @@
 // bytes at HBM rate:
 //
 //  * Work unit: a 64-key tile of one (sequence, KV head) segment.  The
-//    (K_i + 1) x (Hq/Hkv) query rows sharing that KV head are packed as the M
+//    (K_i + 1) x (Hq/Hkv) query rows sharing that KV head are packed as the N
 //    dimension, so every KV byte is read once for all of them (GQA).
 //  * Stream-K split: the global tile sequence (segments in order) is cut into
-//    gridDim.x equal contiguous ranges, one per persistent CTA, regardless of
-//    segment boundaries.  A CTA that covers a whole segment writes the output
-//    directly; otherwise each piece writes a partial (unnormalized O, row max,
-//    row sum) and the last piece to arrive (atomic count, no waiting) merges
-//    them.  Balance is within one tile per CTA for any length mix.
-//  * Tiles are staged with a 3-stage cp.async pipeline (16-byte copies, rows
-//    XOR-swizzled in shared memory), which runs across segment boundaries.
-//  * Q.K^T and P.V use mma.sync m16n8k16 (bf16 in, fp32 accumulate); the
-//    probabilities stay in registers between the two products.  Online softmax
-//    per warp uses quad shuffles.  Four warps split each tile's 64 keys; their
-//    states are merged in shared memory at the end of a piece.
+//    gridDim.x equal contiguous ranges, one per persistent CTA (one CTA per
+//    SM), regardless of segment boundaries.  A CTA that covers a whole segment
+//    writes the output directly; otherwise each piece writes a partial
+//    (unnormalized O, row max, row sum) and the last piece to arrive (atomic
+//    count, no waiting) merges them.
+//  * Warp specialization: one producer warp walks the CTA's tile range and
+//    streams every K and V tile into a ring of shared-memory stages guarded by
+//    full / empty mbarriers, running ahead across segment boundaries: 16-byte
+//    cp.async copies (cache rows, block rows, zero fill past the end) into
+//    XOR-swizzled rows, whose completion arrives on the stage's mbarrier.  (A
+//    256-byte bulk copy per row moves the same bytes at about a quarter of the
+//    rate: the copy engine's cost is per request.)  It also stages each
+//    segment's packed Q rows (bulk copies into 16-byte-padded rows) and a
+//    segment header into one of two Q slots.
+//  * Consumer warps (4 key slices x RS row groups) compute S^T = K Q^T and
+//    O^T += V^T P^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate) and an
+//    online softmax per warp; no CTA-wide barrier per tile.  At the end of a
+//    piece the key-slice states are merged in shared memory.
+//  * Every wait is bounded: a wait that runs out sets SV_DEV_TIMEOUT and the
+//    CTA drains its copies in flight and leaves.
 //
 // fp32 inputs use a CUDA-core kernel (one CTA per segment, fp32 FMA).
 #include <algorithm>
@@ -37,11 +46,20 @@ namespace sv {
 namespace {
 
 constexpr int kTileKeys = 64;
-constexpr int kStages = 3;
-constexpr int kKW = 4;            // warps splitting the keys of one tile
-constexpr int kMaxBatch = 1024;   // sequences per call (schedule held in smem)
+constexpr int kKW = 4;            // consumer warps splitting the keys of one tile
+constexpr int kMaxBatch = 1024;   // sequences per call
 constexpr int kMaxGroups = 256;   // shared-prefix groups per call
+constexpr int kMaxStages = 8;
+constexpr uint32_t kSpinLimit = 1u << 22;   // polls of one mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Byte offsets of the dynamic shared memory (same on host and device).
+struct SmemMap {
+  int ns;                  // ring stages
+  int units_cap, groups_cap;
+  int q;                   // two Q slots (header + packed rows)
+  int merge_o, merge_ml, fin, bars, sched, misc, total;
+};
 
 struct AttnParams {
   int B, Hq, Hkv, g, max_q_rows;
@@ -57,44 +75,131 @@ struct AttnParams {
   uint32_t *counters;             // [B * Hkv]
   uint32_t *dev_status;
   int64_t tiles_bound;            // host bound on the global tile count
-  int pdl_secondary;
+  int pdl_primary;                // let the next launch start at once
   // shared-prefix (bifurcated) arrangement
   int mode;                       // 0 plain; 1 decode partials only; 2 prefix partials
   int G, spb;                     // groups; sequences per prefix row-block
   const int32_t *group;           // [B] non-decreasing
   const int64_t *prefix_start;    // [G]
   const int32_t *prefix_len;      // [G]
+  SmemMap sm;
 };
 
 // ---------------------------------------------------------------- smem layout
 // Warps: 4 key slices (16 keys of each 64-key tile) x RS row groups (8*NB
-// packed query rows each).  Packed row m = j*g + hg for block row j and query
-// head hk*g + hg; a CTA holds up to RS*8*NB rows.
+// packed query rows each), then the producer warp.  Packed row m = j*g + hg
+// for block row j and query head hk*g + hg; a CTA holds up to RS*8*NB rows.
 template <int D, int RS, int NB>
-struct AttnSmem {
-  static constexpr int kWarps = kKW * RS;
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kRowsW = 8 * NB;                        // rows per warp
-  static constexpr int kRows = RS * kRowsW;                    // rows per CTA
-  static constexpr int kTileBytes = kTileKeys * D * 2;         // one K or V tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kOStride = D + 4;                       // padded merge rows (floats)
+struct AttnCfg {
+  static constexpr int kCW = kKW * RS;                          // consumer warps
+  static constexpr int kThreads = (kCW + 1) * 32;
+  static constexpr int kRowsW = 8 * NB;                         // rows per warp
+  static constexpr int kRows = RS * kRowsW;                     // rows per CTA
+  static constexpr int kRowB = D * 2 + 16;                      // padded Q row
+  static constexpr int kTileB = kTileKeys * D * 2;              // one K or V tile (swizzled)
+  static constexpr int kStageB = 2 * kTileB;
+  static constexpr int kQHead = 64;                             // segment header
+  static constexpr int kQSlotB = kQHead + kRows * kRowB;
+  static constexpr int kOStride = D + 4;                        // padded merge rows (floats)
   static constexpr int kMergeO = kRows * kOStride * 4;
-  static constexpr int kMergeML = kWarps * kRowsW * 8;         // (m, l) per warp row
-  static constexpr int kFinal = kRows * 8;                     // merged (m, l) per row
-  static constexpr int kSchedBytes = kMaxBatch * 4 + 4 * kMaxGroups * 4;  // schedule tables
-  static constexpr int kOffStages = 0;
-  static constexpr int kOffMergeO = kStages * kStageBytes;
-  static constexpr int kOffMergeML = kOffMergeO + kMergeO;
-  static constexpr int kOffFinal = kOffMergeML + kMergeML;
-  static constexpr int kOffSched = kOffFinal + kFinal;
-  static constexpr int kOffMisc = kOffSched + kSchedBytes;
-  static constexpr int kBytes = kOffMisc + 64;
-  static_assert(kMaxBatch * 8 <= kStages * kStageBytes, "sequence bases staged in tile buffers");
+  static constexpr int kMergeML = kCW * kRowsW * 8;
+  static constexpr int kFinal = kRows * 8;
+  static_assert(kMaxBatch * 8 <= 2 * kStageB, "unit bases staged in the ring");
+
+  static SmemMap map(int ns, int units_cap, int groups_cap) {
+    auto up = [](int x, int a) { return (x + a - 1) / a * a; };
+    SmemMap m;
+    m.ns = ns;
+    m.units_cap = up(std::max(units_cap, 1), 4);
+    m.groups_cap = up(std::max(groups_cap, 1), 4);
+    int off = ns * kStageB;
+    m.q = off;
+    off += 2 * kQSlotB;
+    m.merge_o = off;
+    off += kMergeO;
+    m.merge_ml = off;
+    off += kMergeML;
+    m.fin = off;
+    off += kFinal;
+    m.bars = up(off, 8);
+    off = m.bars + (2 * ns + 5) * 8;
+    m.sched = up(off, 16);
+    off = m.sched + 4 * (m.units_cap + 4 * m.groups_cap);
+    m.misc = up(off, 16);
+    m.total = m.misc + 64;
+    return m;
+  }
 };
 
-// Swizzled byte offset of (row, 16-byte chunk) inside a tile: chunk ^ (row % 8)
-// makes the 8 rows read by one ldmatrix phase hit 8 different bank groups.
+// ---------------------------------------------------------------- mbarriers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete; false after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it)
+    if (mbar_test(bar, parity)) return true;
+  return false;
+}
+
+// One global -> shared bulk copy completing on `bar` (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+
+// 16-byte cp.async with an L2 cache-policy hint; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, int src_bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+// 2^x with the SFU's approximate exp2 (relative error ~2^-22, subnormal results
+// flushed to zero): far below the bf16 output rounding of the attention.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Padded Q row address inside a Q slot.
+template <int D>
+__device__ __forceinline__ uint32_t prow(int row, int chunk) {
+  return static_cast<uint32_t>(row * (D * 2 + 16) + (chunk << 4));
+}
+// Swizzled byte offset of (row, 16-byte chunk) inside a K or V tile: chunk ^
+// (row % 8) makes the 8 rows read by one ldmatrix phase hit 8 bank groups.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
@@ -117,13 +222,14 @@ struct Sched {
   __device__ __forceinline__ int nseg(int u) const { return mode == 2 ? ns[u] : Hkv; }
 };
 
-__device__ __forceinline__ Sched sched_view(unsigned char *base, int mode, int Hkv) {
+__device__ __forceinline__ Sched sched_view(unsigned char *base, int mode, int Hkv, int units_cap,
+                                            int groups_cap) {
   Sched S;
   S.nt = reinterpret_cast<int32_t *>(base);
-  S.ns = S.nt + kMaxBatch;
-  S.first = S.ns + kMaxGroups;
-  S.cnt = S.first + kMaxGroups;
-  S.segb = S.cnt + kMaxGroups;
+  S.ns = S.nt + units_cap;
+  S.first = S.ns + groups_cap;
+  S.cnt = S.first + groups_cap;
+  S.segb = S.cnt + groups_cap;
   S.mode = mode;
   S.Hkv = Hkv;
   S.units = 0;
@@ -260,51 +366,6 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams &P, const Sched &S,
   return s;
 }
 
-// Issue the cp.async copies of one 64-key K and V tile (threads 0..127).  Keys
-// below L come from the pool, the next Ri from the block rows, the rest are
-// zero-filled (and masked).  A tile entirely inside the cache takes the
-// strided fast path.
-template <int D>
-__device__ __forceinline__ void issue_tile_loads(const AttnParams &P, const SeqInfo &s, int hk,
-                                                 int lt, uint32_t stage_base) {
-  constexpr int CH = D / 8;                 // 16-byte chunks per row
-  constexpr int RPP = 128 / CH;             // rows per pass of 128 threads
-  constexpr int NPASS = kTileKeys / RPP;
-  constexpr int kTile = kTileKeys * D * 2;
-  const int t = threadIdx.x;
-  const int ch = t % CH, rr = t / CH;
-  const int key0 = lt * kTileKeys;
-  if (key0 + kTileKeys <= s.L) {
-    const int64_t off = ((s.kv0 + key0 + rr) * P.Hkv + hk) * D + ch * 8;
-    const int64_t step = static_cast<int64_t>(RPP) * P.Hkv * D;
-#pragma unroll
-    for (int p = 0; p < NPASS; ++p) {
-      const int row = rr + p * RPP;
-      cp_async16(stage_base + swz<D>(row, ch), P.k_cache + off + p * step, 16);
-      cp_async16(stage_base + kTile + swz<D>(row, ch), P.v_cache + off + p * step, 16);
-    }
-    return;
-  }
-#pragma unroll
-  for (int p = 0; p < NPASS; ++p) {
-    const int row = rr + p * RPP;
-    const int key = key0 + row;
-    int64_t off = 0;
-    const uint16_t *kb = P.k_new, *vb = P.v_new;
-    int bytes = 0;
-    if (key < s.L) {
-      off = ((s.kv0 + key) * P.Hkv + hk) * D + ch * 8;
-      kb = P.k_cache;
-      vb = P.v_cache;
-      bytes = 16;
-    } else if (key < s.L + s.Ri) {
-      off = (static_cast<int64_t>(s.r0 + key - s.L) * P.Hkv + hk) * D + ch * 8;
-      bytes = 16;
-    }
-    cp_async16(stage_base + swz<D>(row, ch), kb + off, bytes);
-    cp_async16(stage_base + kTile + swz<D>(row, ch), vb + off, bytes);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // bf16 kernel, operands swapped so keys are the MMA M dimension:
@@ -314,29 +375,135 @@ __device__ __forceinline__ void issue_tile_loads(const AttnParams &P, const SeqI
 // With few packed rows (MHA, K+1 <= 8) this needs half the MMAs of putting the
 // rows on M, and keeps O in 32*NB registers per thread.
 // ---------------------------------------------------------------------------
+struct Ring {            // shared-memory addresses of the pipeline
+  uint32_t base, q, full, empty, qfull, qempty, ebar;
+};
+
+// Producer warp: Q slots and K/V stages for the CTA's tiles [0, ntiles).
+template <int D, int RS, int NB>
+__device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S, Cursor ld,
+                                             int ntiles, const Ring &rg, unsigned char *smem,
+                                             volatile int *abort_flag) {
+  using C = AttnCfg<D, RS, NB>;
+  const int lane = threadIdx.x & 31;
+  const int NS = P.sm.ns;
+  const uint64_t pol = policy_evict_first();
+  SeqInfo s = load_seq(P, S, ld);
+  int st = 0;
+  uint32_t ph = 0;
+  int issued = 0, nq = 0;
+  bool ok = true;
+  for (int k = 0; k < ntiles; ++k) {
+    if (*abort_flag) { ok = false; break; }
+    if (k == 0 || ld.lt == 0) {              // a segment starts: its header and Q rows
+      const int slot = nq & 1;
+      if (!mbar_wait(rg.qempty + 8 * slot, ((nq >> 1) & 1) ^ 1)) { ok = false; break; }
+      const uint32_t qs = rg.q + slot * C::kQSlotB;
+      if (lane == 0) {
+        *reinterpret_cast<SeqInfo *>(smem + (qs - rg.base)) = s;
+        mbar_arrive_tx(rg.qfull + 8 * slot, static_cast<uint32_t>(s.M * D * 2));
+      }
+      __syncwarp();
+      for (int m = lane; m < s.M; m += 32) {
+        const int j = m / P.g, hg = m - j * P.g;
+        bulk_g2s(qs + C::kQHead + prow<D>(m, 0),
+                 P.q + (static_cast<int64_t>(s.r0 + j) * P.Hq + s.hk * P.g + hg) * D, D * 2,
+                 rg.qfull + 8 * slot);
+      }
+      ++nq;
+    }
+    if (!mbar_wait(rg.empty + 8 * st, ph ^ 1)) { ok = false; break; }
+    {
+      // K and V rows of the tile: lane owns chunk lane % CH of rows lane / CH + RPP * p
+      constexpr int CH = D / 8;                 // 16-byte chunks per row
+      constexpr int RPP = 32 / CH;              // rows per pass of the warp
+      constexpr int NPASS = kTileKeys / RPP;
+      const int ch = lane % CH, rr = lane / CH;
+      const uint32_t kdst = rg.base + st * C::kStageB, vdst = kdst + C::kTileB;
+      const int key0 = ld.lt * kTileKeys;
+      if (key0 + kTileKeys <= s.L) {            // whole tile inside the cache
+        const int64_t off = ((s.kv0 + key0 + rr) * P.Hkv + s.hk) * D + ch * 8;
+        const int64_t step = static_cast<int64_t>(RPP) * P.Hkv * D;
+#pragma unroll 8
+        for (int p = 0; p < NPASS; ++p) {
+          const int row = rr + p * RPP;
+          cp_async16_hint(kdst + swz<D>(row, ch), P.k_cache + off + p * step, 16, pol);
+          cp_async16_hint(vdst + swz<D>(row, ch), P.v_cache + off + p * step, 16, pol);
+        }
+      } else {
+#pragma unroll 4
+        for (int p = 0; p < NPASS; ++p) {
+          const int row = rr + p * RPP, key = key0 + row;
+          const uint16_t *kb = P.k_new, *vb = P.v_new;
+          int64_t off = 0;
+          int bytes = 0;
+          if (key < s.L) {
+            off = ((s.kv0 + key) * P.Hkv + s.hk) * D + ch * 8;
+            kb = P.k_cache;
+            vb = P.v_cache;
+            bytes = 16;
+          } else if (key < s.L + s.Ri) {
+            off = (static_cast<int64_t>(s.r0 + key - s.L) * P.Hkv + s.hk) * D + ch * 8;
+            bytes = 16;
+          }
+          cp_async16(kdst + swz<D>(row, ch), kb + off, bytes);
+          cp_async16(vdst + swz<D>(row, ch), vb + off, bytes);
+        }
+      }
+      cp_async_arrive(rg.full + 8 * st);
+    }
+    ++issued;
+    if (++st == NS) { st = 0; ph ^= 1; }
+    if (cursor_advance(ld, S) && k + 1 < ntiles) s = load_seq(P, S, ld);
+  }
+  if (!ok && lane == 0) {
+    set_status(P.dev_status, SV_DEV_TIMEOUT);
+    *abort_flag = 1;
+  }
+  {
+    // Before leaving, every copy this warp started must have landed: wait for
+    // the last fill of each stage and Q slot (all earlier fills completed
+    // before the slot could be refilled).
+    for (int s2 = 0; s2 < NS && s2 < issued; ++s2) {
+      const int last = s2 + (issued - 1 - s2) / NS * NS;
+      mbar_wait(rg.full + 8 * s2, (last / NS) & 1);
+    }
+    for (int s2 = 0; s2 < 2 && s2 < nq; ++s2) {
+      const int last = s2 + (nq - 1 - s2) / 2 * 2;
+      mbar_wait(rg.qfull + 8 * s2, (last >> 1) & 1);
+    }
+  }
+}
+
 template <int D, int RS, int NB>
 __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned char *smem) {
-  using SM = AttnSmem<D, RS, NB>;
-  constexpr int NT = SM::kThreads;
+  using C = AttnCfg<D, RS, NB>;
   constexpr int KS = D / 16;          // k-steps of K.Q^T
   constexpr int DM = D / 16;          // m-tiles of V^T.P^T
-  constexpr int RW = SM::kRowsW;
-  constexpr int OS = SM::kOStride;
-  const uint32_t sbase = smem_u32(smem);
-  int64_t *ubase = reinterpret_cast<int64_t *>(smem + SM::kOffStages);  // before the pipeline
-  int *misc = reinterpret_cast<int *>(smem + SM::kOffMisc);
-  float *merge_o = reinterpret_cast<float *>(smem + SM::kOffMergeO);
-  float2 *merge_ml = reinterpret_cast<float2 *>(smem + SM::kOffMergeML);
-  float2 *fin = reinterpret_cast<float2 *>(smem + SM::kOffFinal);
-  int64_t *misc64 = reinterpret_cast<int64_t *>(misc + 8);
+  constexpr int RW = C::kRowsW;
+  constexpr int OS = C::kOStride;
+  constexpr int NC = C::kCW * 32;     // consumer threads
+  const SmemMap &Mp = P.sm;
+  const int NS = Mp.ns;
+  Ring rg;
+  rg.base = smem_u32(smem);
+  rg.q = rg.base + Mp.q;
+  rg.full = rg.base + Mp.bars;
+  rg.empty = rg.full + 8 * NS;
+  rg.qfull = rg.empty + 8 * NS;
+  rg.qempty = rg.qfull + 16;
+  rg.ebar = rg.qempty + 16;
+  int64_t *ubase = reinterpret_cast<int64_t *>(smem);     // staged in the ring before it starts
+  int *misc = reinterpret_cast<int *>(smem + Mp.misc);
+  int64_t *misc64 = reinterpret_cast<int64_t *>(smem + Mp.misc + 16);
+  volatile int *abort_flag = misc + 1;
+  float *merge_o = reinterpret_cast<float *>(smem + Mp.merge_o);
+  float2 *merge_ml = reinterpret_cast<float2 *>(smem + Mp.merge_ml);
+  float2 *fin = reinterpret_cast<float2 *>(smem + Mp.fin);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ks = warp % kKW, rs = warp / kKW;
-  const int r = lane >> 2, q = lane & 3;
-  const int g = P.g;
-
-  Sched S = sched_view(smem + SM::kOffSched, P.mode, P.Hkv);
-  const int64_t W = build_sched<NT>(P, S, ubase, misc64);
+  Sched S = sched_view(smem + Mp.sched, P.mode, P.Hkv, Mp.units_cap, Mp.groups_cap);
+  const int64_t W = build_sched<C::kThreads>(P, S, ubase, misc64);
   if (W <= 0) return;
   if (W > P.tiles_bound) {
     if (blockIdx.x == 0 && tid == 0) set_status(P.dev_status, SV_DEV_BAD_LENGTH);
@@ -362,42 +529,44 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     cur.lt = static_cast<int>(rel - static_cast<int64_t>(cur.s) * S.nt[lo]);
   }
   int64_t seg_first_tile = t_begin - cur.lt;   // global index of the segment's tile 0
-  __syncthreads();                            // ubase dead: tile buffers free
-
-  // ---- prologue: first kStages-1 tiles in flight
-  Cursor ld = cur;
-  SeqInfo ld_s = load_seq(P, S, ld);
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (st < ntiles) {
-      if (tid < 128) issue_tile_loads<D>(P, ld_s, ld_s.hk, ld.lt, sbase + st * SM::kStageBytes);
-      if (cursor_advance(ld, S) && st + 1 < ntiles) ld_s = load_seq(P, S, ld);
+  if (tid == 0) {
+    for (int s2 = 0; s2 < NS; ++s2) {
+      mbar_init(rg.full + 8 * s2, 32);          // one cp.async arrival per producer lane
+      mbar_init(rg.empty + 8 * s2, C::kCW);
     }
-    cp_async_commit();
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(rg.qfull + 8 * s2, 1);
+      mbar_init(rg.qempty + 8 * s2, C::kCW);
+    }
+    mbar_init(rg.ebar, NC);
+    misc[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  // the ring held ubase (generic writes): order them before the async copies
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  __syncthreads();
+
+  if (warp == C::kCW) {
+    attn_produce<D, RS, NB>(P, S, cur, ntiles, rg, smem, abort_flag);
+    return;
   }
 
-  SeqInfo cs = load_seq(P, S, cur);
-  uint32_t qf[KS][NB][2];          // Q^T B-fragments of this warp's rows
+  // ================================ consumers ================================
+  const int ks = warp % kKW, rs = warp / kKW;
+  const int r = lane >> 2, q = lane & 3;
+  const int g = P.g;
+  const int row_w0 = rs * RW;      // first packed row of this warp
+  uint32_t ephase = 0;
+  bool ok = true;
+  // consumer-group barrier (bounded)
+  auto csync = [&]() {
+    mbar_arrive(rg.ebar);
+    if (!mbar_wait(rg.ebar, ephase)) ok = false;
+    ephase ^= 1;
+  };
+
   float o[DM][NB][4];              // O^T accumulators
   float m_run[NB][2], l_run[NB][2];
-  const int row_w0 = rs * RW;      // first packed row of this warp
-  bool active = row_w0 < cs.M;
-
-  auto load_q = [&]() {
-    const int M = cs.M;
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int m = row_w0 + nb * 8 + r;
-      const bool ok = m < M;
-      const int j = ok ? m / g : 0, hg = ok ? m - j * g : 0;
-      const uint16_t *qrow = P.q + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D;
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qf[kk][nb][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + 2 * q) : 0u;
-        qf[kk][nb][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + 8 + 2 * q) : 0u;
-      }
-    }
-  };
   auto reset_state = [&]() {
 #pragma unroll
     for (int dm = 0; dm < DM; ++dm)
@@ -409,23 +578,34 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       l_run[nb][0] = l_run[nb][1] = 0.0f;
     }
   };
-  load_q();
-  reset_state();
 
-  for (int k = 0; k < ntiles; ++k) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    {   // refill the stage consumed at k-1
-      const int kn = k + kStages - 1;
-      if (kn < ntiles) {
-        if (tid < 128) issue_tile_loads<D>(P, ld_s, ld_s.hk, ld.lt, sbase + (kn % kStages) * SM::kStageBytes);
-        if (cursor_advance(ld, S) && kn + 1 < ntiles) ld_s = load_seq(P, S, ld);
-      }
-      cp_async_commit();
-    }
+  int nq = 0, st = 0;
+  uint32_t ph = 0;
+  SeqInfo cs;
+  uint32_t qslot = 0;
+  bool active = false;
+  auto begin_segment = [&]() -> bool {
+    const int slot = nq & 1;
+    if (!mbar_wait(rg.qfull + 8 * slot, (nq >> 1) & 1)) return false;
+    qslot = rg.q + slot * C::kQSlotB;
+    cs = *reinterpret_cast<const SeqInfo *>(smem + (qslot - rg.base));
+    active = row_w0 < cs.M;
+    reset_state();
+    return true;
+  };
+  auto end_segment = [&]() {     // Q slot no longer read by this warp
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rg.qempty + 8 * (nq & 1));
+    ++nq;
+  };
+  ok = begin_segment();
+
+  for (int k = 0; k < ntiles && ok; ++k) {
+    if (!mbar_wait(rg.full + 8 * st, ph)) { ok = false; break; }
     if (active) {
-      const uint32_t kbase = sbase + (k % kStages) * SM::kStageBytes;
-      const uint32_t vbase = kbase + SM::kTileBytes;
+      const uint32_t kbase = rg.base + st * C::kStageB;
+      const uint32_t vbase = kbase + C::kTileB;
+      const uint32_t qrows = qslot + C::kQHead;
       // ---- S^T = K Q^T for this warp's 16 keys
       float sacc[NB][4];
 #pragma unroll
@@ -433,11 +613,19 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       {
         const int krow = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          uint32_t a[4];
-          ldmatrix_x4(kbase + swz<D>(krow, kk * 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        for (int kk = 0; kk < KS; kk += 2) {
+          uint32_t qb[NB][4];
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sacc[nb], a, qf[kk][nb][0], qf[kk][nb][1]);
+          for (int nb = 0; nb < NB; ++nb)
+            ldmatrix_x4(qrows + prow<D>(row_w0 + nb * 8 + (lane & 7), (kk + (lane >> 4)) * 2 + ((lane >> 3) & 1)),
+                        qb[nb][0], qb[nb][1], qb[nb][2], qb[nb][3]);
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            uint32_t a[4];
+            ldmatrix_x4(kbase + swz<D>(krow, (kk + k2) * 2 + (lane >> 4)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sacc[nb], a, qb[nb][2 * k2], qb[nb][2 * k2 + 1]);
+          }
         }
       }
       // ---- mask (only in tiles reaching past the cache) + online softmax
@@ -462,8 +650,8 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const float m_new = fmaxf(m_run[nb][e], mx);
           const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-          const float alpha = exp2f(m_run[nb][e] - m_use);
-          const float p0 = exp2f(v0 - m_use), p1 = exp2f(v1 - m_use);
+          const float alpha = fast_exp2(m_run[nb][e] - m_use);
+          const float p0 = fast_exp2(v0 - m_use), p1 = fast_exp2(v1 - m_use);
           l_run[nb][e] = l_run[nb][e] * alpha + (p0 + p1);
           m_run[nb][e] = m_new;
           pv[e] = p0;
@@ -491,6 +679,9 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rg.empty + 8 * st);    // stage free for the producer
+    if (++st == NS) { st = 0; ph ^= 1; }
 
     const bool seg_end = cur.lt + 1 == cs.nt;
     const bool last = k + 1 == ntiles;
@@ -498,6 +689,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       ++cur.lt;
       continue;
     }
+    end_segment();
     // ================= end of a piece: merge the key-slice warps =================
     const int Mi = cs.M;
 #pragma unroll
@@ -510,22 +702,22 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
         lv += __shfl_xor_sync(0xffffffffu, lv, 16);
         if (r == 0) merge_ml[warp * RW + nb * 8 + 2 * q + e] = make_float2(m_run[nb][e], lv);
       }
-    __syncthreads();
-    if (tid < SM::kRows) {            // merged (max, sum) of packed row tid
-      const int rg = tid / RW, rl = tid - rg * RW;
+    csync();
+    if (tid < C::kRows) {             // merged (max, sum) of packed row tid
+      const int rg2 = tid / RW, rl = tid - rg2 * RW;
       float mm = -INFINITY;
 #pragma unroll
-      for (int w2 = 0; w2 < kKW; ++w2) mm = fmaxf(mm, merge_ml[(rg * kKW + w2) * RW + rl].x);
+      for (int w2 = 0; w2 < kKW; ++w2) mm = fmaxf(mm, merge_ml[(rg2 * kKW + w2) * RW + rl].x);
       const float mu = mm == -INFINITY ? 0.0f : mm;
       float ll = 0.0f;
 #pragma unroll
       for (int w2 = 0; w2 < kKW; ++w2) {
-        const float2 v = merge_ml[(rg * kKW + w2) * RW + rl];
-        ll += v.y * exp2f(v.x - mu);
+        const float2 v = merge_ml[(rg2 * kKW + w2) * RW + rl];
+        ll += v.y * fast_exp2(v.x - mu);
       }
       fin[tid] = make_float2(mm, ll);
     }
-    __syncthreads();
+    csync();
     // O^T of the 4 key slices into the row-major buffer, in a fixed order
     for (int step = kKW - 1; step >= 0; --step) {
       if (ks == step) {
@@ -535,7 +727,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
           for (int e = 0; e < 2; ++e) {
             const int m = row_w0 + nb * 8 + 2 * q + e;
             const float mm = fin[m].x;
-            const float sc = exp2f(m_run[nb][e] - (mm == -INFINITY ? 0.0f : mm));
+            const float sc = fast_exp2(m_run[nb][e] - (mm == -INFINITY ? 0.0f : mm));
             float *dst = merge_o + m * OS;
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm) {
@@ -551,15 +743,15 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
             }
           }
       }
-      __syncthreads();
+      csync();
     }
     const int seg = cs.seg;
     const int64_t c_first = cta_of_tile(seg_first_tile, W, G);
     const int64_t c_last = cta_of_tile(seg_first_tile + cs.nt - 1, W, G);
     const int npieces = static_cast<int>(c_last - c_first + 1);
-    constexpr int rows_m = SM::kRows;
+    constexpr int rows_m = C::kRows;
     if (npieces == 1 && P.mode == 0) {   // the whole segment is here: normalize, store
-      for (int e = tid; e < Mi * (D / 2); e += NT) {
+      for (int e = tid; e < Mi * (D / 2); e += NC) {
         const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
         const float lsum = fin[m].y;
         const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
@@ -569,7 +761,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       }
     } else {                          // partial: slot = CTA index + segment index
       const int64_t slot = static_cast<int64_t>(blockIdx.x) + seg;
-      for (int e = tid; e < Mi * (D / 2); e += NT) {
+      for (int e = tid; e < Mi * (D / 2); e += NC) {
         const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
         *reinterpret_cast<float2 *>(P.part_o + (slot * rows_m + m) * D + d) =
             make_float2(merge_o[m * OS + d], merge_o[m * OS + d + 1]);
@@ -578,15 +770,15 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     }
     if (npieces > 1 && P.mode == 0) {    // plain mode: the last piece merges
       __threadfence();
-      __syncthreads();
+      csync();
       if (tid == 0) {
         const unsigned old = atomicInc(&P.counters[seg], static_cast<unsigned>(npieces - 1));
         misc[0] = old == static_cast<unsigned>(npieces - 1) ? 1 : 0;
       }
-      __syncthreads();
+      csync();
       if (misc[0]) {                   // last piece to arrive merges the segment
         __threadfence();
-        for (int e = tid; e < Mi * (D / 2); e += NT) {
+        for (int e = tid; e < Mi * (D / 2); e += NC) {
           const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
           float mm = -INFINITY;
           for (int c = 0; c < npieces; ++c)
@@ -596,7 +788,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
           for (int c = 0; c < npieces; ++c) {
             const int64_t slot2 = c_first + c + seg;
             const float2 ml = __ldcg(&P.part_ml[slot2 * rows_m + m]);
-            const float f = exp2f(ml.x - mu);
+            const float f = fast_exp2(ml.x - mu);
             const float2 ov = __ldcg(reinterpret_cast<const float2 *>(P.part_o + (slot2 * rows_m + m) * D + d));
             n0 += f * ov.x;
             n1 += f * ov.y;
@@ -609,25 +801,24 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
         }
       }
     }
-    __syncthreads();                   // merge buffers reusable
-    if (last) break;
+    csync();                           // merge buffers reusable
+    if (last || !ok) break;
     seg_first_tile += cs.nt;
     cursor_advance(cur, S);
-    cs = load_seq(P, S, cur);
-    active = row_w0 < cs.M;
-    load_q();
-    reset_state();
+    if (!begin_segment()) { ok = false; break; }
   }
-  cp_async_wait<0>();
+  if (!ok && lane == 0) {
+    set_status(P.dev_status, SV_DEV_TIMEOUT);
+    *abort_flag = 1;
+  }
 }
 
 template <int D, int RS, int NB>
-__global__ void __launch_bounds__(AttnSmem<D, RS, NB>::kThreads)
+__global__ void __launch_bounds__(AttnCfg<D, RS, NB>::kThreads)
     attn_bf16_kernel(const AttnParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
+  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   attn_bf16_body<D, RS, NB>(P, smem);
-  // A dependent launch (fused step) must not complete before its primary.
-  if (P.pdl_secondary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -650,8 +841,9 @@ template <int D>
 __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const MergeParams MP) {
   extern __shared__ __align__(16) unsigned char msm[];
   constexpr int kTables = kMaxBatch * 4 + 4 * kMaxGroups * 4;
-  Sched Sd = sched_view(msm, 1, MP.P.Hkv);
-  Sched Sp = sched_view(msm + kTables, 2, MP.P.Hkv);
+  if (MP.P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  Sched Sd = sched_view(msm, 1, MP.P.Hkv, kMaxBatch, kMaxGroups);
+  Sched Sp = sched_view(msm + kTables, 2, MP.P.Hkv, kMaxBatch, kMaxGroups);
   int64_t *ud = reinterpret_cast<int64_t *>(msm + 2 * kTables);
   int64_t *up = ud + kMaxBatch;
   int64_t *scratch = up + kMaxGroups;
@@ -746,6 +938,7 @@ __global__ void __launch_bounds__(kF32NT) attn_f32_kernel(const AttnParams P, co
   float (*Qs)[D] = reinterpret_cast<float (*)[D]>(fsm);
   float (*Ks)[D + 1] = reinterpret_cast<float (*)[D + 1]>(fsm + F32Smem<D>::kQ);
   float (*Vs)[D] = reinterpret_cast<float (*)[D]>(fsm + F32Smem<D>::kQ + F32Smem<D>::kK);
+  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int seg = blockIdx.x;
   const int i = seg / P.Hkv, hk = seg - i * P.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -754,7 +947,6 @@ __global__ void __launch_bounds__(kF32NT) attn_f32_kernel(const AttnParams P, co
   if (r0 < 0 || Ri < 1 || Ri > P.max_q_rows || r0 + Ri > P.num_rows || L < 0 || kv0 < 0 ||
       kv0 + L > P.pool_rows) {
     if (tid == 0) set_status(P.dev_status, SV_DEV_BAD_LENGTH);
-    if (P.pdl_secondary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     return;
   }
   const int g = P.g, M = Ri * g;
@@ -825,38 +1017,50 @@ __global__ void __launch_bounds__(kF32NT) attn_f32_kernel(const AttnParams P, co
     for (int c = 0; c < DL; ++c)
       out[(static_cast<int64_t>(r0 + j) * P.Hq + hk * g + hg) * D + lane + 32 * c] = o[a][c] * inv;
   }
-  if (P.pdl_secondary) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+
+template <int D, int RS, int NB>
+SmemMap smem_map_for(const AttnParams &P, int ns) {
+  using C = AttnCfg<D, RS, NB>;
+  return P.mode == 2 ? C::map(ns, P.G, P.G) : C::map(ns, P.B, 1);
+}
+
+// Ring stages for a launch: as many as fit in smem_cap (2..kMaxStages).
+template <int D, int RS, int NB>
+int stages_for(const AttnParams &P, int smem_cap) {
+  int ns = kMaxStages;
+  while (ns > 2 && smem_map_for<D, RS, NB>(P, ns).total > smem_cap) --ns;
+  return ns;
 }
 
 template <int D, int RS, int NB>
-cudaError_t launch_bf16(const AttnParams &P, int grid, cudaStream_t s) {
-  using SM = AttnSmem<D, RS, NB>;
+cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int *grid_used,
+                        cudaStream_t s) {
+  using C = AttnCfg<D, RS, NB>;
+  AttnLaunchOpts opt = o;
+  // room beside another kernel's CTA only pays with at least 3 stages in flight
+  if (opt.smem_min > 0 && (stages_for<D, RS, NB>(P, opt.smem_cap) < 3 ||
+                           smem_map_for<D, RS, NB>(P, 3).total > opt.smem_cap)) {
+    opt.smem_cap = kSmemMax;
+    opt.smem_min = 0;
+  }
+  P.sm = smem_map_for<D, RS, NB>(P, stages_for<D, RS, NB>(P, opt.smem_cap));
+  const int bytes = std::max(P.sm.total, opt.smem_min);
   auto kern = attn_bf16_kernel<D, RS, NB>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, bytes);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(max_grid, std::max(occ, 1) * o.num_sms));
+  *grid_used = grid;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(SM::kThreads);
-  cfg.dynamicSmemBytes = SM::kBytes;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = P.pdl_secondary ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, P);
-}
-
-template <int D, int RS, int NB>
-int occupancy_bf16() {
-  using SM = AttnSmem<D, RS, NB>;
-  auto kern = attn_bf16_kernel<D, RS, NB>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes) != cudaSuccess)
-    return 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, SM::kThreads, SM::kBytes) != cudaSuccess)
-    return 1;
-  return n > 0 ? n : 1;
 }
 
 // Row configuration for rows_m packed rows: (RS, NB) with RS*8*NB >= rows_m.
@@ -867,31 +1071,14 @@ int row_config(int rows_m) {
 int config_rows(int rc) { static const int rows[5] = {8, 16, 32, 48, 64}; return rows[rc]; }
 
 template <int D>
-int occupancy_d(int rc) {
+cudaError_t launch_d(const AttnParams &P, const AttnLaunchOpts &o, int rc, int max_grid, int *grid,
+                     cudaStream_t s) {
   switch (rc) {
-    case 0: return occupancy_bf16<D, 1, 1>();
-    case 1: return occupancy_bf16<D, 1, 2>();
-    case 2: return occupancy_bf16<D, 2, 2>();
-    case 3: return occupancy_bf16<D, 3, 2>();
-    default: return occupancy_bf16<D, 4, 2>();
-  }
-}
-
-int occupancy_for(int D, int rc) {
-  static int cache[2][5] = {{0}};
-  const int di = D == 128 ? 1 : 0;
-  if (cache[di][rc] == 0) cache[di][rc] = D == 64 ? occupancy_d<64>(rc) : occupancy_d<128>(rc);
-  return cache[di][rc];
-}
-
-template <int D>
-cudaError_t launch_d(const AttnParams &P, int rc, int grid, cudaStream_t s) {
-  switch (rc) {
-    case 0: return launch_bf16<D, 1, 1>(P, grid, s);
-    case 1: return launch_bf16<D, 1, 2>(P, grid, s);
-    case 2: return launch_bf16<D, 2, 2>(P, grid, s);
-    case 3: return launch_bf16<D, 3, 2>(P, grid, s);
-    default: return launch_bf16<D, 4, 2>(P, grid, s);
+    case 0: return launch_bf16<D, 1, 1>(P, o, max_grid, grid, s);
+    case 1: return launch_bf16<D, 1, 2>(P, o, max_grid, grid, s);
+    case 2: return launch_bf16<D, 2, 2>(P, o, max_grid, grid, s);
+    case 3: return launch_bf16<D, 3, 2>(P, o, max_grid, grid, s);
+    default: return launch_bf16<D, 4, 2>(P, o, max_grid, grid, s);
   }
 }
 
@@ -909,11 +1096,9 @@ AttnPlan plan_attention(const sv_attn_args &a, int num_sms) {
   // sum over sequences of ceil((L_i + R_i) / 64), per KV head
   p.tiles_bound = static_cast<int64_t>(a.num_kv_heads) *
                   ((a.kv_rows_bound + a.num_rows) / kTileKeys + a.batch);
+  // persistent CTAs: the launch takes min(grid, SMs x resident CTAs per SM)
   p.grid = std::min<int64_t>(kMaxGrid, std::max<int64_t>(1, p.tiles_bound));
-  if (a.dtype == SV_BF16 && num_sms > 0) {
-    const int occ = occupancy_for(a.head_dim, p.row_cfg);
-    p.grid = std::min<int64_t>(p.grid, static_cast<int64_t>(num_sms) * occ);
-  }
+  (void)num_sms;
   p.prefix = a.num_groups > 0;
   p.spb = std::max(1, config_rows(kPrefixCfg) / p.rows_m);
   p.pre_grid = p.pre_tiles_bound = p.pre_slots = 0;
@@ -922,10 +1107,6 @@ AttnPlan plan_attention(const sv_attn_args &a, int num_sms) {
     p.pre_tiles_bound = static_cast<int64_t>(a.num_kv_heads) * rb_max *
                         (a.prefix_rows_bound / kTileKeys + a.num_groups);
     p.pre_grid = std::min<int64_t>(kMaxGrid, std::max<int64_t>(1, p.pre_tiles_bound));
-    if (num_sms > 0) {
-      const int occ = occupancy_for(a.head_dim, kPrefixCfg);
-      p.pre_grid = std::min<int64_t>(p.pre_grid, static_cast<int64_t>(num_sms) * occ);
-    }
     p.pre_slots = p.pre_grid + static_cast<int64_t>(a.num_kv_heads) *
                                    (a.batch / p.spb + 1 + a.num_groups);
   }
@@ -938,9 +1119,9 @@ int attention_slot_rows(const AttnPlan &p) { return config_rows(p.row_cfg); }
 int attention_prefix_rows() { return config_rows(kPrefixCfg); }
 
 cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const AttnWs &ws,
-                             bool pdl_secondary, cudaStream_t s) {
+                             const AttnLaunchOpts &opts, cudaStream_t s) {
   if (a.batch <= 0) return cudaSuccess;
-  AttnParams P;
+  AttnParams P{};
   P.B = a.batch;
   P.Hq = a.num_q_heads;
   P.Hkv = a.num_kv_heads;
@@ -964,7 +1145,7 @@ cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const Att
   P.counters = ws.counters;
   P.dev_status = a.dev_status;
   P.tiles_bound = p.tiles_bound;
-  P.pdl_secondary = pdl_secondary ? 1 : 0;
+  P.pdl_primary = 0;
   P.mode = 0;
   P.G = a.num_groups;
   P.spb = p.spb;
@@ -972,56 +1153,54 @@ cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const Att
   P.prefix_start = a.prefix_start;
   P.prefix_len = a.prefix_len;
   if (a.dtype == SV_F32) {
+    P.pdl_primary = opts.pdl_primary ? 1 : 0;
     const int grid = a.batch * a.num_kv_heads;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kF32NT);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_secondary ? 1 : 0;
     const float *q = static_cast<const float *>(a.q), *kn = static_cast<const float *>(a.k_new),
                 *vn = static_cast<const float *>(a.v_new), *kc = static_cast<const float *>(a.k_cache),
                 *vc = static_cast<const float *>(a.v_cache);
     float *out = static_cast<float *>(a.out);
     if (a.head_dim == 64) {
-      cfg.dynamicSmemBytes = F32Smem<64>::kBytes;
       cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            F32Smem<64>::kBytes);
       if (e != cudaSuccess) return e;
-      return cudaLaunchKernelEx(&cfg, attn_f32_kernel<64>, P, q, kn, vn, kc, vc, out);
+      attn_f32_kernel<64><<<grid, kF32NT, F32Smem<64>::kBytes, s>>>(P, q, kn, vn, kc, vc, out);
+      return cudaGetLastError();
     }
-    cfg.dynamicSmemBytes = F32Smem<128>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          F32Smem<128>::kBytes);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, attn_f32_kernel<128>, P, q, kn, vn, kc, vc, out);
+    attn_f32_kernel<128><<<grid, kF32NT, F32Smem<128>::kBytes, s>>>(P, q, kn, vn, kc, vc, out);
+    return cudaGetLastError();
   }
   const bool d64 = a.head_dim == 64;
+  int grid = 0, pgrid = 0;
   if (!p.prefix) {
-    const int grid = static_cast<int>(p.grid);
-    return d64 ? launch_d<64>(P, p.row_cfg, grid, s) : launch_d<128>(P, p.row_cfg, grid, s);
+    P.pdl_primary = opts.pdl_primary ? 1 : 0;
+    const int mg = static_cast<int>(p.grid);
+    return d64 ? launch_d<64>(P, opts, p.row_cfg, mg, &grid, s)
+               : launch_d<128>(P, opts, p.row_cfg, mg, &grid, s);
   }
   // shared prefix: prefix row-blocks, then decode segments, then the merge
+  // (only the merge lets a following launch start early)
+  AttnLaunchOpts wide = opts;
+  wide.smem_min = 0;
   AttnParams Pp = P;
   Pp.mode = 2;
   Pp.part_o = ws.pre_o;
   Pp.part_ml = reinterpret_cast<float2 *>(ws.pre_ml);
   Pp.tiles_bound = p.pre_tiles_bound;
-  const int pgrid = static_cast<int>(p.pre_grid);
-  cudaError_t e = d64 ? launch_d<64>(Pp, kPrefixCfg, pgrid, s) : launch_d<128>(Pp, kPrefixCfg, pgrid, s);
+  const int mpg = static_cast<int>(p.pre_grid);
+  cudaError_t e = d64 ? launch_d<64>(Pp, wide, kPrefixCfg, mpg, &pgrid, s)
+                      : launch_d<128>(Pp, wide, kPrefixCfg, mpg, &pgrid, s);
   if (e != cudaSuccess) return e;
   AttnParams Pd = P;
   Pd.mode = 1;
-  Pd.pdl_secondary = 0;
-  const int grid = static_cast<int>(p.grid);
-  e = d64 ? launch_d<64>(Pd, p.row_cfg, grid, s) : launch_d<128>(Pd, p.row_cfg, grid, s);
+  const int mg = static_cast<int>(p.grid);
+  e = d64 ? launch_d<64>(Pd, wide, p.row_cfg, mg, &grid, s) : launch_d<128>(Pd, wide, p.row_cfg, mg, &grid, s);
   if (e != cudaSuccess) return e;
   MergeParams MP;
   MP.P = Pd;
+  MP.P.pdl_primary = opts.pdl_primary ? 1 : 0;
   MP.dec_o = ws.dec_o;
   MP.dec_ml = reinterpret_cast<const float2 *>(ws.dec_ml);
   MP.dec_rows = config_rows(p.row_cfg);

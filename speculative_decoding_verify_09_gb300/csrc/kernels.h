@@ -11,6 +11,7 @@ namespace sv {
 
 constexpr int kMaxQRows = 16;   // bound on K_i + 1 block rows per sequence
 constexpr int kMaxRowsM = 64;   // bound on (K_i + 1) * (Hq / Hkv) packed query rows
+constexpr int kSmemMax = 227 * 1024;   // dynamic shared memory one CTA may ask for
 
 // Per logits row statistics written by the sampler's first phase.
 struct RowStats {
@@ -62,7 +63,7 @@ struct SamplerLaunch {
   SamplerPlan plan;
   bool do_append;
   AppendView app;
-  bool pdl_primary;         // trigger dependent launch at kernel start
+  bool pdl_secondary;       // launched early behind the attention: wait for it at the end
 };
 
 SamplerPlan plan_sampler(const sv_sample_args &a);
@@ -81,7 +82,7 @@ struct AttnPlan {
   int rows_m;           // packed query rows per (sequence, KV head): max_q_rows * Hq/Hkv
   int row_cfg;          // kernel row configuration (rows per CTA: 8, 16, 32, 48, 64)
   int m_tiles;          // partial-slot rows / 16
-  int64_t grid;         // persistent CTAs (bf16 path)
+  int64_t grid;         // bound on the persistent CTAs (bf16 path; sizes the partials)
   int64_t tiles_bound;  // bound on the global count of 64-key tiles
   // shared-prefix arrangement (num_groups > 0)
   bool prefix;
@@ -102,7 +103,16 @@ int attention_max_batch();
 int attention_max_groups();
 int attention_slot_rows(const AttnPlan &p);   // rows per decode partial slot
 int attention_prefix_rows();                  // rows per prefix partial slot
+// How one attention call is launched.
+struct AttnLaunchOpts {
+  bool pdl_primary;     // the next launch on the stream may start at once
+  int smem_cap;         // shared memory budget of one CTA (sets the ring depth)
+  int smem_min;         // ask for at least this much (0: no floor)
+  int num_sms;          // SMs of the device (grid = SMs x resident CTAs per SM)
+};
 cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const AttnWs &ws,
-                             bool pdl_secondary, cudaStream_t s);
+                             const AttnLaunchOpts &opts, cudaStream_t s);
+// Shared memory the cluster sampler asks for per CTA (0 if it is not used).
+int sampler_cluster_smem(const SamplerPlan &p);
 
 }  // namespace sv

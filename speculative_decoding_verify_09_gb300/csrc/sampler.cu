@@ -196,7 +196,17 @@ struct SampParams {
   int do_append;
   AppendView app;
   float c_hi, c_lo;   // log2(e)/T as two floats
-  int pdl_primary;
+  int pdl_secondary;  // launched early behind another grid (see PdlTail)
+};
+
+// A launch that may start before the previous grid on its stream has finished
+// (programmatic dependent launch) must not finish before it: every exit path
+// of such a kernel waits for the previous grid first.
+struct PdlTail {
+  int on;
+  __device__ __forceinline__ ~PdlTail() {
+    if (on) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  }
 };
 
 struct SampSmem {
@@ -487,6 +497,7 @@ constexpr int kStatVec = 4;          // vectors per thread per chunk
 
 template <typename T>
 __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P) {
+  const PdlTail tail{P.pdl_secondary};
   constexpr int EPV = LT<T>::EPV;
   constexpr int NW = kStatNT / 32;
   __shared__ float redf[NW];
@@ -624,6 +635,7 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
 // --------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) {
+  const PdlTail tail{P.pdl_secondary};
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SampSmem &sm = *reinterpret_cast<SampSmem *>(smem_raw);
   const sv_sample_args &a = P.a;
@@ -788,7 +800,6 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 
 template <typename T>
 __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
-  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
   __shared__ DrawSmem sm;
   __shared__ unsigned long long scan_red[kDrawNT / 32];
   const sv_sample_args &a = P.a;
@@ -982,7 +993,7 @@ __device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
 
 template <typename T>
 __global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampParams P) {
-  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n");
+  const PdlTail tail{P.pdl_secondary};
   extern __shared__ __align__(16) unsigned char csm_raw[];
   ClusterSmem &sm = *reinterpret_cast<ClusterSmem *>(csm_raw);
   uint4 *slice = reinterpret_cast<uint4 *>(csm_raw + (sizeof(ClusterSmem) + 127) / 128 * 128);
@@ -1390,10 +1401,14 @@ int sampler_max_vocab(int dtype) {
   return kMaxTiles * kSampNT * (dtype == SV_BF16 ? 8 : 4);
 }
 
+int sampler_cluster_smem(const SamplerPlan &p) {
+  return p.cluster ? static_cast<int>((sizeof(ClusterSmem) + 127) / 128 * 128) + kClSmemRows : 0;
+}
+
 template <typename T>
 static cudaError_t launch_cluster(const SampParams &P, cudaStream_t s) {
   auto kern = sampler_cluster_kernel<T>;
-  const int smem = static_cast<int>((sizeof(ClusterSmem) + 127) / 128 * 128) + kClSmemRows;
+  const int smem = sampler_cluster_smem(P.plan);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1403,13 +1418,33 @@ static cudaError_t launch_cluster(const SampParams &P, cudaStream_t s) {
   cfg.blockDim = dim3(kClNT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterN;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = P.pdl_secondary ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// Launch of the first kernel of a path, early (programmatic) when the sampler
+// runs behind another grid.
+template <typename K>
+static cudaError_t launch_first(K kern, int grid, int block, size_t smem, const SampParams &P,
+                                cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = P.pdl_secondary ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
@@ -1423,15 +1458,14 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
     (void)cudaGetLastError();          // no room for a cluster: two-kernel path
   }
   if (P.plan.stat_chunks > 1 || P.a.top_p >= 1.0f) {
-    stats_chunk_kernel<T><<<rows * P.plan.stat_chunks, kStatNT, 0, s>>>(P);
+    e = launch_first(stats_chunk_kernel<T>, rows * P.plan.stat_chunks, kStatNT, 0, P, s);
   } else {
     const size_t smem = kSmemRowOff + kRowSmemBytes;
     e = cudaFuncSetAttribute(stats_row_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    stats_row_kernel<T><<<rows, kSampNT, smem, s>>>(P);
+    e = launch_first(stats_row_kernel<T>, rows, kSampNT, smem, P, s);
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   draw_kernel<T><<<P.a.batch * P.plan.draw_chunks, kDrawNT, 0, s>>>(P);
   return cudaGetLastError();
@@ -1447,7 +1481,7 @@ cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s) {
   const double c = 1.4426950408889634 / static_cast<double>(L.a.temperature);
   P.c_hi = static_cast<float>(c);
   P.c_lo = static_cast<float>(c - static_cast<double>(P.c_hi));
-  P.pdl_primary = L.pdl_primary ? 1 : 0;
+  P.pdl_secondary = L.pdl_secondary ? 1 : 0;
   if (2 * L.a.num_rows - L.a.batch <= 0) return cudaSuccess;
   return L.a.dtype == SV_BF16 ? launch_t<uint16_t>(P, s) : launch_t<float>(P, s);
 }
