@@ -217,11 +217,24 @@ sv::AttnLaunchOpts opts_alone() {
   return sv::AttnLaunchOpts{false, std::min(half, sv::kSmemMax), 0, num_sms_current()};
 }
 
-// Attention ahead of the sampler in the fused step: launched the same way, and
-// lets the sampling launch start early (it runs on the SMs as they free up).
-sv::AttnLaunchOpts opts_step() {
+// Attention ahead of the sampler in the fused step; the sampling launch may
+// start at once.  With the cluster sampler (one CTA per SM, small shared
+// memory) each SM keeps room for one sampler CTA beside two attention CTAs, so
+// the latency-bound sampling runs under the bandwidth-bound attention: the
+// attention CTAs take at most (SM - sampler CTA) / 2 and more than a third of
+// the SM (so three of them never share one SM).
+sv::AttnLaunchOpts opts_step(const sv::SamplerPlan &sp) {
   sv::AttnLaunchOpts o = opts_alone();
   o.pdl_primary = true;
+  const SmemFacts f = smem_facts();
+  const int samp = sv::sampler_cluster_smem(sp);
+  if (f.per_sm <= 0 || samp <= 0) return o;
+  const int cap = (f.per_sm - samp - 3 * f.reserved) / 2;
+  const int floor3 = f.per_sm / 3 - f.reserved + 16;
+  if (cap > floor3) {
+    o.smem_cap = cap;
+    o.smem_min = floor3;
+  }
   return o;
 }
 
@@ -439,7 +452,7 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   SL.app.row_bytes = attn->num_kv_heads * attn->head_dim * esz;
   if (SL.app.row_bytes % 16)
     return fail(SV_ERR_UNSUPPORTED, "step: K/V row bytes not a multiple of 16");
-  if ((st = run_attention(attn, L, ws, opts_step(), s)) != SV_OK) return st;
+  if ((st = run_attention(attn, L, ws, opts_step(L.splan), s)) != SV_OK) return st;
   cudaError_t e = sv::launch_sampler(SL, s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
   return SV_OK;

@@ -185,14 +185,6 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
-// 2^x with the SFU's approximate exp2 (relative error ~2^-22, subnormal results
-// flushed to zero): far below the bf16 output rounding of the attention.
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Padded Q row address inside a Q slot.
 template <int D>
 __device__ __forceinline__ uint32_t prow(int row, int chunk) {
@@ -1039,9 +1031,8 @@ cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int
                         cudaStream_t s) {
   using C = AttnCfg<D, RS, NB>;
   AttnLaunchOpts opt = o;
-  // room beside another kernel's CTA only pays with at least 3 stages in flight
-  if (opt.smem_min > 0 && (stages_for<D, RS, NB>(P, opt.smem_cap) < 3 ||
-                           smem_map_for<D, RS, NB>(P, 3).total > opt.smem_cap)) {
+  // a budget that leaves room for another kernel's CTA must still hold 2 stages
+  if (opt.smem_min > 0 && smem_map_for<D, RS, NB>(P, 2).total > opt.smem_cap) {
     opt.smem_cap = kSmemMax;
     opt.smem_min = 0;
   }
@@ -1049,6 +1040,11 @@ cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int
   const int bytes = std::max(P.sm.total, opt.smem_min);
   auto kern = attn_bf16_kernel<D, RS, NB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  if (e != cudaSuccess) return e;
+  // all of the SM's unified L1 as shared memory (the loads bypass L1): an SM
+  // running this kernel then still has room for another kernel's CTA
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, bytes);

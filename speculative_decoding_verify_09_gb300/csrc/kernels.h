@@ -45,6 +45,7 @@ struct SamplerPlan {
   int stat_chunks;          // CTAs per row in the statistics phase (1: nucleus path)
   int draw_chunks;          // CTAs per sequence in the draw phase
   bool cluster;             // one CTA cluster per sequence (no nucleus, rows fit in smem)
+  int cluster_nvt;          // 16-byte vectors per thread and row in the cluster kernel (1, 2)
 };
 
 struct AppendView {   // what the fused step's append needs (all device pointers)

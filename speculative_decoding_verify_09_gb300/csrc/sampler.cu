@@ -934,42 +934,51 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
 
 // --------------------------------------------------------------------------
 // Cluster path (no nucleus): one thread-block cluster of kClusterN CTAs per
-// sequence.  Everything between the phases goes through distributed shared
-// memory and cluster barriers: no global atomics, no fences, no second launch.
-//   A  CTA k copies slice k of every row of the sequence into its shared
-//      memory (one cp.async round trip) and computes each row's slice max and
-//      slice sum of exp((l - m)/T); rows are handled 8 at a time so their
-//      reductions overlap.
-//   B  CTA 0 merges every row from the C slices (one DSMEM load per thread),
-//      evaluates the probability of each draft token and runs the accept
-//      tests; n is published in CTA 0's shared memory.
-//   C  every CTA: exact fixed-point sums of its slice of row n, one run of
-//      vpt vectors per thread, for the residual and for q_hat (fallback),
-//      plus its slice of the append.
-//   D  CTA 0 scans the C * 256 run sums in vocabulary order (CTA-major) and
-//      walks the one run holding the crossing in the owner CTA's slice.
+// sequence; CTA k owns vocabulary slice k of every row of the sequence.  The
+// phases meet at three cluster barriers and exchange data through distributed
+// shared memory: no global atomics, no fences, no second launch.
+//   A  CTA k loads slice k of every row into registers (rows in groups of
+//      8, all loads of a group in flight together); per row the warp max,
+//      then each thread's 2^((l - max) log2(e)/T) summed across the warp,
+//      merged across the CTA as (max, sum) pairs.
+//   B  every CTA merges each row's 16 slice statistics, evaluates the draft
+//      tokens' probabilities and runs the accept tests, so all CTAs hold n
+//      without another barrier; CTA 0 writes the outputs.
+//   C  append slice k of the accepted block rows; exact fixed-point sums of
+//      row n (the residual, and q_hat for the empty-residual fallback) per
+//      thread run, re-read from L2, scanned inside the CTA.
+// Shared memory holds only the statistics (a few KB), so a cluster's CTAs fit
+// beside the attention's CTAs on any SM in the fused step.
+//   D  every CTA reads the 16 slice totals and locates the target in
+//      vocabulary order; inside the owner CTA the thread whose run holds it
+//      walks that run.
+// Weights use the SFU's approximate exp2 (relative error ~2^-22) and fp32
+// (max, sum) merges: relative error of a probability stays below ~2e-6, far
+// inside the 1e-5 near-tie windows of the decisions.
 // --------------------------------------------------------------------------
-constexpr int kClusterN = 16;
+constexpr int kClusterN = 8;
 constexpr int kClNT = 256;
 constexpr int kClNW = kClNT / 32;
 constexpr int kMaxRows = 2 * kMaxQRows - 1;          // 2K+1 rows per sequence
-constexpr int kRowGroup = 8;                         // rows reduced together
+constexpr int kRowGroup = 4;                         // rows reduced together
 constexpr int kClVPT = 2;                            // vectors per thread per row slice
-constexpr int kClSmemRows = 96 * 1024;               // row slices cached in smem
 
 struct ClusterSmem {
-  float pm[kMaxRows];                                // slice max per row
-  float ps_hi[kMaxRows], ps_lo[kMaxRows];            // slice sum per row
+  float pm[kMaxRows], ps[kMaxRows];                  // slice (max, sum) per row
   uint32_t pbad[kMaxRows];
-  float st_m[kMaxRows], st_ihi[kMaxRows], st_ilo[kMaxRows];   // merged (CTA 0)
-  int n;                                             // decision (CTA 0)
-  float redf[kMaxRows][kClNW];
-  FF redff[kMaxRows][kClNW];
+  float st_m[kMaxRows], st_inv[kMaxRows];            // merged per row (every CTA)
+  uint32_t st_bad[kMaxRows];
+  float pdraft[kMaxRows];                            // probability of the row's draft token
+  uint32_t dbits[kMaxRows];                          // logit bits at the draft token
+  int dtok[kMaxRows];
+  float redm[kMaxRows][kClNW], reds[kMaxRows][kClNW];
   uint32_t redb[kMaxRows][kClNW];
-  unsigned long long run0[kClNT], run1[kClNT];       // residual / q_hat run sums
+  unsigned long long tot[2];                         // slice totals of the two run sums
   unsigned long long scan_red[kClNW];
-  unsigned long long bc64[2];
-  int bc[4];
+  unsigned long long dec_local;                      // target inside this slice (owner only)
+  uint32_t draw_u24[kMaxQRows];                      // draw uniform if n = index
+  int dec_use, dec_owner;
+  int n;
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -991,15 +1000,32 @@ __device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
   return reinterpret_cast<X *>(r);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampParams P) {
+// 2^(d * log2(e)/T) for d = l - max <= 0 (0 for d = -inf).
+struct Ex2c {
+  float c_hi, c_lo;
+  __device__ __forceinline__ float operator()(float d) const {
+    return d == -INFINITY ? 0.0f : fast_exp2(__fmaf_rn(d, c_hi, __fmul_rn(d, c_lo)));
+  }
+};
+
+// (m, s) <- merge of two (max, sum of weights relative to max) pairs.
+__device__ __forceinline__ void ms_merge(float &m, float &s, float m2, float s2, const Ex2c &e) {
+  const float mn = fmaxf(m, m2);
+  float r = 0.0f;
+  if (m > -INFINITY) r = __fmul_rn(s, e(m - mn));
+  if (m2 > -INFINITY) r = __fmaf_rn(s2, e(m2 - mn), r);
+  m = mn;
+  s = r;
+}
+
+template <typename T, int NVT>
+__global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampParams P) {
   const PdlTail tail{P.pdl_secondary};
-  extern __shared__ __align__(16) unsigned char csm_raw[];
-  ClusterSmem &sm = *reinterpret_cast<ClusterSmem *>(csm_raw);
-  uint4 *slice = reinterpret_cast<uint4 *>(csm_raw + (sizeof(ClusterSmem) + 127) / 128 * 128);
+  __shared__ ClusterSmem sm;
   constexpr int EPV = LT<T>::EPV;
   constexpr int C = kClusterN;
   const sv_sample_args &a = P.a;
+  const Ex2c ex2c{P.c_hi, P.c_lo};
   const uint32_t k = cluster_ctarank();
   const int i = blockIdx.x / C;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -1007,7 +1033,7 @@ __global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampPar
     if (k == 0 && tid == 0) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
     return;
   }
-  const int V = a.vocab, R = static_cast<int>(a.num_rows);
+  const int V = a.vocab;
   const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
   const int nrows = 2 * K + 1;
   const int L = a.kv_len[i];
@@ -1022,50 +1048,46 @@ __global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampPar
   const int v0 = min(NV, static_cast<int>(k) * per), v1 = min(NV, v0 + per);
   const int nv = v1 - v0;
 
-  // ---- CTA 0 prefetches the logit at the draft token of rows mq and mq + 16
-  const int mq = tid / C, mc = tid % C;             // row and slice merged by this thread
-  uint32_t dbits[2] = {0u, 0u};
-  int dtok[2] = {-1, -1};
-  if (k == 0 && mc == 0) {
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      const int q = mq + pass * (kClNT / C);
-      if (q < nrows && q != K) {
-        const int j = q < K ? q : q - K - 1;
-        dtok[pass] = a.draft_tokens[p0 + j];
-        if (dtok[pass] >= 0 && dtok[pass] < V) dbits[pass] = LT<T>::bits(row_ptr(q)[dtok[pass]]);
-      }
+  // ---- the logit at each row's draft token (every CTA needs the probabilities)
+  if (tid < nrows) {
+    int tok = -1;
+    uint32_t bits = 0;
+    if (tid != K) {
+      const int j = tid < K ? tid : tid - K - 1;
+      tok = a.draft_tokens[p0 + j];
+      if (tok >= 0 && tok < V) bits = LT<T>::bits(row_ptr(tid)[tok]);
     }
+    sm.dtok[tid] = tok;
+    sm.dbits[tid] = bits;
   }
-  // ---- phase A: slice k of every row into shared memory
-  for (int q = 0; q < nrows; ++q) {
+  // ---- phase A: slice k of every row into registers, (max, sum) per row
+  // Vector j of this thread in row q (elements past V and past the slice read
+  // as -inf).
+  auto row_vec = [&](int q, int j) -> uint4 {
+    const int v = tid + j * kClNT;
+    const uint32_t ni = LT<T>::NEG_INF_BITS * (EPV == 8 ? 0x10001u : 1u);
+    if (v >= nv) return make_uint4(ni, ni, ni, ni);
     const T *rp = row_ptr(q);
-    const bool al = (reinterpret_cast<uintptr_t>(rp) & 15) == 0;
-    for (int v = tid; v < nv; v += kClNT) {
-      if (al && (v0 + v + 1) * EPV <= V)
-        cp_async16(smem_u32(slice + q * nv + v), rp + (v0 + v) * EPV, 16);
-      else
-        slice[q * nv + v] = load_vec<T>(rp, V, v0 + v, al);
-    }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  // slice max per row, kRowGroup rows at a time (compile-time bounds, so the
-  // rows' chains interleave)
+    return load_vec<T>(rp, V, v0 + v, (reinterpret_cast<uintptr_t>(rp) & 15) == 0);
+  };
   for (int g0 = 0; g0 < nrows; g0 += kRowGroup) {
-    float mx[kRowGroup];
+    uint4 raw[kRowGroup][NVT];
+#pragma unroll
+    for (int u = 0; u < kRowGroup; ++u)
+#pragma unroll
+      for (int j = 0; j < NVT; ++j)
+        if (g0 + u < nrows) raw[u][j] = row_vec(g0 + u, j);
+    float mx[kRowGroup], sx[kRowGroup];
     uint32_t bad[kRowGroup];
 #pragma unroll
     for (int u = 0; u < kRowGroup; ++u) {
       mx[u] = -INFINITY;
       bad[u] = 0;
+      if (g0 + u < nrows) {
 #pragma unroll
-      for (int j = 0; j < kClVPT; ++j) {
-        const int v = tid + j * kClNT;
-        if (g0 + u < nrows && v < nv) {
+        for (int j = 0; j < NVT; ++j) {
           uint32_t b[EPV];
-          unpack<T>(slice[(g0 + u) * nv + v], b);
+          unpack<T>(raw[u][j], b);
 #pragma unroll
           for (int e = 0; e < EPV; ++e) {
             const float x = LT<T>::val(b[e]);
@@ -1082,172 +1104,134 @@ __global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampPar
         mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], o));
         bad[u] |= __shfl_xor_sync(0xffffffffu, bad[u], o);
       }
-    if (l == 0) {
-#pragma unroll
-      for (int u = 0; u < kRowGroup; ++u)
-        if (g0 + u < nrows) {
-          sm.redf[g0 + u][w] = mx[u];
-          sm.redb[g0 + u][w] = bad[u];
-        }
-    }
-  }
-  __syncthreads();
-  if (tid < nrows) {
-    float mx = sm.redf[tid][0];
-    uint32_t bd = sm.redb[tid][0];
-#pragma unroll
-    for (int x = 1; x < kClNW; ++x) {
-      mx = fmaxf(mx, sm.redf[tid][x]);
-      bd |= sm.redb[tid][x];
-    }
-    sm.pm[tid] = mx;
-    sm.pbad[tid] = bd;
-  }
-  __syncthreads();
-  // slice sum per row of exp((l - m_slice)/T): 8-element tree, float-float
-  for (int g0 = 0; g0 < nrows; g0 += kRowGroup) {
-    FF acc[kRowGroup];
 #pragma unroll
     for (int u = 0; u < kRowGroup; ++u) {
-      acc[u] = ff_make(0.0f);
-      const float mq_ = g0 + u < nrows ? sm.pm[g0 + u] : -INFINITY;
-      const WeightFn wf{mq_, P.c_hi, P.c_lo};
+      sx[u] = 0.0f;
+      if (g0 + u < nrows && mx[u] > -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < kClVPT; ++j) {
-        const int v = tid + j * kClNT;
-        if (mq_ > -INFINITY && v < nv) {
+        for (int j = 0; j < NVT; ++j) {
           uint32_t b[EPV];
-          unpack<T>(slice[(g0 + u) * nv + v], b);
-          float t8[EPV];
+          unpack<T>(raw[u][j], b);
+          float t[EPV];
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) t8[e] = wf(LT<T>::val(b[e]));
+          for (int e = 0; e < EPV; ++e) t[e] = ex2c(LT<T>::val(b[e]) - mx[u]);
 #pragma unroll
           for (int st = EPV / 2; st > 0; st >>= 1)
 #pragma unroll
-            for (int e = 0; e < st; ++e) t8[e] = __fadd_rn(t8[e], t8[e + st]);
-          acc[u] = ff_add(acc[u], ff_make(t8[0]));
+            for (int e = 0; e < st; ++e) t[e] = __fadd_rn(t[e], t[e + st]);
+          sx[u] = __fadd_rn(sx[u], t[0]);
         }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-      for (int u = 0; u < kRowGroup; ++u) {
-        FF t;
-        t.hi = __shfl_xor_sync(0xffffffffu, acc[u].hi, o);
-        t.lo = __shfl_xor_sync(0xffffffffu, acc[u].lo, o);
-        acc[u] = ff_add(acc[u], t);
-      }
+      for (int u = 0; u < kRowGroup; ++u) sx[u] = __fadd_rn(sx[u], __shfl_xor_sync(0xffffffffu, sx[u], o));
     if (l == 0) {
 #pragma unroll
       for (int u = 0; u < kRowGroup; ++u)
-        if (g0 + u < nrows) sm.redff[g0 + u][w] = acc[u];
+        if (g0 + u < nrows) {
+          sm.redm[g0 + u][w] = mx[u];
+          sm.reds[g0 + u][w] = sx[u];
+          sm.redb[g0 + u][w] = bad[u];
+        }
     }
   }
   __syncthreads();
   if (tid < nrows) {
-    FF t = sm.redff[tid][0];
+    float m = sm.redm[tid][0], s = sm.reds[tid][0];
+    uint32_t bd = sm.redb[tid][0];
 #pragma unroll
-    for (int x = 1; x < kClNW; ++x) t = ff_add(t, sm.redff[tid][x]);
-    sm.ps_hi[tid] = t.hi;
-    sm.ps_lo[tid] = t.lo;
+    for (int x = 1; x < kClNW; ++x) {
+      ms_merge(m, s, sm.redm[tid][x], sm.reds[tid][x], ex2c);
+      bd |= sm.redb[tid][x];
+    }
+    sm.pm[tid] = m;
+    sm.ps[tid] = s;
+    sm.pbad[tid] = bd;
   }
-  cluster_sync_all();                              // (1) slices of all rows done
+  cluster_sync_all();                              // (1) slice statistics of all rows
 
-  // ---- phase B (CTA 0): merge row mq from slice mc, 16 lanes per row
-  if (k == 0) {
-    static_assert(kClNT / C * 2 >= kMaxRows, "rows merged two per 16-lane group pass");
+  // ---- phase B (every CTA): merge row mq from slice mc, C lanes per row
+  {
+    const int mq = tid / C, mc = tid % C;
+    static_assert(kClNT / C * 2 >= kMaxRows, "rows merged in two passes of C-lane groups");
     for (int pass = 0; pass < 2; ++pass) {
       const int q = mq + pass * (kClNT / C);
       const bool live = q < nrows;
-      float m = -INFINITY, shi = 0.0f, slo = 0.0f;
+      float m = -INFINITY, s = 0.0f;
       uint32_t bd = 0;
       if (live) {
         m = *dsmem(&sm.pm[q], mc);
-        shi = *dsmem(&sm.ps_hi[q], mc);
-        slo = *dsmem(&sm.ps_lo[q], mc);
+        s = *dsmem(&sm.ps[q], mc);
         bd = *dsmem(&sm.pbad[q], mc);
       }
-      float M = m;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      for (int o = C / 2; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
         bd |= __shfl_xor_sync(0xffffffffu, bd, o);
-      }
-      FF S = ff_make(0.0f);
-      if (m > -INFINITY) {
-        const float f = WeightFn{M, P.c_hi, P.c_lo}(m);     // exp((m_c - M)/T)
-        S = ff_add(FF{__fmul_rn(shi, f), 0.0f}, FF{__fmul_rn(slo, f), 0.0f});
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        FF t;
-        t.hi = __shfl_xor_sync(0xffffffffu, S.hi, o);
-        t.lo = __shfl_xor_sync(0xffffffffu, S.lo, o);
-        S = ff_add(S, t);
+        ms_merge(m, s, m2, s2, ex2c);
       }
       if (live && mc == 0) {
-        const bool ok = !bd && M > -INFINITY && S.hi > 0.0f;
-        const float rh = ok ? __frcp_rn(S.hi) : 0.0f;    // 1/S as float-float
-        const float res = ok ? __fmaf_rn(-S.hi, rh, 1.0f) - S.lo * rh : 0.0f;
-        sm.st_m[q] = M;
-        sm.st_ihi[q] = rh;
-        sm.st_ilo[q] = ok ? rh * res : 0.0f;
-        sm.pbad[q] = ok ? 0u : 1u;                 // reused: 1 = row unusable
+        const bool ok = !bd && m > -INFINITY && s > 0.0f;
+        const float inv = ok ? __frcp_rn(s) : 0.0f;
+        sm.st_m[q] = m;
+        sm.st_inv[q] = inv;
+        sm.st_bad[q] = ok ? 0u : 1u;
+        float pd = 0.0f;
+        const int tok = sm.dtok[q];
+        if (q != K && ok && tok >= 0 && tok < V)
+          pd = __fmul_rn(ex2c(LT<T>::val(sm.dbits[q]) - m), inv);
+        sm.pdraft[q] = pd;
       }
     }
-    __syncthreads();
-    // probability of the draft token in rows mq and mq + 16 (prefetched logits)
-    if (mc == 0) {
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        const int q = mq + pass * (kClNT / C);
-        if (q < nrows && q != K) {
-          float pd = 0.0f;
-          if (sm.pbad[q] == 0 && dtok[pass] >= 0 && dtok[pass] < V) {
-            const float wv = WeightFn{sm.st_m[q], P.c_hi, P.c_lo}(LT<T>::val(dbits[pass]));
-            pd = __fmaf_rn(wv, sm.st_ihi[q], __fmul_rn(wv, sm.st_ilo[q]));
-          }
-          sm.ps_hi[q] = pd;                        // reused: draft probability
-        }
+  }
+  __syncthreads();
+  // accept tests, lane j for draft j+1 (same decisions in every CTA)
+  if (w == 0) {
+    int okall = 1;
+    for (int q = l; q < nrows; q += 32) okall &= sm.st_bad[q] == 0;
+    okall = __all_sync(0xffffffffu, okall) && L >= 0;
+    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+    bool rej = false, bad = false;
+    int d = 0;
+    if (okall && l < K) {
+      d = sm.dtok[l];
+      if (d < 0 || d >= V) {
+        rej = bad = true;
+      } else {
+        const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
+                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                    static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+        const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;     // exact
+        rej = !(__fmul_rn(u, sm.pdraft[K + 1 + l]) < sm.pdraft[l]);
       }
     }
-    __syncthreads();
-    // accept tests, lane j for draft j+1
-    if (w == 0) {
-      int okall = 1;
-      for (int q = l; q < nrows; q += 32) okall &= sm.pbad[q] == 0;
-      okall = __all_sync(0xffffffffu, okall) && L >= 0;
-      const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
-      bool rej = false, bad = false;
-      int d = 0;
-      if (okall && l < K) {
-        d = a.draft_tokens[p0 + l];
-        if (d < 0 || d >= V) {
-          rej = bad = true;
-        } else {
-          const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
-                                         static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                         static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
-                                      static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
-          const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;     // exact
-          rej = !(__fmul_rn(u, sm.ps_hi[K + 1 + l]) < sm.ps_hi[l]);
-        }
-      }
-      const unsigned rm = __ballot_sync(0xffffffffu, rej);
-      const unsigned bm = __ballot_sync(0xffffffffu, bad);
-      const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
+    const unsigned rm = __ballot_sync(0xffffffffu, rej);
+    const unsigned bm = __ballot_sync(0xffffffffu, bad);
+    const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
+    if (l == 0) sm.n = n;
+    if (k == 0) {
       if (l <= K) a.out_tokens[r0 + l] = (n >= 0 && l < n) ? d : -1;
       if (l == 0) {
         a.num_accepted[i] = n;
-        sm.n = n;
         if (!okall) set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
         else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
       }
     }
   }
-  cluster_sync_all();                              // (2) n and merged rows in CTA 0
-  const int n = *dsmem(&sm.n, 0);
+  if (w == 1 && l <= K) {            // draw uniforms for every possible n (position L + n + 1)
+    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
+    const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
+                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
+                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+    sm.draw_u24[l] = u24(wv.y);
+  }
+  __syncthreads();
+  const int n = sm.n;
 
   // ---- phase C: append slice k of block rows 0..n, run sums of row n
   if (P.do_append) {
@@ -1281,105 +1265,113 @@ __global__ void __launch_bounds__(kClNT, 2) sampler_cluster_kernel(const SampPar
     }
   }
   if (n < 0) {
-    cluster_sync_all();
+    cluster_sync_all();                            // no CTA leaves while others read it
     return;
   }
   const int mode = n < K ? 0 : 1;
   const int qt = n, qd = K + 1 + n;                 // target row n, draft row n
-  RowProb pq, pp;
-  pq.wf = WeightFn{*dsmem(&sm.st_m[qt], 0), P.c_hi, P.c_lo};
-  pq.tau = 0;
-  pq.inv_hi = *dsmem(&sm.st_ihi[qt], 0);
-  pq.inv_lo = *dsmem(&sm.st_ilo[qt], 0);
-  pp = pq;
-  if (mode == 0) {
-    pp.wf = WeightFn{*dsmem(&sm.st_m[qd], 0), P.c_hi, P.c_lo};
-    pp.inv_hi = *dsmem(&sm.st_ihi[qd], 0);
-    pp.inv_lo = *dsmem(&sm.st_ilo[qd], 0);
-  }
+  const float mq_ = sm.st_m[qt], iq = sm.st_inv[qt];
+  const float mp_ = mode == 0 ? sm.st_m[qd] : 0.0f, ip = mode == 0 ? sm.st_inv[qd] : 0.0f;
+  auto qhat = [&](uint32_t b) { return __fmul_rn(ex2c(LT<T>::val(b) - mq_), iq); };
+  auto phat = [&](uint32_t b) { return __fmul_rn(ex2c(LT<T>::val(b) - mp_), ip); };
   const int vpt = (per + kClNT - 1) / kClNT;        // vectors per run
-  {
-    unsigned long long s0 = 0, s1 = 0;
-    const int ra = tid * vpt, rb_ = min(nv, ra + vpt);
-    for (int v = ra; v < rb_; ++v) {
-      uint32_t bq[EPV], bd[EPV];
-      unpack<T>(slice[qt * nv + v], bq);
-      if (mode == 0) unpack<T>(slice[qd * nv + v], bd);
+  const int ra = min(nv, tid * vpt), rb = min(nv, ra + vpt);
+  const T *rq = row_ptr(qt), *rd = row_ptr(qd);
+  const bool alq = (reinterpret_cast<uintptr_t>(rq) & 15) == 0;
+  const bool ald = (reinterpret_cast<uintptr_t>(rd) & 15) == 0;
+  unsigned long long s0 = 0, s1 = 0;
+  for (int v = ra; v < rb; ++v) {
+    uint32_t bq[EPV], bd[EPV];
+    unpack<T>(load_vec<T>(rq, V, v0 + v, alq), bq);
+    if (mode == 0) unpack<T>(load_vec<T>(rd, V, v0 + v, ald), bd);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const float qh = row_prob<T>(pq, bq[e]);
-        s1 += fix52(qh);
-        if (mode == 0) s0 += fix52(fmaxf(__fsub_rn(qh, row_prob<T>(pp, bd[e])), 0.0f));
+    for (int e = 0; e < EPV; ++e) {
+      const float qh = qhat(bq[e]);
+      s1 += fix52(qh);
+      if (mode == 0) s0 += fix52(fmaxf(__fsub_rn(qh, phat(bd[e])), 0.0f));
+    }
+  }
+  if (mode != 0) s0 = s1;
+  unsigned long long z0, z1;
+  const unsigned long long ex0 = block_exclusive_scan_u64<kClNT>(s0, sm.scan_red, &z0);
+  __syncthreads();
+  const unsigned long long ex1 = block_exclusive_scan_u64<kClNT>(s1, sm.scan_red, &z1);
+  if (tid == 0) {
+    sm.tot[0] = z0;
+    sm.tot[1] = z1;
+  }
+  cluster_sync_all();                              // (2) slice totals visible
+
+  // ---- phase D: locate the target among the slices; the owner walks its run
+  if (w == 0) {
+    unsigned long long t0 = 0, t1 = 0;
+    if (l < C) {
+      t0 = *dsmem(&sm.tot[0], l);
+      t1 = *dsmem(&sm.tot[1], l);
+    }
+    unsigned long long c0 = t0, c1 = t1;           // inclusive prefix over slices
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y0 = __shfl_up_sync(0xffffffffu, c0, o);
+      const unsigned long long y1 = __shfl_up_sync(0xffffffffu, c1, o);
+      if (l >= o) {
+        c0 += y0;
+        c1 += y1;
       }
     }
-    sm.run0[tid] = mode == 0 ? s0 : s1;
-    sm.run1[tid] = s1;
-  }
-  cluster_sync_all();                              // (3) all run sums visible
-
-  // ---- phase D (CTA 0): scan the run sums, walk the owner run
-  if (k == 0) {
-    const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
-    const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
-                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
-                                static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
-    const unsigned long long ku = u24(wv.y);
-    unsigned long long rs[C];                        // global runs g = tid*C + u
-    for (int round = 0; round < 2; ++round) {
-      const int use = round == 0 ? mode : 1;
-#pragma unroll
-      for (int u = 0; u < C; ++u) {
-        const int g = tid * C + u;
-        rs[u] = use == 0 ? *dsmem(&sm.run0[g % kClNT], g / kClNT)
-                         : *dsmem(&sm.run1[g % kClNT], g / kClNT);
+    const unsigned long long Z0 = __shfl_sync(0xffffffffu, c0, 31);
+    const unsigned long long Z1 = __shfl_sync(0xffffffffu, c1, 31);
+    const unsigned long long pre0 = __shfl_sync(0xffffffffu, c0 - t0, static_cast<int>(k));
+    const unsigned long long pre1 = __shfl_sync(0xffffffffu, c1 - t1, static_cast<int>(k));
+    if (l == 0) {
+      int use = mode;
+      if (use == 0 && Z0 == 0) {                   // rejected, empty residual: draw from q_hat
+        use = 1;
+        if (k == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
       }
-      unsigned long long mine = 0;
-#pragma unroll
-      for (int u = 0; u < C; ++u) mine += rs[u];
-      unsigned long long Z;
-      const unsigned long long ex = block_exclusive_scan_u64<kClNT>(mine, sm.scan_red, &Z);
+      const unsigned long long Z = use == 0 ? Z0 : Z1;
+      const unsigned long long pre = use == 0 ? pre0 : pre1;
+      const unsigned long long mine = use == 0 ? sm.tot[0] : sm.tot[1];
+      int owner = 0;
+      unsigned long long local = 0;
       if (Z == 0) {
-        if (use == 0) {                            // rejected, empty residual: draw from q_hat
-          if (tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
-          continue;
-        }
-        if (tid == 0) a.out_tokens[r0 + n] = -1;
-        break;
+        if (k == 0) a.out_tokens[r0 + n] = -1;     // empty q_hat: cannot happen for a valid row
+      } else {
+        const unsigned long long ku = sm.draw_u24[n];
+        const unsigned long long tg = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);   // floor(k*Z/2^24)
+        owner = pre <= tg && tg < pre + mine;
+        local = tg - pre;
       }
-      const unsigned long long tg = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);
-      if (ex <= tg && tg < ex + mine) {
-        unsigned long long c = ex;
-        int g = tid * C;
+      sm.dec_use = use;
+      sm.dec_owner = owner;
+      sm.dec_local = local;
+    }
+  }
+  __syncthreads();
+  if (sm.dec_owner) {
+    const int use = sm.dec_use;
+    const unsigned long long local = sm.dec_local;
+    const unsigned long long ex = use == 0 ? ex0 : ex1, mine = use == 0 ? s0 : s1;
+    if (ex <= local && local < ex + mine) {
+      unsigned long long c = ex;
+      int x = -1;
+      for (int v = ra; v < rb && x < 0; ++v) {
+        uint32_t bq[EPV], bd[EPV];
+        unpack<T>(load_vec<T>(rq, V, v0 + v, alq), bq);
+        if (use == 0) unpack<T>(load_vec<T>(rd, V, v0 + v, ald), bd);
 #pragma unroll
-        for (int u = 0; u < C; ++u) {
-          if (c + rs[u] > tg) { g = tid * C + u; break; }
-          c += rs[u];
-        }
-        const int cta = g / kClNT, run = g % kClNT;
-        const int cnv = min(NV, cta * per + per) - min(NV, cta * per);    // slice length of cta
-        const int va = run * vpt, vb = min(cnv, va + vpt);
-        const uint4 *rslice = dsmem(slice, cta);
-        int x = -1;
-        for (int v = va; v < vb && x < 0; ++v) {
-          uint32_t bq[EPV], bd[EPV];
-          unpack<T>(rslice[qt * cnv + v], bq);
-          if (use == 0) unpack<T>(rslice[qd * cnv + v], bd);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            if (x < 0) {
-              const float qh = row_prob<T>(pq, bq[e]);
-              c += use == 0 ? fix52(fmaxf(__fsub_rn(qh, row_prob<T>(pp, bd[e])), 0.0f)) : fix52(qh);
-              if (c > tg) x = (min(NV, cta * per) + v) * EPV + e;
-            }
+        for (int e = 0; e < EPV; ++e) {
+          if (x < 0) {
+            const float qh = qhat(bq[e]);
+            c += use == 0 ? fix52(fmaxf(__fsub_rn(qh, phat(bd[e])), 0.0f)) : fix52(qh);
+            if (c > local) x = (v0 + v) * EPV + e;
           }
         }
-        a.out_tokens[r0 + n] = x;
       }
-      break;
+      a.out_tokens[r0 + n] = x;
     }
   }
-  cluster_sync_all();                              // (4) CTA 0 done reading remote slices
+  cluster_sync_all();                              // (3) no CTA leaves while its totals are read
 }
 
 }  // namespace
@@ -1392,8 +1384,8 @@ SamplerPlan plan_sampler(const sv_sample_args &a) {
   p.draw_chunks = std::max(1, std::min(64, (nv + 511) / 512));
   // one cluster per sequence when there is no nucleus and the rows' slices fit
   const int per = (nv + kClusterN - 1) / kClusterN;
-  p.cluster = a.top_p >= 1.0f && (2 * a.max_q_rows - 1) * per * 16 <= kClSmemRows &&
-              per <= kClVPT * kClNT;
+  p.cluster_nvt = per > kClNT ? 2 : 1;
+  p.cluster = a.top_p >= 1.0f && per <= kClVPT * kClNT;
   return p;
 }
 
@@ -1402,14 +1394,15 @@ int sampler_max_vocab(int dtype) {
 }
 
 int sampler_cluster_smem(const SamplerPlan &p) {
-  return p.cluster ? static_cast<int>((sizeof(ClusterSmem) + 127) / 128 * 128) + kClSmemRows : 0;
+  return p.cluster ? static_cast<int>(sizeof(ClusterSmem)) : 0;
 }
 
 template <typename T>
 static cudaError_t launch_cluster(const SampParams &P, cudaStream_t s) {
-  auto kern = sampler_cluster_kernel<T>;
-  const int smem = sampler_cluster_smem(P.plan);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = P.plan.cluster_nvt == 2 ? sampler_cluster_kernel<T, 2> : sampler_cluster_kernel<T, 1>;
+  const int smem = 0;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
