@@ -58,7 +58,17 @@ struct SmemMap {
   int ns;                  // ring stages
   int units_cap, groups_cap;
   int q;                   // two Q slots (header + packed rows)
-  int merge_o, merge_ml, fin, bars, sched, misc, total;
+  int merge_o, merge_ml, fin, jobs, bars, sched, misc, total;
+};
+
+// A stream-K merge handed from the consumer warps to the merger warp: the
+// piece's partial is in global memory; the merger counts the pieces of the
+// segment and, for the last one, combines them into the output.
+constexpr int kJobs = 4;
+struct MergeJob {
+  int seg;              // segment (-1: no more jobs)
+  int npieces, Mi, r0, hk;
+  int64_t c_first;      // first piece's CTA index
 };
 
 struct AttnParams {
@@ -92,7 +102,7 @@ struct AttnParams {
 template <int D, int RS, int NB>
 struct AttnCfg {
   static constexpr int kCW = kKW * RS;                          // consumer warps
-  static constexpr int kThreads = (kCW + 1) * 32;
+  static constexpr int kThreads = (kCW + 2) * 32;               // + producer + merger
   static constexpr int kRowsW = 8 * NB;                         // rows per warp
   static constexpr int kRows = RS * kRowsW;                     // rows per CTA
   static constexpr int kRowB = D * 2 + 16;                      // padded Q row
@@ -101,7 +111,7 @@ struct AttnCfg {
   static constexpr int kQHead = 64;                             // segment header
   static constexpr int kQSlotB = kQHead + kRows * kRowB;
   static constexpr int kOStride = D + 4;                        // padded merge rows (floats)
-  static constexpr int kMergeO = kRows * kOStride * 4;
+  static constexpr int kMergeO = 2 * kRows * kOStride * 4;      // two key-slice sums
   static constexpr int kMergeML = kCW * kRowsW * 8;
   static constexpr int kFinal = kRows * 8;
   static_assert(kMaxBatch * 8 <= 2 * kStageB, "unit bases staged in the ring");
@@ -121,8 +131,10 @@ struct AttnCfg {
     off += kMergeML;
     m.fin = off;
     off += kFinal;
+    m.jobs = up(off, 16);
+    off = m.jobs + kJobs * static_cast<int>(sizeof(MergeJob)) + kRows * 8;   // + merger's row stats
     m.bars = up(off, 8);
-    off = m.bars + (2 * ns + 5) * 8;
+    off = m.bars + (2 * ns + 5 + 2 * kJobs) * 8;
     m.sched = up(off, 16);
     off = m.sched + 4 * (m.units_cap + 4 * m.groups_cap);
     m.misc = up(off, 16);
@@ -368,7 +380,7 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams &P, const Sched &S,
 // rows on M, and keeps O in 32*NB registers per thread.
 // ---------------------------------------------------------------------------
 struct Ring {            // shared-memory addresses of the pipeline
-  uint32_t base, q, full, empty, qfull, qempty, ebar;
+  uint32_t base, q, full, empty, qfull, qempty, ebar, jfull, jempty;
 };
 
 // Producer warp: Q slots and K/V stages for the CTA's tiles [0, ntiles).
@@ -467,6 +479,82 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
   }
 }
 
+// Merger warp: for every multi-piece segment the consumers finished, count
+// the piece (release of the partial at gpu scope, then an atomic increment
+// that wraps to zero); the last piece to arrive combines all pieces' partials
+// into the output.  Off the consumers' path, so their next segment proceeds.
+template <int D, int RS, int NB>
+__device__ __forceinline__ void attn_merge_jobs(const AttnParams &P, const Ring &rg,
+                                                MergeJob *jobs, float2 *mfin,
+                                                volatile int *abort_flag) {
+  using C = AttnCfg<D, RS, NB>;
+  constexpr int rows_m = C::kRows;
+  const int lane = threadIdx.x & 31, g = P.g;
+  for (int nj = 0;; ++nj) {
+    const int js = nj % kJobs;
+    if (!mbar_wait(rg.jfull + 8 * js, (nj / kJobs) & 1)) {
+      if (lane == 0) {
+        set_status(P.dev_status, SV_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return;
+    }
+    const MergeJob jb = jobs[js];
+    if (jb.seg < 0) return;
+    int last = 0;
+    if (lane == 0) {
+      __threadfence();              // the consumers' partial writes, visible at gpu scope
+      const unsigned old = atomicInc(&P.counters[jb.seg], static_cast<unsigned>(jb.npieces - 1));
+      last = old == static_cast<unsigned>(jb.npieces - 1);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      // per row, the pieces' (max, sum) folded into one
+      for (int m = lane; m < jb.Mi; m += 32) {
+        float mm = -INFINITY, den = 0.0f;
+#pragma unroll 4
+        for (int c = 0; c < jb.npieces; ++c) {
+          const float2 v = __ldcg(&P.part_ml[(jb.c_first + c + jb.seg) * rows_m + m]);
+          const float mn = fmaxf(mm, v.x);
+          const float mu = mn == -INFINITY ? 0.0f : mn;
+          den = den * fast_exp2(mm - mu) + v.y * fast_exp2(v.x - mu);
+          mm = mn;
+        }
+        mfin[m] = make_float2(mm, den);
+      }
+      __syncwarp();
+      // the weighted sum of the pieces' O rows, four columns at a time
+#pragma unroll 2
+      for (int e = lane; e < jb.Mi * (D / 4); e += 32) {
+        const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
+        const float mm = mfin[m].x, den = mfin[m].y;
+        const float mu = mm == -INFINITY ? 0.0f : mm;
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+        for (int c = 0; c < jb.npieces; ++c) {
+          const int64_t slot2 = jb.c_first + c + jb.seg;
+          const float f = fast_exp2(__ldcg(&P.part_ml[slot2 * rows_m + m].x) - mu);
+          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d));
+          acc.x = fmaf(f, ov.x, acc.x);
+          acc.y = fmaf(f, ov.y, acc.y);
+          acc.z = fmaf(f, ov.z, acc.z);
+          acc.w = fmaf(f, ov.w, acc.w);
+        }
+        const int j = m / g, hg = m - j * g;
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(jb.r0 + j) * P.Hq + jb.hk * g + hg) * D + d) = pk;
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rg.jempty + 8 * js);
+  }
+}
+
 template <int D, int RS, int NB>
 __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned char *smem) {
   using C = AttnCfg<D, RS, NB>;
@@ -485,6 +573,10 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   rg.qfull = rg.empty + 8 * NS;
   rg.qempty = rg.qfull + 16;
   rg.ebar = rg.qempty + 16;
+  rg.jfull = rg.ebar + 8;
+  rg.jempty = rg.jfull + 8 * kJobs;
+  MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + Mp.jobs);
+  float2 *mfin = reinterpret_cast<float2 *>(smem + Mp.jobs + kJobs * sizeof(MergeJob));
   int64_t *ubase = reinterpret_cast<int64_t *>(smem);     // staged in the ring before it starts
   int *misc = reinterpret_cast<int *>(smem + Mp.misc);
   int64_t *misc64 = reinterpret_cast<int64_t *>(smem + Mp.misc + 16);
@@ -531,6 +623,10 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       mbar_init(rg.qempty + 8 * s2, C::kCW);
     }
     mbar_init(rg.ebar, NC);
+    for (int s2 = 0; s2 < kJobs; ++s2) {
+      mbar_init(rg.jfull + 8 * s2, NC);         // every consumer thread, after its partial writes
+      mbar_init(rg.jempty + 8 * s2, 1);         // the merger, done with the job
+    }
     misc[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -540,6 +636,10 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
 
   if (warp == C::kCW) {
     attn_produce<D, RS, NB>(P, S, cur, ntiles, rg, smem, abort_flag);
+    return;
+  }
+  if (warp == C::kCW + 1) {
+    attn_merge_jobs<D, RS, NB>(P, rg, jobs, mfin, abort_flag);
     return;
   }
 
@@ -584,6 +684,16 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     active = row_w0 < cs.M;
     reset_state();
     return true;
+  };
+  int njob = 0;
+  // Hand a merge job to the merger warp (every consumer thread calls this after
+  // its partial writes; seg = -1 ends the merger).
+  auto post_job = [&](const MergeJob &jb) {
+    const int js = njob % kJobs;
+    if (!mbar_wait(rg.jempty + 8 * js, ((njob / kJobs) & 1) ^ 1)) ok = false;
+    if (tid == 0) jobs[js] = jb;
+    mbar_arrive(rg.jfull + 8 * js);
+    ++njob;
   };
   auto end_segment = [&]() {     // Q slot no longer read by this warp
     __syncwarp();
@@ -710,9 +820,12 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       fin[tid] = make_float2(mm, ll);
     }
     csync();
-    // O^T of the 4 key slices into the row-major buffer, in a fixed order
-    for (int step = kKW - 1; step >= 0; --step) {
-      if (ks == step) {
+    // O^T of the 4 key slices in two steps: slices 1 and 3 store into buffers
+    // A and B, then slices 0 and 2 add theirs (fixed order: deterministic);
+    // the row-major result is A + B.
+    static_assert(kKW == 4, "two-step merge of four key slices");
+    for (int step = 0; step < 2; ++step) {
+      if ((ks & 1) == (step == 0 ? 1 : 0)) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
@@ -720,12 +833,12 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
             const int m = row_w0 + nb * 8 + 2 * q + e;
             const float mm = fin[m].x;
             const float sc = fast_exp2(m_run[nb][e] - (mm == -INFINITY ? 0.0f : mm));
-            float *dst = merge_o + m * OS;
+            float *dst = merge_o + (ks >> 1) * C::kRows * OS + m * OS;
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm) {
               const int d0 = dm * 16 + r;
               const float a0 = o[dm][nb][e] * sc, a1 = o[dm][nb][2 + e] * sc;
-              if (step == kKW - 1) {
+              if (step == 0) {
                 dst[d0] = a0;
                 dst[d0 + 8] = a1;
               } else {
@@ -737,61 +850,37 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       }
       csync();
     }
+    const float *mob = merge_o + C::kRows * OS;   // buffer B; merge_o is A
     const int seg = cs.seg;
     const int64_t c_first = cta_of_tile(seg_first_tile, W, G);
     const int64_t c_last = cta_of_tile(seg_first_tile + cs.nt - 1, W, G);
     const int npieces = static_cast<int>(c_last - c_first + 1);
     constexpr int rows_m = C::kRows;
     if (npieces == 1 && P.mode == 0) {   // the whole segment is here: normalize, store
-      for (int e = tid; e < Mi * (D / 2); e += NC) {
-        const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
+      for (int e = tid; e < Mi * (D / 4); e += NC) {
+        const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
         const float lsum = fin[m].y;
         const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+        const float4 a = *reinterpret_cast<const float4 *>(merge_o + m * OS + d);
+        const float4 b = *reinterpret_cast<const float4 *>(mob + m * OS + d);
         const int j = m / g, hg = m - j * g;
-        *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) =
-            pack_bf16x2(merge_o[m * OS + d] * inv, merge_o[m * OS + d + 1] * inv);
+        uint2 pk;
+        pk.x = pack_bf16x2((a.x + b.x) * inv, (a.y + b.y) * inv);
+        pk.y = pack_bf16x2((a.z + b.z) * inv, (a.w + b.w) * inv);
+        *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) = pk;
       }
     } else {                          // partial: slot = CTA index + segment index
       const int64_t slot = static_cast<int64_t>(blockIdx.x) + seg;
-      for (int e = tid; e < Mi * (D / 2); e += NC) {
-        const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
-        *reinterpret_cast<float2 *>(P.part_o + (slot * rows_m + m) * D + d) =
-            make_float2(merge_o[m * OS + d], merge_o[m * OS + d + 1]);
+      for (int e = tid; e < Mi * (D / 4); e += NC) {
+        const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
+        const float4 a = *reinterpret_cast<const float4 *>(merge_o + m * OS + d);
+        const float4 b = *reinterpret_cast<const float4 *>(mob + m * OS + d);
+        __stcg(reinterpret_cast<float4 *>(P.part_o + (slot * rows_m + m) * D + d),
+               make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
       }
-      if (tid < Mi) P.part_ml[slot * rows_m + tid] = fin[tid];
-    }
-    if (npieces > 1 && P.mode == 0) {    // plain mode: the last piece merges
-      __threadfence();
-      csync();
-      if (tid == 0) {
-        const unsigned old = atomicInc(&P.counters[seg], static_cast<unsigned>(npieces - 1));
-        misc[0] = old == static_cast<unsigned>(npieces - 1) ? 1 : 0;
-      }
-      csync();
-      if (misc[0]) {                   // last piece to arrive merges the segment
-        __threadfence();
-        for (int e = tid; e < Mi * (D / 2); e += NC) {
-          const int m = e / (D / 2), d = (e - m * (D / 2)) * 2;
-          float mm = -INFINITY;
-          for (int c = 0; c < npieces; ++c)
-            mm = fmaxf(mm, __ldcg(&P.part_ml[(c_first + c + seg) * rows_m + m].x));
-          const float mu = mm == -INFINITY ? 0.0f : mm;
-          float n0 = 0.0f, n1 = 0.0f, den = 0.0f;
-          for (int c = 0; c < npieces; ++c) {
-            const int64_t slot2 = c_first + c + seg;
-            const float2 ml = __ldcg(&P.part_ml[slot2 * rows_m + m]);
-            const float f = fast_exp2(ml.x - mu);
-            const float2 ov = __ldcg(reinterpret_cast<const float2 *>(P.part_o + (slot2 * rows_m + m) * D + d));
-            n0 += f * ov.x;
-            n1 += f * ov.y;
-            den += f * ml.y;
-          }
-          const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-          const int j = m / g, hg = m - j * g;
-          *reinterpret_cast<uint32_t *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) =
-              pack_bf16x2(n0 * inv, n1 * inv);
-        }
-      }
+      if (tid < Mi) __stcg(&P.part_ml[slot * rows_m + tid], fin[tid]);
+      if (npieces > 1 && P.mode == 0)    // plain mode: the merger counts pieces, the last merges
+        post_job(MergeJob{seg, npieces, Mi, cs.r0, cs.hk, c_first});
     }
     csync();                           // merge buffers reusable
     if (last || !ok) break;
@@ -803,6 +892,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     set_status(P.dev_status, SV_DEV_TIMEOUT);
     *abort_flag = 1;
   }
+  post_job(MergeJob{-1, 0, 0, 0, 0, 0});
 }
 
 template <int D, int RS, int NB>
