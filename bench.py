@@ -185,6 +185,7 @@ def main():
 
     import torch
     import speculative_decoding_verify_09_gb300 as pkg
+    from speculative_decoding_verify_09_gb300 import shard
     pkg.build()
     api = pkg.load()
     torch.cuda.set_device(local_rank)
@@ -193,9 +194,13 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
+    # weak scaling: rank r owns global sequences [r*B, (r+1)*B) of a batch of
+    # world*B sequences (the same shapes on every rank, uniforms keyed by the
+    # global sequence id); no exchange on the data path
     w = W.workload(WORKLOAD)
     inp = W.make_inputs(w)
-    inp["seq_ids"] = inp["seq_ids"] + rank * w.B          # global sequence ids
+    lo, _ = shard.rank_range(world * w.B, rank, world)
+    inp["seq_ids"] = inp["seq_ids"] + lo
     from speculative_decoding_verify_09_gb300.buffers import StepBuffers
     sets = [StepBuffers(inp, api) for _ in range(args.sets)]
     nbytes = W.step_bytes(inp)
@@ -241,11 +246,7 @@ def main():
                     fn(d)
         ev1.record(stream)
         torch.cuda.synchronize()
-        ms = ev0.elapsed_time(ev1)
-        if dist:
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = shard.max_over_ranks(ev0.elapsed_time(ev1), dist, device="cuda")
         return ms, reps * len(sets)
 
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
@@ -256,11 +257,7 @@ def main():
     clocks = clk.stop()
     ms_attn, n_attn = timed(attn_only, args.attn_steps)
 
-    emitted_all = emitted
-    if dist:
-        t = torch.tensor([emitted], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t)
-        emitted_all = int(t.item())
+    emitted_all = int(shard.sum_over_ranks(emitted, dist, device="cuda"))
     per_step_ms = ms_step / n_steps
     value = world * n_steps / (ms_step / 1e3)
     attn_us = 1e3 * ms_attn / n_attn
@@ -299,11 +296,7 @@ def main():
         for k, t in outs.items():
             host_out[k].copy_(t, non_blocking=True)
         stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = shard.max_over_ranks(time.perf_counter() - t0, dist, device="cuda")
     e2e = {"value": world * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 

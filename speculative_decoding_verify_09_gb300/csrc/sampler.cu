@@ -7,18 +7,27 @@
 // from the last target row.  Same section: temperature / nucleus modify the
 // probabilities before the scheme.  Batch without padding: EMS-SD abstract.
 //
-// Kernel layout: one CTA per logits row (target rows 0..R-1, then draft rows).
-// Each CTA streams its row once from HBM (max), then re-reads it from L2 for
-// the weight sum and, with top_p < 1, for the nucleus cut.  The last CTA of a
-// sequence to finish (atomic arrival count, no waiting) takes that sequence's
-// decisions, draws its token and, in the fused step, appends its accepted K/V
-// rows.
+// Three paths, chosen on the host (plan_sampler):
+//  * Cluster path (top_p >= 1, slice of a row <= 512 vectors per CTA): one
+//    thread-block cluster of 8 CTAs per sequence, every phase exchanged through
+//    distributed shared memory; a few KB of shared memory per CTA, so in the
+//    fused step it runs beside the attention's CTAs (see the cluster kernel).
+//  * Chunked statistics (top_p >= 1, longer rows, or no room for a cluster):
+//    CTA (row, chunk) -> the last chunk of a row merges, the last row of a
+//    sequence runs the accept tests; then the draw kernel.
+//  * Nucleus path (top_p < 1): one CTA per row streams it once from HBM into
+//    shared memory (or from L2 when longer than 64 KB) and finds max, sum and
+//    the tie-inclusive nucleus cut on chip; the last row of a sequence runs the
+//    accept tests; then the draw kernel (per-sequence chunks of row n_i) draws
+//    and, in the fused step, appends the accepted K/V rows.
 //
-// Precision: per-element weights exp((l - lmax)/T) are fp32 (exp2f with the
-// constant log2(e)/T held as two floats); sums use Kahan fp32 per thread and
-// fp64 across threads; the accept test is evaluated in fp64; the inverse-CDF
-// draw accumulates exact 64-bit fixed-point values (2^-52 units), so the
-// chosen index does not depend on the summation order.
+// Precision: per-element weights 2^((l - lmax) log2(e)/T) in fp32 (the two
+// statistics paths: exp2f and float-float sums; the cluster path: the SFU's
+// approximate exp2 and fp32 (max, sum) merges, relative error below ~2e-6);
+// the accept test compares u * p_hat < q_hat in fp32; the inverse-CDF draw
+// accumulates exact 64-bit fixed-point weights (2^-52 units), so the chosen
+// index does not depend on the summation order.  The near-tie windows of the
+// decisions (1e-5) are far wider than these errors.
 #include <algorithm>
 
 #include "common.cuh"
