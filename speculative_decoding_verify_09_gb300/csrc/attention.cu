@@ -50,6 +50,10 @@ constexpr int kKW = 4;            // consumer warps splitting the keys of one ti
 constexpr int kMaxBatch = 1024;   // sequences per call
 constexpr int kMaxGroups = 256;   // shared-prefix groups per call
 constexpr int kMaxStages = 8;
+// The split weighs each segment as its tiles plus kSegCost tiles: starting and
+// finishing a segment (Q load, epilogue, partial, merge) costs about that much
+// time, so CTAs that cross more segments get fewer tiles and all end together.
+constexpr int kSegCost = 3;
 constexpr uint32_t kSpinLimit = 1u << 22;   // polls of one mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -114,7 +118,7 @@ struct AttnCfg {
   static constexpr int kMergeO = 2 * kRows * kOStride * 4;      // two key-slice sums
   static constexpr int kMergeML = kCW * kRowsW * 8;
   static constexpr int kFinal = kRows * 8;
-  static_assert(kMaxBatch * 8 <= 2 * kStageB, "unit bases staged in the ring");
+  static_assert(kMaxBatch * 16 <= 2 * kStageB, "unit tile and cost bases staged in the ring");
 
   static SmemMap map(int ns, int units_cap, int groups_cap) {
     auto up = [](int x, int a) { return (x + a - 1) / a * a; };
@@ -240,11 +244,14 @@ __device__ __forceinline__ Sched sched_view(unsigned char *base, int mode, int H
   return S;
 }
 
-// Fill the schedule tables and the per-unit tile offsets `ubase` (block-wide,
-// identical in every CTA).  Returns the global tile count W, 0 if there is no
-// work, -1 if the inputs are inconsistent (dev_status gets BAD_LENGTH).
+// Fill the schedule tables, the per-unit tile offsets `ubase` and cost offsets
+// `cbase` (a segment costs its tiles + kSegCost; block-wide, identical in every
+// CTA).  Returns the global tile count W (scratch[0]; the total cost in
+// scratch[1]), 0 if there is no work, -1 if the inputs are inconsistent
+// (dev_status gets BAD_LENGTH).
 template <int NT>
-__device__ int64_t build_sched(const AttnParams &P, Sched &S, int64_t *ubase, int64_t *scratch) {
+__device__ int64_t build_sched(const AttnParams &P, Sched &S, int64_t *ubase, int64_t *cbase,
+                               int64_t *scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B;
   int bad = 0;
@@ -286,26 +293,34 @@ __device__ int64_t build_sched(const AttnParams &P, Sched &S, int64_t *ubase, in
     if (P.mode == 2 || P.mode == 1) return -1;
   }
   if (warp == 0) {
-    int64_t carry = 0, segc = 0;
+    int64_t carry = 0, segc = 0, costc = 0;
     for (int base = 0; base < S.units; base += 32) {
       const int u = base + lane;
       const int64_t nsu = u < S.units ? S.nseg(u) : 0;
-      const int64_t v = u < S.units ? static_cast<int64_t>(S.nt[u]) * nsu : 0;
-      int64_t inc = v, sinc = nsu;
+      const int64_t ntu = u < S.units ? S.nt[u] : 0;
+      const int64_t v = ntu * nsu;
+      const int64_t cv = ntu > 0 ? (ntu + kSegCost) * nsu : 0;
+      int64_t inc = v, sinc = nsu, cinc = cv;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
         const int64_t t2 = __shfl_up_sync(0xffffffffu, sinc, o);
-        if (lane >= o) { inc += t; sinc += t2; }
+        const int64_t t3 = __shfl_up_sync(0xffffffffu, cinc, o);
+        if (lane >= o) { inc += t; sinc += t2; cinc += t3; }
       }
       if (u < S.units) {
         ubase[u] = carry + inc - v;
+        cbase[u] = costc + cinc - cv;
         if (P.mode == 2) S.segb[u] = static_cast<int32_t>(segc + sinc - nsu);
       }
       carry += __shfl_sync(0xffffffffu, inc, 31);
       segc += __shfl_sync(0xffffffffu, sinc, 31);
+      costc += __shfl_sync(0xffffffffu, cinc, 31);
     }
-    if (lane == 0) scratch[0] = carry;
+    if (lane == 0) {
+      scratch[0] = carry;
+      scratch[1] = costc;
+    }
   }
   __syncthreads();
   return scratch[0];
@@ -326,9 +341,24 @@ __device__ __forceinline__ bool cursor_advance(Cursor &c, const Sched &S) {
   return true;
 }
 
-// CTA whose range [c*W/G, (c+1)*W/G) holds global tile t (requires G <= W).
+// CTA whose range [c*W/G, (c+1)*W/G) holds position t (requires G <= W).
 __device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t W, int64_t G) {
   return ((t + 1) * G + W - 1) / W - 1;
+}
+
+// Global tile at cost position x (0 <= x <= Wc): the first tile of the segment
+// while x is inside the segment's kSegCost lead-in, then one tile per cost unit.
+__device__ __forceinline__ int64_t tile_of_cost(int64_t x, const Sched &S, const int64_t *ubase,
+                                                const int64_t *cbase, int64_t Wc, int64_t W) {
+  if (x >= Wc) return W;
+  int lo = 0, hi = S.units - 1;          // largest unit with cbase <= x (it has tiles)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cbase[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  const int64_t nt = S.nt[lo], per = nt + kSegCost;
+  const int64_t rel = x - cbase[lo], sg = rel / per, within = rel - sg * per;
+  return ubase[lo] + sg * nt + (within > kSegCost ? within - kSegCost : 0);
 }
 
 struct SeqInfo {       // one segment
@@ -578,6 +608,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   MergeJob *jobs = reinterpret_cast<MergeJob *>(smem + Mp.jobs);
   float2 *mfin = reinterpret_cast<float2 *>(smem + Mp.jobs + kJobs * sizeof(MergeJob));
   int64_t *ubase = reinterpret_cast<int64_t *>(smem);     // staged in the ring before it starts
+  int64_t *cbase = ubase + Mp.units_cap;
   int *misc = reinterpret_cast<int *>(smem + Mp.misc);
   int64_t *misc64 = reinterpret_cast<int64_t *>(smem + Mp.misc + 16);
   volatile int *abort_flag = misc + 1;
@@ -587,17 +618,20 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   Sched S = sched_view(smem + Mp.sched, P.mode, P.Hkv, Mp.units_cap, Mp.groups_cap);
-  const int64_t W = build_sched<C::kThreads>(P, S, ubase, misc64);
+  const int64_t W = build_sched<C::kThreads>(P, S, ubase, cbase, misc64);
   if (W <= 0) return;
   if (W > P.tiles_bound) {
     if (blockIdx.x == 0 && tid == 0) set_status(P.dev_status, SV_DEV_BAD_LENGTH);
     return;
   }
+  const int64_t Wc = misc64[1];                 // total cost
   const int64_t G = W < static_cast<int64_t>(gridDim.x) ? W : static_cast<int64_t>(gridDim.x);
   if (blockIdx.x >= G) return;
-  const int64_t t_begin = (static_cast<int64_t>(blockIdx.x) * W) / G;
-  const int64_t t_end = (static_cast<int64_t>(blockIdx.x + 1) * W) / G;
-  const int ntiles = static_cast<int>(t_end - t_begin);   // >= 1 since G <= W
+  // equal cost per CTA (tiles + kSegCost per segment started), contiguous in tile order
+  const int64_t t_begin = tile_of_cost((static_cast<int64_t>(blockIdx.x) * Wc) / G, S, ubase, cbase, Wc, W);
+  const int64_t t_end = tile_of_cost((static_cast<int64_t>(blockIdx.x + 1) * Wc) / G, S, ubase, cbase, Wc, W);
+  const int ntiles = static_cast<int>(t_end - t_begin);
+  if (ntiles <= 0) return;                      // a range inside a segment's lead-in
 
   Cursor cur;
   {
@@ -612,7 +646,8 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     cur.s = static_cast<int>(rel / S.nt[lo]);
     cur.lt = static_cast<int>(rel - static_cast<int64_t>(cur.s) * S.nt[lo]);
   }
-  int64_t seg_first_tile = t_begin - cur.lt;   // global index of the segment's tile 0
+  // cost position of the current segment's start (its lead-in, then its tiles)
+  int64_t seg_cost = cbase[cur.u] + static_cast<int64_t>(cur.s) * (S.nt[cur.u] + kSegCost);
   if (tid == 0) {
     for (int s2 = 0; s2 < NS; ++s2) {
       mbar_init(rg.full + 8 * s2, 32);          // one cp.async arrival per producer lane
@@ -852,8 +887,8 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     }
     const float *mob = merge_o + C::kRows * OS;   // buffer B; merge_o is A
     const int seg = cs.seg;
-    const int64_t c_first = cta_of_tile(seg_first_tile, W, G);
-    const int64_t c_last = cta_of_tile(seg_first_tile + cs.nt - 1, W, G);
+    const int64_t c_first = cta_of_tile(seg_cost + kSegCost, Wc, G);
+    const int64_t c_last = cta_of_tile(seg_cost + kSegCost + cs.nt - 1, Wc, G);
     const int npieces = static_cast<int>(c_last - c_first + 1);
     constexpr int rows_m = C::kRows;
     if (npieces == 1 && P.mode == 0) {   // the whole segment is here: normalize, store
@@ -879,12 +914,63 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
       }
       if (tid < Mi) __stcg(&P.part_ml[slot * rows_m + tid], fin[tid]);
-      if (npieces > 1 && P.mode == 0)    // plain mode: the merger counts pieces, the last merges
+      if (npieces > 1 && P.mode == 0 && !last) {
+        // plain mode, mid-range: the merger warp counts the piece; the last merges
         post_job(MergeJob{seg, npieces, Mi, cs.r0, cs.hk, c_first});
+      } else if (npieces > 1 && P.mode == 0) {
+        // the CTA's final piece: the consumer warps (idle from here on) count it
+        // and, if it is the last to arrive, merge with all their threads and every
+        // piece's loads in flight together
+        csync();
+        if (tid == 0) {
+          __threadfence();
+          const unsigned old = atomicInc(&P.counters[seg], static_cast<unsigned>(npieces - 1));
+          misc[0] = old == static_cast<unsigned>(npieces - 1) ? 1 : 0;
+        }
+        csync();
+        if (misc[0]) {
+          __threadfence();
+          if (tid < Mi) {                  // fin is free: the partial is written
+            float mm = -INFINITY, den = 0.0f;
+#pragma unroll 4
+            for (int c = 0; c < npieces; ++c) {
+              const float2 v = __ldcg(&P.part_ml[(c_first + c + seg) * rows_m + tid]);
+              const float mn = fmaxf(mm, v.x);
+              const float mu = mn == -INFINITY ? 0.0f : mn;
+              den = den * fast_exp2(mm - mu) + v.y * fast_exp2(v.x - mu);
+              mm = mn;
+            }
+            fin[tid] = make_float2(mm, den);
+          }
+          csync();
+          for (int e = tid; e < Mi * (D / 4); e += NC) {
+            const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
+            const float mm = fin[m].x, den = fin[m].y;
+            const float mu = mm == -INFINITY ? 0.0f : mm;
+            const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+            for (int c = 0; c < npieces; ++c) {
+              const int64_t slot2 = c_first + c + seg;
+              const float f = fast_exp2(__ldcg(&P.part_ml[slot2 * rows_m + m].x) - mu);
+              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d));
+              acc.x = fmaf(f, ov.x, acc.x);
+              acc.y = fmaf(f, ov.y, acc.y);
+              acc.z = fmaf(f, ov.z, acc.z);
+              acc.w = fmaf(f, ov.w, acc.w);
+            }
+            const int j = m / g, hg = m - j * g;
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) = pk;
+          }
+        }
+      }
     }
     csync();                           // merge buffers reusable
     if (last || !ok) break;
-    seg_first_tile += cs.nt;
+    seg_cost += cs.nt + kSegCost;
     cursor_advance(cur, S);
     if (!begin_segment()) { ok = false; break; }
   }
@@ -928,13 +1014,16 @@ __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const Merge
   Sched Sp = sched_view(msm + kTables, 2, MP.P.Hkv, kMaxBatch, kMaxGroups);
   int64_t *ud = reinterpret_cast<int64_t *>(msm + 2 * kTables);
   int64_t *up = ud + kMaxBatch;
-  int64_t *scratch = up + kMaxGroups;
+  int64_t *cd = up + kMaxGroups;
+  int64_t *cp = cd + kMaxBatch;
+  int64_t *scratch = cp + kMaxGroups;
   AttnParams P = MP.P;
   P.mode = 1;
-  const int64_t Wd = build_sched<kMergeNT>(P, Sd, ud, scratch);
+  const int64_t Wd = build_sched<kMergeNT>(P, Sd, ud, cd, scratch);
   AttnParams P2 = MP.P;
   P2.mode = 2;
-  const int64_t Wp = build_sched<kMergeNT>(P2, Sp, up, scratch + 1);
+  const int64_t Wp = build_sched<kMergeNT>(P2, Sp, up, cp, scratch + 2);
+  const int64_t Wcd = scratch[1], Wcp = scratch[3];
   if (Wd <= 0 || Wp < 0) return;
   const int i = blockIdx.x / P.Hkv, hk = blockIdx.x - i * P.Hkv;
   if (Sd.nt[i] == 0) return;
@@ -943,8 +1032,8 @@ __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const Merge
   // decode pieces
   const int64_t Gd = Wd < MP.dec_grid ? Wd : MP.dec_grid;
   const int seg_d = i * P.Hkv + hk;
-  const int64_t td = ud[i] + static_cast<int64_t>(hk) * Sd.nt[i];
-  const int64_t cfd = cta_of_tile(td, Wd, Gd), cld = cta_of_tile(td + Sd.nt[i] - 1, Wd, Gd);
+  const int64_t td = cd[i] + static_cast<int64_t>(hk) * (Sd.nt[i] + kSegCost) + kSegCost;
+  const int64_t cfd = cta_of_tile(td, Wcd, Gd), cld = cta_of_tile(td + Sd.nt[i] - 1, Wcd, Gd);
   // prefix pieces
   const int gg = P.group[i];
   const int ntp = Wp > 0 ? Sp.nt[gg] : 0;
@@ -955,10 +1044,10 @@ __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const Merge
     const int rb = (i - Sp.first[gg]) / P.spb;
     const int s_in = hk * nrb + rb;
     seg_p = Sp.segb[gg] + s_in;
-    const int64_t tp = up[gg] + static_cast<int64_t>(s_in) * ntp;
+    const int64_t tp = cp[gg] + static_cast<int64_t>(s_in) * (ntp + kSegCost) + kSegCost;
     const int64_t Gp = Wp < MP.pre_grid ? Wp : MP.pre_grid;
-    cfp = cta_of_tile(tp, Wp, Gp);
-    clp = cta_of_tile(tp + ntp - 1, Wp, Gp);
+    cfp = cta_of_tile(tp, Wcp, Gp);
+    clp = cta_of_tile(tp + ntp - 1, Wcp, Gp);
     rowoff = (r0 - P.cu_q[Sp.first[gg] + rb * P.spb]) * g;
   }
   for (int e = threadIdx.x; e < Mi * (D / 2); e += kMergeNT) {
@@ -994,7 +1083,7 @@ __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const Merge
   }
 }
 
-constexpr int kMergeSmem = 2 * (kMaxBatch * 4 + 4 * kMaxGroups * 4) + (kMaxBatch + kMaxGroups + 2) * 8;
+constexpr int kMergeSmem = 2 * (kMaxBatch * 4 + 4 * kMaxGroups * 4) + (2 * kMaxBatch + 2 * kMaxGroups + 4) * 8;
 
 // ---------------------------------------------------------------------------
 // fp32 kernel (CUDA cores): one CTA per (sequence, KV head), whole segment.
