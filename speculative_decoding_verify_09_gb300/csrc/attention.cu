@@ -60,7 +60,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Byte offsets of the dynamic shared memory (same on host and device).
 struct SmemMap {
   int ns;                  // ring stages
-  int units_cap, groups_cap;
+  int units_cap, groups_cap, b_cap;
   int q;                   // two Q slots (header + packed rows)
   int merge_o, merge_ml, fin, jobs, bars, sched, misc, total;
 };
@@ -99,6 +99,12 @@ struct AttnParams {
   SmemMap sm;
 };
 
+// Bytes of the schedule tables (see Sched): int64 kst, int32 klen, cuq, nt, and
+// four int32 group tables.
+__host__ __device__ constexpr int sched_bytes(int units_cap, int groups_cap, int b_cap) {
+  return 8 * units_cap + 4 * units_cap + 4 * b_cap + 4 * units_cap + 16 * groups_cap;
+}
+
 // ---------------------------------------------------------------- smem layout
 // Warps: 4 key slices (16 keys of each 64-key tile) x RS row groups (8*NB
 // packed query rows each), then the producer warp.  Packed row m = j*g + hg
@@ -120,12 +126,13 @@ struct AttnCfg {
   static constexpr int kFinal = kRows * 8;
   static_assert(kMaxBatch * 16 <= 2 * kStageB, "unit tile and cost bases staged in the ring");
 
-  static SmemMap map(int ns, int units_cap, int groups_cap) {
+  static SmemMap map(int ns, int units_cap, int groups_cap, int b_cap) {
     auto up = [](int x, int a) { return (x + a - 1) / a * a; };
     SmemMap m;
     m.ns = ns;
     m.units_cap = up(std::max(units_cap, 1), 4);
     m.groups_cap = up(std::max(groups_cap, 1), 4);
+    m.b_cap = up(b_cap + 1, 4);
     int off = ns * kStageB;
     m.q = off;
     off += 2 * kQSlotB;
@@ -140,7 +147,7 @@ struct AttnCfg {
     m.bars = up(off, 8);
     off = m.bars + (2 * ns + 5 + 2 * kJobs) * 8;
     m.sched = up(off, 16);
-    off = m.sched + 4 * (m.units_cap + 4 * m.groups_cap);
+    off = m.sched + sched_bytes(m.units_cap, m.groups_cap, m.b_cap);
     m.misc = up(off, 16);
     m.total = m.misc + 64;
     return m;
@@ -220,6 +227,9 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 //   mode 2:   segment (KV head, row-block) over the group's prefix rows, for
 //             the packed query rows of up to spb whole sequences of the group.
 struct Sched {
+  int64_t *kst;         // [units] first pool row: kv_start (mode 0/1) or prefix_start (mode 2)
+  int32_t *klen;        // [units] kv_len (mode 0/1) or prefix_len (mode 2)
+  int32_t *cuq;         // [B+1] cu_q
   int32_t *nt;          // [units] tiles per segment
   int32_t *ns;          // [groups] segments per unit (mode 2)
   int32_t *first;       // [groups] first sequence of the group (mode 2)
@@ -231,9 +241,12 @@ struct Sched {
 };
 
 __device__ __forceinline__ Sched sched_view(unsigned char *base, int mode, int Hkv, int units_cap,
-                                            int groups_cap) {
+                                            int groups_cap, int b_cap) {
   Sched S;
-  S.nt = reinterpret_cast<int32_t *>(base);
+  S.kst = reinterpret_cast<int64_t *>(base);
+  S.klen = reinterpret_cast<int32_t *>(S.kst + units_cap);
+  S.cuq = S.klen + units_cap;
+  S.nt = S.cuq + b_cap;
   S.ns = S.nt + units_cap;
   S.first = S.ns + groups_cap;
   S.cnt = S.first + groups_cap;
@@ -260,7 +273,13 @@ __device__ int64_t build_sched(const AttnParams &P, Sched &S, int64_t *ubase, in
     const int64_t kv0 = P.kv_start[i];
     const bool ok = r0 >= 0 && r1 - r0 >= 1 && r1 - r0 <= P.max_q_rows && r1 <= P.num_rows &&
                     L >= 0 && kv0 >= 0 && kv0 + L <= P.pool_rows;
-    if (P.mode != 2) S.nt[i] = ok ? (L + (r1 - r0) + kTileKeys - 1) / kTileKeys : 0;
+    S.cuq[i] = r0;
+    if (i == B - 1) S.cuq[B] = r1;
+    if (P.mode != 2) {
+      S.nt[i] = ok ? (L + (r1 - r0) + kTileKeys - 1) / kTileKeys : 0;
+      S.klen[i] = L;
+      S.kst[i] = kv0;
+    }
     bad |= !ok;
     if (P.mode != 0) {          // shared-prefix groups: non-decreasing, in range
       const int gi = P.group[i];
@@ -282,6 +301,8 @@ __device__ int64_t build_sched(const AttnParams &P, Sched &S, int64_t *ubase, in
       S.cnt[gg] = n;
       S.ns[gg] = P.Hkv * ((n + P.spb - 1) / P.spb);
       S.nt[gg] = ok ? (pl + kTileKeys - 1) / kTileKeys : 0;
+      S.klen[gg] = pl;
+      S.kst[gg] = ps;
     }
   }
   bad = __syncthreads_or(bad);
@@ -377,11 +398,11 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams &P, const Sched &S,
   s.nt = S.nt[c.u];
   if (S.mode != 2) {
     const int i = c.u;
-    s.r0 = P.cu_q[i];
-    s.Ri = P.cu_q[i + 1] - s.r0;
+    s.r0 = S.cuq[i];
+    s.Ri = S.cuq[i + 1] - s.r0;
     s.M = s.Ri * P.g;
-    s.L = P.kv_len[i];
-    s.kv0 = P.kv_start[i];
+    s.L = S.klen[i];
+    s.kv0 = S.kst[i];
     s.hk = c.s;
     s.seg = i * P.Hkv + c.s;
   } else {
@@ -390,11 +411,11 @@ __device__ __forceinline__ SeqInfo load_seq(const AttnParams &P, const Sched &S,
     const int rb = c.s - s.hk * nrb;
     const int f = S.first[c.u] + rb * P.spb;
     const int n = min(P.spb, S.cnt[c.u] - rb * P.spb);
-    s.r0 = P.cu_q[f];
-    s.M = (P.cu_q[f + n] - s.r0) * P.g;
+    s.r0 = S.cuq[f];
+    s.M = (S.cuq[f + n] - s.r0) * P.g;
     s.Ri = 0;
-    s.L = P.prefix_len[c.u];
-    s.kv0 = P.prefix_start[c.u];
+    s.L = S.klen[c.u];
+    s.kv0 = S.kst[c.u];
     s.seg = S.segb[c.u] + c.s;
   }
   return s;
@@ -617,7 +638,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   float2 *fin = reinterpret_cast<float2 *>(smem + Mp.fin);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  Sched S = sched_view(smem + Mp.sched, P.mode, P.Hkv, Mp.units_cap, Mp.groups_cap);
+  Sched S = sched_view(smem + Mp.sched, P.mode, P.Hkv, Mp.units_cap, Mp.groups_cap, Mp.b_cap);
   const int64_t W = build_sched<C::kThreads>(P, S, ubase, cbase, misc64);
   if (W <= 0) return;
   if (W > P.tiles_bound) {
@@ -1008,10 +1029,10 @@ struct MergeParams {
 template <int D>
 __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const MergeParams MP) {
   extern __shared__ __align__(16) unsigned char msm[];
-  constexpr int kTables = kMaxBatch * 4 + 4 * kMaxGroups * 4;
+  constexpr int kTables = sched_bytes(kMaxBatch, kMaxGroups, kMaxBatch + 4);
   if (MP.P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  Sched Sd = sched_view(msm, 1, MP.P.Hkv, kMaxBatch, kMaxGroups);
-  Sched Sp = sched_view(msm + kTables, 2, MP.P.Hkv, kMaxBatch, kMaxGroups);
+  Sched Sd = sched_view(msm, 1, MP.P.Hkv, kMaxBatch, kMaxGroups, kMaxBatch + 4);
+  Sched Sp = sched_view(msm + kTables, 2, MP.P.Hkv, kMaxBatch, kMaxGroups, kMaxBatch + 4);
   int64_t *ud = reinterpret_cast<int64_t *>(msm + 2 * kTables);
   int64_t *up = ud + kMaxBatch;
   int64_t *cd = up + kMaxGroups;
@@ -1083,7 +1104,8 @@ __global__ void __launch_bounds__(kMergeNT) attn_prefix_merge_kernel(const Merge
   }
 }
 
-constexpr int kMergeSmem = 2 * (kMaxBatch * 4 + 4 * kMaxGroups * 4) + (2 * kMaxBatch + 2 * kMaxGroups + 4) * 8;
+constexpr int kMergeSmem = 2 * sched_bytes(kMaxBatch, kMaxGroups, kMaxBatch + 4) +
+                           (2 * kMaxBatch + 2 * kMaxGroups + 4) * 8;
 
 // ---------------------------------------------------------------------------
 // fp32 kernel (CUDA cores): one CTA per (sequence, KV head), whole segment.
@@ -1194,7 +1216,7 @@ __global__ void __launch_bounds__(kF32NT) attn_f32_kernel(const AttnParams P, co
 template <int D, int RS, int NB>
 SmemMap smem_map_for(const AttnParams &P, int ns) {
   using C = AttnCfg<D, RS, NB>;
-  return P.mode == 2 ? C::map(ns, P.G, P.G) : C::map(ns, P.B, 1);
+  return P.mode == 2 ? C::map(ns, P.G, P.G, P.B) : C::map(ns, P.B, 1, P.B);
 }
 
 // Ring stages for a launch: as many as fit in smem_cap (2..kMaxStages).
