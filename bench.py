@@ -266,35 +266,23 @@ def main():
     sha = src_sha()
     traffic = traffic_record(sha)
 
-    # end to end through the C ABI with pinned host buffers
+    # end to end through the C ABI: every step copies its inputs (one pinned
+    # host arena -> one device arena), runs the fused call and copies its
+    # results back (one device arena -> pinned host), then synchronizes
+    from speculative_decoding_verify_09_gb300.buffers import StagedStep
     d = sets[0]
-    host_in = {k: torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).pin_memory()
-               for k, v in (("q", inp["q"]), ("k_new", inp["k_new"]), ("v_new", inp["v_new"]),
-                            ("tgt", inp["target_logits"]), ("drf", inp["draft_logits"]),
-                            ("drafts", inp["draft_tokens"]), ("cu_q", inp["cu_q"]),
-                            ("kv_len", inp["kv_len"]), ("kv_start", inp["kv_start"]),
-                            ("kv_cap", inp["kv_cap"]), ("seq_ids", inp["seq_ids"]))}
-    dev_views = {"q": d.q.view(torch.int16), "k_new": d.k_new.view(torch.int16),
-                 "v_new": d.v_new.view(torch.int16), "tgt": d.tgt.view(torch.int16),
-                 "drf": d.drf.view(torch.int16), "drafts": d.drafts, "cu_q": d.cu_q,
-                 "kv_len": d.kv_len, "kv_start": d.kv_start, "kv_cap": d.kv_cap,
-                 "seq_ids": d.seq_ids}
-    outs = {"out": d.out.view(torch.int16), "num_accepted": d.num_accepted,
-            "out_tokens": d.out_tokens, "new_kv_len": d.new_kv_len}
-    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    staged = StagedStep(d)
+    staged.pack(inp)
+    h2d, d2h = staged.in_bytes, staged.out_bytes
     for it in range(3 + args.e2e_steps):
         if it == 3:
             if dist:
                 dist.barrier()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        for k, t in host_in.items():
-            dev_views[k].copy_(t, non_blocking=True)
-        step(d)
-        for k, t in outs.items():
-            host_out[k].copy_(t, non_blocking=True)
+        staged.upload()
+        api.spec_verify_step(staged.attn, staged.sample, d.kv_cap, d.new_kv_len, d.ws)
+        staged.download()
         stream.synchronize()
     e2e_s = shard.max_over_ranks(time.perf_counter() - t0, dist, device="cuda")
     e2e = {"value": world * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -83,3 +83,94 @@ class StepBuffers:
 
     def status_bits(self):
         return int(self.status.item()) & 0xFFFFFFFF
+
+
+def _torch_dtype(a):
+    return {np.dtype(np.uint16): torch.bfloat16, np.dtype(np.float32): torch.float32,
+            np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64}[a.dtype]
+
+
+class StagedStep:
+    """A step's per-step inputs and outputs in two contiguous device arenas,
+    each with a pinned host mirror, so that a step is one host-to-device copy,
+    the fused call and one device-to-host copy.  The KV pools, the workspace and
+    the argument structs are those of `base` (a StepBuffers), which stay
+    resident on the device.
+
+    Inputs: q, k_new, v_new, target / draft logits, draft tokens, cu_q, kv_len,
+    kv_start, kv_cap, seq_ids.  Outputs: out, num_accepted, out_tokens,
+    new_kv_len.  Write a step's inputs with `pack` (or into `host_in` views),
+    then `upload`, run the step on `base`'s structs, `download`."""
+
+    IN = ("q", "k_new", "v_new", "target_logits", "draft_logits", "draft_tokens", "cu_q",
+          "kv_len", "kv_start", "kv_cap", "seq_ids")
+    OUT = ("out", "num_accepted", "out_tokens", "new_kv_len")
+
+    def __init__(self, base):
+        self.base = base
+        ins = {"q": base.q, "k_new": base.k_new, "v_new": base.v_new,
+               "target_logits": base.tgt, "draft_logits": base.drf,
+               "draft_tokens": base.drafts, "cu_q": base.cu_q, "kv_len": base.kv_len,
+               "kv_start": base.kv_start, "kv_cap": base.kv_cap, "seq_ids": base.seq_ids}
+        outs = {"out": base.out, "num_accepted": base.num_accepted,
+                "out_tokens": base.out_tokens, "new_kv_len": base.new_kv_len}
+        self.in_bytes, self.host_in, self.dev_in, self._in = self._arena(ins)
+        self.out_bytes, self.host_out, self.dev_out, self._out = self._arena(outs)
+        # the step's structs point into the device arenas from now on
+        for name, t in self._in[1].items():
+            setattr(base, {"target_logits": "tgt", "draft_logits": "drf",
+                           "draft_tokens": "drafts"}.get(name, name), t)
+        for name, t in self._out[1].items():
+            setattr(base, name, t)
+        self._rebind()
+
+    @staticmethod
+    def _arena(tensors):
+        offs, off = {}, 0
+        for name, t in tensors.items():
+            offs[name] = off
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        devb = torch.empty(off, dtype=torch.uint8, device="cuda")
+        hv, dv = {}, {}
+        for name, t in tensors.items():
+            n = t.numel() * t.element_size()
+            hv[name] = host[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+            dv[name] = devb[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+            dv[name].copy_(t)
+        return off, host, devb, (hv, dv)
+
+    def _rebind(self):
+        b, api = self.base, self.base.api
+        pre = {}
+        if getattr(b, "group", None) is not None:
+            pre = dict(group=b.group, prefix_start=b.prefix_start, prefix_len=b.prefix_len,
+                       prefix_rows_bound=b.attn.prefix_rows_bound)
+        self.attn = b.attn = api.attn_args(
+            b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.cu_q, b.kv_start, b.kv_len, b.out,
+            max_q_rows=b.attn.max_q_rows, kv_rows_bound=b.attn.kv_rows_bound,
+            scale=b.attn.scale, dev_status=b.status, **pre)
+        s = b.sample
+        self.sample = b.sample = api.sample_args(
+            b.tgt, b.drf, b.drafts, b.cu_q, b.kv_len, b.num_accepted, b.out_tokens,
+            max_q_rows=s.max_q_rows, temperature=s.temperature, top_p=s.top_p, seed=s.seed,
+            seq_ids=b.seq_ids, dev_status=b.status)
+
+    def pack(self, inp):
+        """Write a host input dict (bf16 as uint16 bits) into the pinned arena."""
+        hv = self._in[0]
+        for name in self.IN:
+            a = np.ascontiguousarray(inp[name])
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            hv[name].view(torch.int16 if hv[name].dtype == torch.bfloat16 else hv[name].dtype) \
+                .copy_(torch.from_numpy(a).view(hv[name].shape))
+
+    def upload(self):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def download(self):
+        self.host_out.copy_(self.dev_out, non_blocking=True)
+
+    def result(self, name):
+        return self._out[0][name]

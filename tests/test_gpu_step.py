@@ -119,3 +119,27 @@ def test_repeated_steps_are_identical(api):
         outs.append((d.out.clone(), d.out_tokens.clone(), d.new_kv_len.clone()))
     for o in outs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
+
+
+def test_staged_step_one_copy_each_way(api):
+    """Inputs in one pinned arena, one copy in, the fused call, one copy out:
+    the host-side results equal the oracle's (same check as the plain path)."""
+    from speculative_decoding_verify_09_gb300.buffers import StagedStep
+    inp = W.make_inputs(W.workload("bass_b8", B=4, Hq=8, Hkv=8, V=2000, L_lo=50, L_hi=400,
+                                   gen_seed=29))
+    d = DeviceStep(inp, api)
+    st = StagedStep(d)
+    st.dev_in.zero_()                      # nothing left over from construction
+    st.pack(inp)
+    st.upload()
+    api.spec_verify_step(st.attn, st.sample, d.kv_cap, d.new_kv_len, d.ws)
+    st.download()
+    torch.cuda.synchronize()
+    ref = oracle.verify_step(inp)
+    out = st.result("out").float().numpy()
+    assert np.max(np.abs(out - ref["out"])) < 2e-2
+    _, ties = compare_sampling(ref, st.result("num_accepted").numpy(),
+                               st.result("out_tokens").numpy(), inp["cu_q"])
+    if ties == 0:
+        assert np.array_equal(st.result("new_kv_len").numpy(), ref["new_kv_len"])
+    assert d.status_bits() == ref["status"]
