@@ -18,7 +18,7 @@ from .philox import philox4x32, verify_uniforms, word_to_uniform
 from .sampling import (process_row, accept, residual, sample_index, verify_sequence,
                        reject_sample, to_f64, bf16_bits_to_f64, TIE_EPS, TIE_ACCEPT, TIE_DRAW,
                        DEV_CAPACITY, DEV_BAD_TOKEN, DEV_NONFINITE, DEV_EMPTY_RESIDUAL,
-                       DEV_BAD_LENGTH)
+                       DEV_BAD_LENGTH, DEV_BAD_PARAM, params_ok)
 from .attention import attention_row, verify_attention
 from .append import kv_append
 from .step import verify_step

@@ -21,9 +21,18 @@ Readings where the pages are silent (each one is listed in the design notes):
   * the compare is `u * p_hat(x~) < q_hat(x~)` with u in [0,1): for p_hat > 0
     this is u < min(1, q/p) with no division, p == q always accepts, and for
     p_hat == 0 the draft is accepted iff q_hat > 0;
-  * temperature first (z = logit / T), then nucleus on the tempered softmax;
-    the nucleus keeps {x : z_x >= tau}, tau the largest attained value whose
-    upper set holds mass >= top_p (tie-inclusive, no index tie-break);
+  * temperature first (z = logit / T), then top-k, then nucleus on the
+    renormalized top-k distribution (the usual order of these transforms);
+    top-k keeps {x : z_x >= tau_k}, tau_k the k-th largest value of z counted
+    with multiplicity (ties at the boundary kept); the nucleus keeps
+    {x : z_x >= tau}, tau the largest attained value whose upper set holds
+    mass >= top_p (tie-inclusive, no index tie-break);
+  * temperature 0 is greedy decoding: the processed row is one-hot at the
+    first (lowest-index) maximum of the logits, and the accept / residual
+    rules then keep a draft iff it is that argmax;
+  * per-sequence temperature / top_p / top_k arrays override the scalars; an
+    invalid per-sequence value (T < 0 or NaN, top_p <= 0 or NaN, top_k < 0)
+    makes that sequence fail with the NONFINITE and BAD_PARAM bits;
   * the same processing is applied to q and p;
   * the inverse-CDF draw walks the vocabulary in index order and takes the first
     x whose cumulative weight exceeds u * Z (strict, so zero weights are never
@@ -43,6 +52,7 @@ DEV_BAD_TOKEN = 2
 DEV_NONFINITE = 4
 DEV_EMPTY_RESIDUAL = 8
 DEV_BAD_LENGTH = 16
+DEV_BAD_PARAM = 64
 
 # Near-tie audit windows.  Decisions this close to a boundary may legitimately
 # differ between an fp32 GPU path and this fp64 oracle; they are counted and
@@ -93,21 +103,39 @@ class ProcessedRow:
         self.probs, self.valid, self.tau, self.margin = probs, valid, tau, margin
 
 
-def process_row(logits, temperature, top_p):
-    """Temperature then nucleus, on one row of exact float64 logits.
+def params_ok(temperature, top_p, top_k):
+    """Valid processing parameters (as float32 / int32 values)."""
+    T = float(np.float32(temperature))
+    tp = float(np.float32(top_p))
+    return T >= 0.0 and tp > 0.0 and int(top_k) >= 0
+
+
+def process_row(logits, temperature, top_p, top_k=0):
+    """Temperature, then top-k, then nucleus, on one row of exact float64
+    logits; temperature 0 is greedy (one-hot at the first maximum).
 
     temperature and top_p are taken as the float32 values the C-ABI receives.
     """
     T = float(np.float32(temperature))
     tp = float(np.float32(top_p))
+    k = int(top_k)
     l = np.asarray(logits, dtype=np.float64)
     V = l.shape[0]
     if np.any(np.isnan(l)) or np.any(l == np.inf) or not np.any(l > -np.inf):
         return ProcessedRow(np.zeros(V), False, np.nan, np.inf)
+    if T == 0.0:                         # greedy
+        probs = np.zeros(V)
+        x = int(np.argmax(l))            # first maximum
+        probs[x] = 1.0
+        return ProcessedRow(probs, True, l[x], np.inf)
     z = l / T
     w = np.exp(z - z.max())              # exp(-inf) = 0 for masked entries
+    tau_k = -np.inf
+    if 0 < k < V:
+        tau_k = np.sort(z)[::-1][k - 1]  # k-th largest, with multiplicity
+        w = np.where(z >= tau_k, w, 0.0)
     if tp >= 1.0:
-        return ProcessedRow(w / w.sum(), True, -np.inf, np.inf)
+        return ProcessedRow(w / w.sum(), True, tau_k, np.inf)
     P = w / w.sum()
     # Tie classes of equal z, highest first; upper-set masses M_k.
     vals, inv = np.unique(z, return_inverse=True)
@@ -226,14 +254,16 @@ def verify_sequence(q_rows, p_rows, drafts, u_acc, u_smp, audit=None):
 # the batch
 # --------------------------------------------------------------------------
 def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
-                  temperature, top_p, seed, seq_ids=None):
+                  temperature, top_p, seed, seq_ids=None, top_k=0, temperatures=None,
+                  top_ps=None, top_ks=None):
     """Batched verify sampling over ragged sequences (no padding).
 
     target_logits [R, V], draft_logits [R-B, V] (stored float32 or bf16 bits);
     rows of sequence i: target cu_q[i] + j (j = 0..K_i), draft cu_q[i] - i + j
     (j = 0..K_i-1); draft_tokens [R-B] indexed like the draft rows.
     Row j decides token index pos = kv_len[i] + j + 1 with Philox uniforms
-    keyed by (seed, seq_id, pos).
+    keyed by (seed, seq_id, pos).  temperatures / top_ps / top_ks ([B] or
+    None) override temperature / top_p / top_k per sequence.
 
     Returns dict with num_accepted [B] (-1 for a failed sequence), out_tokens
     [R] (drafts for j < n_i, the sampled token at j = n_i, -1 after; all -1 for
@@ -269,9 +299,16 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
         p0 = r0 - i
         pos = kv_len[i] + np.arange(K + 1, dtype=np.int64) + 1
         u_acc, u_smp = verify_uniforms(seed, seq_ids[i], pos)
-        qp = [process_row(to_f64(target_logits[r0 + j]), temperature, top_p)
+        T_i = temperature if temperatures is None else temperatures[i]
+        tp_i = top_p if top_ps is None else top_ps[i]
+        tk_i = top_k if top_ks is None else top_ks[i]
+        if not params_ok(T_i, tp_i, tk_i):
+            seq_status[i] = DEV_NONFINITE | DEV_BAD_PARAM
+            num_acc[i] = -1
+            continue
+        qp = [process_row(to_f64(target_logits[r0 + j]), T_i, tp_i, tk_i)
               for j in range(K + 1)]
-        pp = [process_row(to_f64(draft_logits[p0 + j]), temperature, top_p)
+        pp = [process_row(to_f64(draft_logits[p0 + j]), T_i, tp_i, tk_i)
               for j in range(K)]
         if not all(r.valid for r in qp + pp):
             seq_status[i] = DEV_NONFINITE

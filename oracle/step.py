@@ -33,7 +33,8 @@ def verify_step(inp, attention=True):
                                prefix)
     s = reject_sample(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
                       inp["cu_q"], inp["kv_len"], inp["temperature"], inp["top_p"],
-                      inp["seed"], inp.get("seq_ids"))
+                      inp["seed"], inp.get("seq_ids"), inp.get("top_k", 0),
+                      inp.get("temperatures"), inp.get("top_ps"), inp.get("top_ks"))
     kc, vc, new_len, st = kv_append(inp["k_cache"], inp["v_cache"], inp["k_new"],
                                     inp["v_new"], inp["cu_q"], inp["kv_start"],
                                     inp["kv_len"], inp["kv_cap"], s["num_accepted"])

@@ -477,3 +477,114 @@ def test_top_p_one_is_identity_and_minus_inf_is_masked():
     assert abs(r.probs.sum() - 1) < 1e-15
     assert not S.process_row(np.full(4, -np.inf), 1.0, 1.0).valid
     assert not S.process_row(np.array([0.0, np.inf]), 1.0, 0.9).valid
+
+
+# --------------------------------------------------------------------------
+# greedy, top-k and per-sequence parameters (SpS, "compatibility with
+# standard sampling methods": the transforms apply before the scheme)
+# --------------------------------------------------------------------------
+def _topk_by_sorting(z, k):
+    """Keep the k largest values, ties at the boundary kept, by full sort."""
+    order = sorted(range(len(z)), key=lambda x: -z[x])
+    thresh = z[order[k - 1]]
+    return np.array([zz >= thresh for zz in z])
+
+
+@pytest.mark.parametrize("k", [1, 2, 5, 17, 99, 100, 150])
+def test_top_k_matches_sorting_with_ties(k):
+    rng = np.random.default_rng(k)
+    for T in (1.0, 0.7):
+        l = rng.integers(-6, 6, size=100).astype(np.float64) * 0.5     # heavy ties
+        l[rng.integers(0, 100, size=5)] = -np.inf
+        r = S.process_row(l, T, 1.0, k)
+        z = l / float(np.float32(T))
+        if k < 100:
+            keep = _topk_by_sorting(z, k)
+        else:
+            keep = np.ones(100, dtype=bool)
+        w = np.where(keep, np.exp(z - z[np.isfinite(z)].max()), 0.0)
+        assert np.allclose(r.probs, w / w.sum(), rtol=1e-12, atol=0)
+        assert (r.probs > 0).sum() >= min(k, int(np.isfinite(l).sum()))
+
+
+def test_top_k_then_top_p_is_nucleus_of_the_renormalized_top_k():
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        l = rng.normal(0, 2, size=60)
+        l[:10] = np.round(l[:10])                       # a few ties
+        k, tp = int(rng.integers(1, 60)), float(np.float32(rng.uniform(0.1, 0.99)))
+        r = S.process_row(l, 1.0, tp, k)
+        keep = _topk_by_sorting(l, k)
+        w = np.where(keep, np.exp(l - l.max()), 0.0)
+        P = w / w.sum()
+        nuc = _nucleus_by_sorting(np.where(keep, l, -np.inf), tp)
+        want = np.where(np.isin(np.arange(len(l)), sorted(nuc)), P, 0.0)
+        if r.margin > 1e-9:
+            assert np.allclose(r.probs, want / want.sum(), rtol=1e-12, atol=0)
+
+
+def test_greedy_row_is_one_hot_at_first_maximum():
+    l = np.array([0.5, 3.0, -1.0, 3.0, 2.0, -np.inf])
+    r = S.process_row(l, 0.0, 0.9, 3)
+    assert r.valid and list(r.probs) == [0, 1, 0, 0, 0, 0]
+    r = S.process_row(np.array([-np.inf, -np.inf]), 0.0, 1.0)
+    assert not r.valid
+
+
+def test_greedy_batch_keeps_drafts_equal_to_the_argmax_then_emits_it():
+    """Closed form: with T = 0 a step keeps drafts while they equal the
+    argmax of the target row, then emits the argmax of the first row that
+    disagrees (or of the bonus row)."""
+    rng = np.random.default_rng(8)
+    B, V = 6, 40
+    K = rng.integers(0, 5, size=B)
+    cu = np.concatenate([[0], np.cumsum(K + 1)]).astype(np.int32)
+    R = int(cu[-1])
+    tgt = rng.integers(-5, 5, size=(R, V)).astype(np.float32)      # ties in the argmax
+    src = np.concatenate([np.arange(cu[i], cu[i + 1] - 1) for i in range(B)])
+    drf = tgt[src] + rng.integers(-1, 2, size=(R - B, V)).astype(np.float32)
+    drafts = np.array([int(np.argmax(tgt[src[j]])) if rng.random() < 0.7 else
+                       int(rng.integers(0, V)) for j in range(R - B)], dtype=np.int32)
+    res = S.reject_sample(tgt, drf, drafts, cu, np.zeros(B, dtype=np.int32), 0.0, 1.0, 9)
+    for i in range(B):
+        r0, p0 = int(cu[i]), int(cu[i]) - i
+        n = 0
+        while n < K[i] and drafts[p0 + n] == int(np.argmax(tgt[r0 + n])):
+            n += 1
+        assert res["num_accepted"][i] == n
+        assert list(res["out_tokens"][r0:r0 + n]) == list(drafts[p0:p0 + n])
+        assert res["out_tokens"][r0 + n] == int(np.argmax(tgt[r0 + n]))
+
+
+def test_per_sequence_parameters_equal_separate_batches():
+    rng = np.random.default_rng(12)
+    B, V = 5, 300
+    _, _, tgt, drf, cu = _batch_logits(rng, V, B, 3)
+    drafts = rng.integers(0, V, size=int(cu[-1]) - B).astype(np.int32)
+    kv = rng.integers(0, 100, size=B).astype(np.int32)
+    Ts = np.array([1.0, 0.0, 0.6, 1.3, 0.0], dtype=np.float32)
+    tps = np.array([1.0, 0.9, 0.5, 0.95, 1.0], dtype=np.float32)
+    tks = np.array([0, 0, 20, 5, 3], dtype=np.int32)
+    seq_ids = np.arange(B, dtype=np.int64) + 40
+    whole = S.reject_sample(tgt, drf, drafts, cu, kv, 1.0, 1.0, 77, seq_ids, 0, Ts, tps, tks)
+    for i in range(B):
+        r0, r1, p0 = int(cu[i]), int(cu[i + 1]), int(cu[i]) - i
+        one = S.reject_sample(tgt[r0:r1], drf[p0:p0 + r1 - r0 - 1], drafts[p0:p0 + r1 - r0 - 1],
+                              np.array([0, r1 - r0]), kv[i:i + 1], Ts[i], tps[i], 77,
+                              seq_ids[i:i + 1], tks[i])
+        assert whole["num_accepted"][i] == one["num_accepted"][0]
+        assert list(whole["out_tokens"][r0:r1]) == list(one["out_tokens"])
+
+
+def test_bad_per_sequence_parameters_fail_only_that_sequence():
+    rng = np.random.default_rng(13)
+    B, V = 4, 64
+    _, _, tgt, drf, cu = _batch_logits(rng, V, B, 2)
+    drafts = rng.integers(0, V, size=int(cu[-1]) - B).astype(np.int32)
+    Ts = np.array([1.0, -1.0, np.nan, 1.0], dtype=np.float32)
+    tps = np.array([1.0, 1.0, 1.0, 0.0], dtype=np.float32)
+    res = S.reject_sample(tgt, drf, drafts, cu, np.zeros(B, dtype=np.int32), 1.0, 1.0, 1,
+                          None, 0, Ts, tps, None)
+    assert list(res["num_accepted"][1:]) == [-1, -1, -1] and res["num_accepted"][0] >= 0
+    assert res["seq_status"][1] == S.DEV_NONFINITE | S.DEV_BAD_PARAM
+    assert np.all(res["out_tokens"][cu[1]:] == -1)
