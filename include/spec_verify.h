@@ -54,7 +54,7 @@ extern "C" {
 #endif
 
 #define SV_API __attribute__((visibility("default")))
-#define SV_ABI_VERSION 1
+#define SV_ABI_VERSION 2
 
 typedef enum sv_status {
   SV_OK = 0,
@@ -80,9 +80,12 @@ enum {
   SV_DEV_BAD_LENGTH = 16u,     /* cu_q / kv_len / kv_start / prefix values
                                   inconsistent with the host bounds or the
                                   pool: that sequence is skipped */
-  SV_DEV_TIMEOUT = 32u         /* an internal wait of the attention pipeline
+  SV_DEV_TIMEOUT = 32u,        /* an internal wait of the attention pipeline
                                   gave up (not expected; outputs of the
                                   affected CTA are left unwritten) */
+  SV_DEV_BAD_PARAM = 64u       /* a per-sequence temperature < 0 or NaN, top_p
+                                  <= 0 or NaN, or top_k < 0: that sequence
+                                  fails (with SV_DEV_NONFINITE) */
 };
 
 /* Verify attention (a1, a1b).  scale * q.k softmax over keys
@@ -131,7 +134,7 @@ typedef struct sv_sample_args {
   int32_t dtype;            /* sv_dtype of both logits tensors */
   int32_t max_q_rows;       /* host bound on R_i, 1..16 */
   int64_t num_rows;         /* R = cu_q[B] (host copy) */
-  float temperature;        /* > 0 */
+  float temperature;        /* >= 0; 0 = greedy */
   float top_p;              /* (0, 1]; >= 1 disables the nucleus */
   uint64_t seed;            /* Philox key */
   const int32_t *cu_q;      /* [dev] [B+1] */
@@ -143,6 +146,17 @@ typedef struct sv_sample_args {
   int32_t *num_accepted;    /* [dev] [B] out */
   int32_t *out_tokens;      /* [dev] [R] out */
   uint32_t *dev_status;     /* [dev] one word */
+  /* Added in ABI 2.  Processing order: temperature, top-k, top-p (the
+   * speculative-sampling paper, section "Modified rejection sampling": such
+   * transforms change q and p before the scheme).  temperature 0 is greedy:
+   * q and p become one-hot at the first (lowest-index) maximum, so a draft is
+   * kept iff it is the target row's argmax.  top_k > 0 keeps the tokens whose
+   * logit is at least the k-th largest (ties at the boundary kept); top-p then
+   * applies to the renormalized top-k distribution. */
+  int32_t top_k;            /* >= 0; 0 disables */
+  const float *temperatures;/* [dev] [B] per-sequence temperature or NULL */
+  const float *top_ps;      /* [dev] [B] per-sequence top_p or NULL */
+  const int32_t *top_ks;    /* [dev] [B] per-sequence top_k or NULL */
 } sv_sample_args;
 
 /* Workspace bytes for an attention call, a sampling call, or (both

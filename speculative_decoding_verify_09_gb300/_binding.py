@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
 SV_OK, SV_ERR_INVALID, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = range(5)
 SV_F32, SV_BF16 = 0, 1
 DEV_CAPACITY, DEV_BAD_TOKEN, DEV_NONFINITE, DEV_EMPTY_RESIDUAL, DEV_BAD_LENGTH = 1, 2, 4, 8, 16
+DEV_TIMEOUT, DEV_BAD_PARAM = 32, 64
 
 _p = ctypes.c_void_p
 
@@ -41,7 +42,8 @@ class SampleArgs(ctypes.Structure):
         ("temperature", ctypes.c_float), ("top_p", ctypes.c_float), ("seed", ctypes.c_uint64),
         ("cu_q", _p), ("target_logits", _p), ("draft_logits", _p), ("draft_tokens", _p),
         ("kv_len", _p), ("seq_ids", _p), ("num_accepted", _p), ("out_tokens", _p),
-        ("dev_status", _p),
+        ("dev_status", _p), ("top_k", ctypes.c_int32), ("temperatures", _p), ("top_ps", _p),
+        ("top_ks", _p),
     ]
 
 

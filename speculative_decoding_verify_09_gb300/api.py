@@ -66,10 +66,12 @@ def attn_args(q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, *,
 
 def sample_args(target_logits, draft_logits, draft_tokens, cu_q, kv_len, num_accepted,
                 out_tokens, *, max_q_rows, temperature, top_p, seed, seq_ids=None,
-                dev_status=None):
+                dev_status=None, top_k=0, temperatures=None, top_ps=None, top_ks=None):
     """sv_sample_args for target_logits [R, V], draft_logits [R-B, V],
     draft_tokens [R-B] int32, cu_q [B+1], kv_len [B], outputs num_accepted [B]
-    and out_tokens [R] (int32), seq_ids [B] int64 or None."""
+    and out_tokens [R] (int32), seq_ids [B] int64 or None.  temperature 0 is
+    greedy; top_k 0 disables top-k; temperatures / top_ps ([B] float32) and
+    top_ks ([B] int32) override the scalars per sequence."""
     s = SampleArgs()
     R, V = target_logits.shape
     s.batch = cu_q.shape[0] - 1
@@ -86,8 +88,10 @@ def sample_args(target_logits, draft_logits, draft_tokens, cu_q, kv_len, num_acc
     s.kv_len, s.seq_ids = _ptr(kv_len), _ptr(seq_ids)
     s.num_accepted, s.out_tokens = _ptr(num_accepted), _ptr(out_tokens)
     s.dev_status = _ptr(dev_status)
+    s.top_k = int(top_k)
+    s.temperatures, s.top_ps, s.top_ks = _ptr(temperatures), _ptr(top_ps), _ptr(top_ks)
     s._keep = (target_logits, draft_logits, draft_tokens, cu_q, kv_len, seq_ids, num_accepted,
-               out_tokens, dev_status)
+               out_tokens, dev_status, temperatures, top_ps, top_ks)
     return s
 
 

@@ -71,12 +71,16 @@ class StepBuffers:
         if "target_logits" in inp:
             self.tgt, self.drf = dev(inp["target_logits"]), dev(inp["draft_logits"])
             self.drafts = dev(inp["draft_tokens"])
+            per = {k: dev(np.asarray(inp[k])) for k in ("temperatures", "top_ps", "top_ks")
+                   if inp.get(k) is not None}
+            self.per_seq = per
             self.sample = api.sample_args(self.tgt, self.drf, self.drafts, self.cu_q, self.kv_len,
                                           self.num_accepted, self.out_tokens,
                                           max_q_rows=self.max_q_rows,
                                           temperature=inp["temperature"], top_p=inp["top_p"],
                                           seed=inp["seed"] if seed is None else seed,
-                                          seq_ids=self.seq_ids, dev_status=self.status)
+                                          seq_ids=self.seq_ids, dev_status=self.status,
+                                          top_k=inp.get("top_k", 0), **per)
         else:
             self.sample = None
         self.ws = api.Workspace.for_args(self.attn, self.sample)
@@ -154,7 +158,8 @@ class StagedStep:
         self.sample = b.sample = api.sample_args(
             b.tgt, b.drf, b.drafts, b.cu_q, b.kv_len, b.num_accepted, b.out_tokens,
             max_q_rows=s.max_q_rows, temperature=s.temperature, top_p=s.top_p, seed=s.seed,
-            seq_ids=b.seq_ids, dev_status=b.status)
+            seq_ids=b.seq_ids, dev_status=b.status, top_k=s.top_k,
+            **getattr(b, "per_seq", {}))
 
     def pack(self, inp):
         """Write a host input dict (bf16 as uint16 bits) into the pinned arena."""

@@ -97,8 +97,9 @@ sv_status check_sample(const sv_sample_args *a) {
   if (a->num_rows < a->batch || a->num_rows > static_cast<int64_t>(a->batch) * a->max_q_rows)
     return fail(SV_ERR_INVALID, "sampling: num_rows %lld inconsistent with batch %d and max_q_rows %d",
                 static_cast<long long>(a->num_rows), a->batch, a->max_q_rows);
-  if (!(a->temperature > 0.0f) || !std::isfinite(a->temperature))
-    return fail(SV_ERR_INVALID, "sampling: temperature must be finite and > 0 (greedy not built)");
+  if (!(a->temperature >= 0.0f) || !std::isfinite(a->temperature))
+    return fail(SV_ERR_INVALID, "sampling: temperature must be finite and >= 0 (0 = greedy)");
+  if (a->top_k < 0) return fail(SV_ERR_INVALID, "sampling: top_k must be >= 0");
   if (!(a->top_p > 0.0f) || std::isnan(a->top_p))
     return fail(SV_ERR_INVALID, "sampling: top_p must be > 0");
   if (a->batch > 0) {

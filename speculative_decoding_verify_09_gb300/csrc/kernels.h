@@ -20,7 +20,8 @@ struct RowStats {
   uint32_t valid;     // 0: NaN / +inf / only -inf in the row
   float inv_hi;       // 1 / ssum as a float-float pair
   float inv_lo;
-  uint32_t pad;
+  int32_t amax;       // greedy row (temperature 0): index of the one-hot; else -1
+  float c_hi, c_lo;   // log2(e) / T of the row's sequence as a float pair
   double ssum;        // sum over the kept set of exp((l - lmax) / T)
 };
 

@@ -137,12 +137,18 @@ struct RowPass {
   // f(bits[EPV]) for every vector this thread owns, in increasing v.
   template <typename F>
   __device__ __forceinline__ void each(F &&f) const {
+    each_v([&](int, const uint32_t (&b)[LT<T>::EPV]) { f(b); });
+  }
+
+  // f(v, bits[EPV]) for every vector v this thread owns, in increasing v.
+  template <typename F>
+  __device__ __forceinline__ void each_v(F &&f) const {
     constexpr int EPV = LT<T>::EPV;
     if (cached) {
       for (int v = threadIdx.x; v < NV; v += kSampNT) {
         uint32_t b[EPV];
         unpack<T>(srow[v], b);
-        f(b);
+        f(v, b);
       }
     } else {
       for (int base = 0; base < NV; base += kStream * kSampNT) {
@@ -157,7 +163,7 @@ struct RowPass {
           if (base + k * kSampNT + static_cast<int>(threadIdx.x) < NV) {
             uint32_t b[EPV];
             unpack<T>(tmp[k], b);
-            f(b);
+            f(base + k * kSampNT + static_cast<int>(threadIdx.x), b);
           }
         }
       }
@@ -263,11 +269,19 @@ __device__ __forceinline__ int seq_of_draft_row(const int32_t *cu_q, int B, int 
 // many, over the whole row).
 // --------------------------------------------------------------------------
 template <typename T>
-__device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, float top_p,
-                            SampSmem &sm, uint32_t &tau_out, double &ssum_out) {
+__device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf0, uint32_t kmin, double S,
+                            float top_p, SampSmem &sm, uint32_t &tau_out, double &ssum_out) {
   constexpr int EPV = LT<T>::EPV;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   const double target = static_cast<double>(top_p) * S;
+  // weights of the elements kept by top-k (keys below kmin weigh 0)
+  struct Masked {
+    WeightFn f;
+    uint32_t kmin;
+    __device__ __forceinline__ float operator()(uint32_t bits) const {
+      return LT<T>::key(bits) < kmin ? 0.0f : f(LT<T>::val(bits));
+    }
+  } wb{wf0, kmin};
 
   // coarse bins: bin b = min((127 - biased_exp(w)) / 4, 7)
   float acc[8];
@@ -276,7 +290,7 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, 
   rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
-      const float x = wf(LT<T>::val(bits[e]));
+      const float x = wb(bits[e]);
       const int ex = 127 - static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);
       const int b = min(max(ex, 0) >> 2, 7);
 #pragma unroll
@@ -304,7 +318,7 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, 
   int mine = 0;
   rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) mine += is_cand(wf(LT<T>::val(bits[e]))) ? 1 : 0;
+    for (int e = 0; e < EPV; ++e) mine += is_cand(wb(bits[e])) ? 1 : 0;
   });
   unsigned long long total = 0;
   const unsigned long long off =
@@ -315,7 +329,7 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, 
     rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float x = wf(LT<T>::val(bits[e]));
+        const float x = wb(bits[e]);
         if (is_cand(x)) {
           sm.cand_key[o] = LT<T>::key(bits[e]);
           sm.cand_w[o] = x;
@@ -336,7 +350,7 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf, double S, 
       rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
-          if (LT<T>::key(bits[e]) >= cand) sum += wf(LT<T>::val(bits[e]));
+          if (LT<T>::key(bits[e]) >= cand) sum += wb(bits[e]);
       });
     }
     return sum;
@@ -366,37 +380,42 @@ struct RowProb {
   WeightFn wf;
   uint32_t tau;
   float inv_hi, inv_lo;
+  int amax;            // >= 0: greedy row, one-hot at this index
 };
 
-__device__ __forceinline__ RowProb rowprob_of(const RowStats *st, float c_hi, float c_lo) {
+__device__ __forceinline__ RowProb rowprob_of(const RowStats *st) {
   RowProb r;
-  r.wf = WeightFn{__ldcg(&st->lmax), c_hi, c_lo};
+  r.wf = WeightFn{__ldcg(&st->lmax), __ldcg(&st->c_hi), __ldcg(&st->c_lo)};
   r.tau = __ldcg(&st->tau_key);
   r.inv_hi = __ldcg(&st->inv_hi);
   r.inv_lo = __ldcg(&st->inv_lo);
+  r.amax = __ldcg(&st->amax);
   return r;
 }
 
+// q_hat of vocabulary index x whose logit has the bits `bits`.
 template <typename T>
-__device__ __forceinline__ float row_prob(const RowProb &rp, uint32_t bits) {
+__device__ __forceinline__ float row_prob(const RowProb &rp, uint32_t bits, int x) {
+  if (rp.amax >= 0) return x == rp.amax ? 1.0f : 0.0f;
   if (LT<T>::key(bits) < rp.tau) return 0.0f;
   const float w = rp.wf(LT<T>::val(bits));
   return __fmaf_rn(w, rp.inv_hi, __fmul_rn(w, rp.inv_lo));
 }
 
-// Fixed-point (2^-52) draw weight of one vector: mode 0 the residual
-// max(0, q_hat - p_hat), mode 1 q_hat.  Element e of the vector is `e`.
+// Fixed-point (2^-52) draw weight of vocabulary index x: mode 0 the residual
+// max(0, q_hat - p_hat), mode 1 q_hat.
 template <typename T>
 __device__ __forceinline__ unsigned long long fix_weight(const RowProb &pq, const RowProb &pp,
-                                                         int mode, uint32_t bq, uint32_t bp) {
-  float r = row_prob<T>(pq, bq);
-  if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp)), 0.0f);
+                                                         int mode, uint32_t bq, uint32_t bp, int x) {
+  float r = row_prob<T>(pq, bq, x);
+  if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp, x)), 0.0f);
   return fix52(r);
 }
 
-// Finish a row's statistics (one thread): ssum and its float-float inverse.
+// Finish a row's statistics (one thread): ssum and its float-float inverse,
+// the row's log2(e)/T constant and, for a greedy row, its argmax.
 __device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t tau, bool valid,
-                                            double ssum) {
+                                            double ssum, float c_hi, float c_lo, int amax) {
   RowStats o;
   o.lmax = lmax;
   o.tau_key = tau;
@@ -404,7 +423,9 @@ __device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t t
   const double inv = valid && ssum > 0.0 ? 1.0 / ssum : 0.0;
   o.inv_hi = static_cast<float>(inv);
   o.inv_lo = static_cast<float>(inv - static_cast<double>(o.inv_hi));
-  o.pad = 0;
+  o.amax = valid ? amax : -1;
+  o.c_hi = c_hi;
+  o.c_lo = c_lo;
   o.ssum = ssum;
   *st = o;
 }
@@ -448,10 +469,10 @@ __device__ void accept_sequence(const SampParams &P, int i) {
     } else {
       const T *tgt = static_cast<const T *>(a.target_logits);
       const T *drf = static_cast<const T *>(a.draft_logits);
-      const RowProb pq = rowprob_of(&st[r0 + lane], P.c_hi, P.c_lo);
-      const RowProb pp = rowprob_of(&st[R + p0 + lane], P.c_hi, P.c_lo);
-      const float qh = row_prob<T>(pq, LT<T>::bits(tgt[static_cast<int64_t>(r0 + lane) * V + d]));
-      const float ph = row_prob<T>(pp, LT<T>::bits(drf[static_cast<int64_t>(p0 + lane) * V + d]));
+      const RowProb pq = rowprob_of(&st[r0 + lane]);
+      const RowProb pp = rowprob_of(&st[R + p0 + lane]);
+      const float qh = row_prob<T>(pq, LT<T>::bits(tgt[static_cast<int64_t>(r0 + lane) * V + d]), d);
+      const float ph = row_prob<T>(pp, LT<T>::bits(drf[static_cast<int64_t>(p0 + lane) * V + d]), d);
       const U4 w = philox4x32_10(U4{static_cast<uint32_t>(L + lane + 1), sid_lo, sid_hi, 0u}, k0, k1);
       const float u = static_cast<float>(u24(w.x)) * 0x1p-24f;          // exact
       rej = !(__fmul_rn(u, ph) < qh);
@@ -630,7 +651,7 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
         }
       }
       const bool valid = !anybad && M > -INFINITY;
-      write_stats(&P.ws.stats[r], M, 0u, valid, ff_to_double(S));
+      write_stats(&P.ws.stats[r], M, 0u, valid, ff_to_double(S), P.c_hi, P.c_lo, -1);
     }
   }
   __syncthreads();
@@ -638,10 +659,32 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
 }
 
 // --------------------------------------------------------------------------
-// Phase 1b (nucleus): one CTA per row.  The row is read once from HBM into
-// shared memory (or streamed from L2 when longer than 64 KB), then max, sum,
-// and the nucleus cut run on chip.
+// Phase 1b (nucleus, top-k, greedy, per-sequence parameters): one CTA per row.
+// The row is read once from HBM into shared memory (or streamed from L2 when
+// longer than 64 KB), then max, top-k key, sum and the nucleus cut run on chip.
 // --------------------------------------------------------------------------
+// Order-preserving key of the k-th largest element of the row (largest key
+// with at least k elements at or above it), by a bitwise search with one
+// counting pass per key bit.
+template <typename T>
+__device__ uint32_t topk_key(const RowPass<T> &rp, int k, SampSmem &sm) {
+  constexpr int EPV = LT<T>::EPV;
+  uint32_t tau = 0;
+  for (int bit = LT<T>::KEY_BITS - 1; bit >= 0; --bit) {
+    const uint32_t cand = tau | (1u << bit);
+    unsigned long long mine = 0;
+    rp.each([&](const uint32_t (&bits)[EPV]) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) mine += LT<T>::key(bits[e]) >= cand ? 1ull : 0ull;
+    });
+    unsigned long long total;
+    block_exclusive_scan_u64<kSampNT>(mine, sm.red64, &total);
+    if (total >= static_cast<unsigned long long>(k)) tau = cand;
+    __syncthreads();
+  }
+  return tau;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) {
   const PdlTail tail{P.pdl_secondary};
@@ -673,16 +716,41 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
   });
   bad = __syncthreads_or(bad);
   mx = block_max_f<kSampNT>(mx, sm.redf);
-  const bool valid = !bad && mx > -INFINITY;
+  // this sequence's processing parameters (arrays override the scalars)
+  const float Tr = a.temperatures ? a.temperatures[i] : a.temperature;
+  const float tpr = a.top_ps ? a.top_ps[i] : a.top_p;
+  const int tkr = a.top_ks ? a.top_ks[i] : a.top_k;
+  const bool param_ok = Tr >= 0.0f && tpr > 0.0f && tkr >= 0;     // NaN fails the compares
+  if (!param_ok && tid == 0) set_status(a.dev_status, SV_DEV_BAD_PARAM);
+  const bool valid = param_ok && !bad && mx > -INFINITY;
   uint32_t tau = 0;
   double ssum = 0.0;
-  if (valid) {
-    const WeightFn wf{mx, P.c_hi, P.c_lo};
+  float c_hi = 0.0f, c_lo = 0.0f;
+  int amax = -1;
+  if (valid && Tr == 0.0f) {
+    // greedy: one-hot at the lowest index holding the maximum
+    float first = -static_cast<float>(a.vocab);
+    rp.each_v([&](int v, const uint32_t (&bits)[EPV]) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (LT<T>::val(bits[e]) == mx) first = fmaxf(first, -static_cast<float>(v * EPV + e));
+    });
+    __syncthreads();
+    amax = static_cast<int>(-block_max_f<kSampNT>(first, sm.redf));
+    ssum = 1.0;
+  } else if (valid) {
+    const double c = 1.4426950408889634 / static_cast<double>(Tr);
+    c_hi = static_cast<float>(c);
+    c_lo = static_cast<float>(c - static_cast<double>(c_hi));
+    const WeightFn wf{mx, c_hi, c_lo};
+    uint32_t kmin = 0;
+    if (tkr > 0 && tkr < a.vocab) kmin = topk_key<T>(rp, tkr, sm);
     float s = 0.0f, comp = 0.0f;
     rp.each([&](const uint32_t (&bits)[EPV]) {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float y = __fsub_rn(wf(LT<T>::val(bits[e])), comp);
+        const float wv = LT<T>::key(bits[e]) < kmin ? 0.0f : wf(LT<T>::val(bits[e]));
+        const float y = __fsub_rn(wv, comp);
         const float t = __fadd_rn(s, y);
         comp = __fsub_rn(__fsub_rn(t, s), y);
         s = t;
@@ -690,9 +758,14 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
     });
     FF S[1] = {FF{s, -comp}};
     block_sum_ff<1>(S, sm.red[1]);
-    nucleus_cut<T>(rp, wf, ff_to_double(S[0]), a.top_p, sm, tau, ssum);
+    if (tpr < 1.0f) {
+      nucleus_cut<T>(rp, wf, kmin, ff_to_double(S[0]), tpr, sm, tau, ssum);
+    } else {
+      tau = kmin;
+      ssum = ff_to_double(S[0]);
+    }
   }
-  if (tid == 0) write_stats(&P.ws.stats[r], mx, tau, valid, ssum);
+  if (tid == 0) write_stats(&P.ws.stats[r], mx, tau, valid, ssum, c_hi, c_lo, amax);
   arrive_sequence<T>(P, i, &sm.bcast[3]);
 }
 
@@ -739,7 +812,7 @@ __device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int
         unpack<T>(q[k], bq);
         if (mode == 0) unpack<T>(d[k], bd);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u);
+        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u, v * EPV + e);
       }
     }
   }
@@ -778,7 +851,7 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
         unpack<T>(load_vec<T>(trow, V, va + k, al_t), bq[k]);
         if (mode == 0) unpack<T>(load_vec<T>(drow, V, va + k, al_d), bd[k]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u);
+        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u, (va + k) * EPV + e);
       }
     }
     unsigned long long total;
@@ -793,7 +866,7 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           if (!found && va + k < v1) {
-            c += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u);
+            c += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u, (va + k) * EPV + e);
             if (c > tgt) { x = (va + k) * EPV + e; found = true; }
           }
         }
@@ -868,8 +941,8 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const T *trow = static_cast<const T *>(a.target_logits) + static_cast<int64_t>(r0 + n) * V;
   const T *drow = mode == 0 ? static_cast<const T *>(a.draft_logits) + static_cast<int64_t>(p0 + n) * V
                             : trow;
-  const RowProb pq = rowprob_of(&P.ws.stats[r0 + n], P.c_hi, P.c_lo);
-  const RowProb pp = mode == 0 ? rowprob_of(&P.ws.stats[R + p0 + n], P.c_hi, P.c_lo) : pq;
+  const RowProb pq = rowprob_of(&P.ws.stats[r0 + n]);
+  const RowProb pp = mode == 0 ? rowprob_of(&P.ws.stats[R + p0 + n]) : pq;
   const int NV = (V + EPV - 1) / EPV;
   const int per = (NV + NCH - 1) / NCH;
   const int v0 = min(NV, c * per), v1 = min(NV, v0 + per);
@@ -1389,12 +1462,15 @@ SamplerPlan plan_sampler(const sv_sample_args &a) {
   SamplerPlan p;
   const int epv = a.dtype == SV_BF16 ? 8 : 4;
   const int nv = (a.vocab + epv - 1) / epv;
-  p.stat_chunks = a.top_p < 1.0f ? 1 : std::max(1, std::min(32, (nv + 1023) / 1024));
+  // greedy, top-k and per-sequence parameters take the row path (stat_chunks 1)
+  const bool extended = a.temperature == 0.0f || a.top_k > 0 || a.temperatures || a.top_ps ||
+                        a.top_ks;
+  p.stat_chunks = a.top_p < 1.0f || extended ? 1 : std::max(1, std::min(32, (nv + 1023) / 1024));
   p.draw_chunks = std::max(1, std::min(64, (nv + 511) / 512));
   // one cluster per sequence when there is no nucleus and the rows' slices fit
   const int per = (nv + kClusterN - 1) / kClusterN;
   p.cluster_nvt = per > kClNT ? 2 : 1;
-  p.cluster = a.top_p >= 1.0f && per <= kClVPT * kClNT;
+  p.cluster = a.top_p >= 1.0f && !extended && per <= kClVPT * kClNT;
   return p;
 }
 
@@ -1459,7 +1535,7 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
     if (e == cudaSuccess) return e;
     (void)cudaGetLastError();          // no room for a cluster: two-kernel path
   }
-  if (P.plan.stat_chunks > 1 || P.a.top_p >= 1.0f) {
+  if (P.plan.stat_chunks > 1) {
     e = launch_first(stats_chunk_kernel<T>, rows * P.plan.stat_chunks, kStatNT, 0, P, s);
   } else {
     const size_t smem = kSmemRowOff + kRowSmemBytes;

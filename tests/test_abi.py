@@ -44,7 +44,7 @@ def test_exports_exactly_the_declared_symbols(binding):
 
 
 def test_struct_mirrors_and_version(binding):
-    assert binding.lib.sv_abi_version() == 1
+    assert binding.lib.sv_abi_version() == 2
     assert binding.lib.sv_struct_size(0) == ctypes.sizeof(binding.AttnArgs)
     assert binding.lib.sv_struct_size(1) == ctypes.sizeof(binding.SampleArgs)
 
@@ -96,7 +96,8 @@ def test_shared_prefix_needs_bf16(binding):
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("temperature", 0.0, 1), ("temperature", float("inf"), 1), ("top_p", 0.0, 1),
+    ("temperature", -1.0, 1), ("temperature", float("inf"), 1), ("temperature", float("nan"), 1),
+    ("top_p", 0.0, 1), ("top_k", -1, 1),
     ("vocab", 0, 4), ("vocab", 10 ** 7, 4), ("num_rows", 1, 1), ("target_logits", 0, 1),
 ])
 def test_sampling_host_validation(binding, field, value, status):

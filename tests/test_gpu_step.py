@@ -34,7 +34,8 @@ def check_step(api, inp, attn_rows=None):
     d = run_step(api, inp)
     ref_s = oracle.reject_sample(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
                                  inp["cu_q"], inp["kv_len"], inp["temperature"], inp["top_p"],
-                                 inp["seed"], inp["seq_ids"])
+                                 inp["seed"], inp["seq_ids"], inp.get("top_k", 0),
+                                 inp.get("temperatures"), inp.get("top_ps"), inp.get("top_ks"))
     na = d.num_accepted.cpu().numpy()
     _, ties = compare_sampling(ref_s, na, d.out_tokens.cpu().numpy(), inp["cu_q"])
     # append: checked against the oracle's append driven by the GPU's own
@@ -143,3 +144,15 @@ def test_staged_step_one_copy_each_way(api):
     if ties == 0:
         assert np.array_equal(st.result("new_kv_len").numpy(), ref["new_kv_len"])
     assert d.status_bits() == ref["status"]
+
+
+
+def test_step_with_per_sequence_parameters(api):
+    """Fused step on the row path (greedy / top-k / nucleus per sequence):
+    decisions, appended rows and lengths as the oracle's."""
+    inp = W.make_inputs(W.workload("bass_b8", B=6, Hq=8, Hkv=8, V=3000, L_lo=40, L_hi=300,
+                                   gen_seed=51))
+    inp["temperatures"] = np.array([0.0, 1.0, 0.7, 0.0, 1.2, 0.9], dtype=np.float32)
+    inp["top_ps"] = np.array([1.0, 0.9, 1.0, 1.0, 0.6, 0.95], dtype=np.float32)
+    inp["top_ks"] = np.array([0, 20, 5, 0, 0, 200], dtype=np.int32)
+    check_step(api, inp)

@@ -21,8 +21,8 @@ Float tensors are float32 arrays, or bfloat16 stored as uint16 bit patterns
 (rounded to nearest even from float32 draws).
 
 Draft tokens are drawn from softmax(draft_logits / T) over the full vocabulary
-(Gumbel-max with this module's RNG), standing in for the draft model's own
-sampler.
+(Gumbel-max with this module's RNG; the row's argmax when T = 0), standing in
+for the draft model's own sampler.
 """
 from dataclasses import dataclass, replace
 import numpy as np
@@ -48,6 +48,7 @@ class Workload:
     draft_noise: float = 1.0
     temperature: float = 1.0
     top_p: float = 1.0
+    top_k: int = 0             # 0: no top-k
     philox_seed: int = 0
     prefix_len: int = 0        # > 0: shared prefixes of this length (bifurcated)
     groups: int = 1            # shared-prefix groups (contiguous runs of sequences)
@@ -146,7 +147,7 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
                head_dim=w.D, dtype=w.dtype, cu_q=cu_q, kv_start=kv_start,
                kv_len=L.astype(np.int32), kv_cap=cap.astype(np.int32),
                seq_ids=np.arange(w.B, dtype=np.int64),
-               temperature=w.temperature, top_p=w.top_p, seed=w.philox_seed,
+               temperature=w.temperature, top_p=w.top_p, top_k=w.top_k, seed=w.philox_seed,
                scale=0.0, pool_rows=P)
     if shared:
         G = len(plen)
@@ -170,6 +171,9 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
         # stand-in draft sampler: Gumbel-max on draft_logits / T, row by row
         toks = np.empty(R - w.B, dtype=np.int32)
         for r in range(R - w.B):
+            if w.temperature == 0.0:         # greedy drafting: the draft row's argmax
+                toks[r] = int(np.argmax(_as_f32(drf[r])))
+                continue
             g = -np.log(-np.log(rng.uniform(np.finfo(np.float32).tiny, 1.0,
                                             size=w.V).astype(np.float64)))
             toks[r] = int(np.argmax(_as_f32(drf[r]).astype(np.float64) / w.temperature + g))
