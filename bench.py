@@ -38,8 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 def workload_desc(w):
-    return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, KV len U[{w.L_lo},{w.L_hi}], "
-            f"K={w.K_lo}, V={w.V}, {w.dtype}, T={w.temperature}, top_p={w.top_p}")
+    K = f"K={w.K_lo}" if w.K_lo == w.K_hi else f"K in [{w.K_lo},{w.K_hi}]"
+    pre = f", shared prefix {w.prefix_len}" if w.prefix_len else ""
+    return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, KV len {w.L_dist} "
+            f"[{w.L_lo},{w.L_hi}]{pre}, {K}, V={w.V}, {w.dtype}, T={w.temperature}, "
+            f"top_p={w.top_p}, top_k={w.top_k}")
 
 
 def peaks():
@@ -55,7 +58,7 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel_src_sha):
+def traffic_record(kernel_src_sha, workload=WORKLOAD):
     """DRAM bytes per attention launch from a committed ncu summary, if it was
     taken on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -63,7 +66,7 @@ def traffic_record(kernel_src_sha):
         return None
     for ln in open(p):
         f = ln.split()
-        if len(f) == 4 and f[0] == "attention" and f[1] == WORKLOAD and f[2] == kernel_src_sha:
+        if len(f) == 4 and f[0] == "attention" and f[1] == workload and f[2] == kernel_src_sha:
             return float(f[3])
     return None
 
@@ -134,14 +137,16 @@ def cpu_baseline(inp, budget_s=12.0):
         if el >= budget_s:
             break
     return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} whole {WORKLOAD} steps (attention + sampling + append), "
+            "sample": f"{n} whole {inp['workload'].name} steps (attention + sampling + append), "
                       f"{el:.1f} s, OMP/BLAS threads 1"}
 
 
 def run_reference(args, rank):
     if rank != 0:
         return
-    w = W.workload(WORKLOAD)
+    over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
+                              ("top_p", args.top_p)) if v is not None}
+    w = W.workload(args.workload, **over)
     inp = W.make_inputs(w)
     import oracle
     for _ in range(min(args.warmup, 1)):
@@ -174,6 +179,11 @@ def main():
                     help="attention-only launches timed for the roofline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch directly (profiling)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS),
+                    help="input shapes (default: the headline bass_b8)")
+    ap.add_argument("--temperature", type=float, default=None, help="override (0 = greedy)")
+    ap.add_argument("--top-k", type=int, default=None, help="override (0 = off)")
+    ap.add_argument("--top-p", type=float, default=None, help="override")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -197,7 +207,9 @@ def main():
     # weak scaling: rank r owns global sequences [r*B, (r+1)*B) of a batch of
     # world*B sequences (the same shapes on every rank, uniforms keyed by the
     # global sequence id); no exchange on the data path
-    w = W.workload(WORKLOAD)
+    over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
+                              ("top_p", args.top_p)) if v is not None}
+    w = W.workload(args.workload, **over)
     inp = W.make_inputs(w)
     lo, _ = shard.rank_range(world * w.B, rank, world)
     inp["seq_ids"] = inp["seq_ids"] + lo
@@ -218,7 +230,7 @@ def main():
     torch.cuda.synchronize()
     n_acc = sets[0].num_accepted.cpu().numpy()
     emitted = int(np.sum(n_acc + 1))
-    esz = 2
+    esz = 4 if w.dtype == "f32" else 2
     append_bytes = 2 * 2 * emitted * w.Hkv * w.D * esz        # K and V, read + write
     step_total = nbytes["attention"] + nbytes["sampler"] + append_bytes
 
@@ -264,7 +276,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
     sha = src_sha()
-    traffic = traffic_record(sha)
+    traffic = traffic_record(sha, args.workload)
 
     # end to end through the C ABI: every step copies its inputs (one pinned
     # host arena -> one device arena), runs the fused call and copies its
@@ -296,7 +308,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_steps,
             "warmup": max(args.warmup, 3), "ms_per_step": per_step_ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded; random-init tensors of the workload's shapes)",
             "config": {"workload": workload_desc(w), "parallelism": f"dp{world} (sequence shards)",
                        "global_batch": world * w.B,
