@@ -229,8 +229,14 @@ struct SampSmem {
   float redf[32];
   unsigned long long red64[32];
   int bcast[8];
-  uint32_t cand_key[kCandCap];
-  float cand_w[kCandCap];
+  unsigned long long sel[4];              // broadcast of a select step
+  union {
+    struct {                              // nucleus cut: candidates
+      uint32_t cand_key[kCandCap];
+      float cand_w[kCandCap];
+    };
+    unsigned long long hist[kSampNW][256];  // top-k select: per-warp histograms
+  };
 };
 
 constexpr size_t kSmemRowOff = (sizeof(SampSmem) + 127) / 128 * 128;
@@ -370,6 +376,81 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf0, uint32_t 
   block_sum_ff<1>(ss, sm.red[buf]);
   ssum_out = ff_to_double(ss[0]);
   tau_out = tau;
+}
+
+// --------------------------------------------------------------------------
+// Top-k key: the largest order-preserving key tau with at least k elements at
+// or above it (the k-th largest, ties kept), by a radix select over key bytes
+// from the top: per pass a 256-bin count of the elements matching the bytes
+// fixed so far (one private histogram per warp, added per bin afterwards),
+// then the largest bin whose upper count still reaches k.
+// --------------------------------------------------------------------------
+template <typename T>
+__device__ uint32_t topk_key(const RowPass<T> &rp, int k, SampSmem &sm) {
+  constexpr int EPV = LT<T>::EPV;
+  constexpr int KB = LT<T>::KEY_BITS;
+  const int tid = threadIdx.x, w = tid >> 5;
+  const unsigned long long target = static_cast<unsigned long long>(k);
+  unsigned long long *myh = sm.hist[w];
+  uint32_t prefix = 0;               // key bits fixed so far
+  unsigned long long above = 0;      // count of elements above the prefix range
+  for (int fixed = 0; fixed < KB; fixed += 8) {
+    const int shift = KB - fixed - 8;
+    for (int b = tid; b < kSampNW * 256; b += kSampNT) (&sm.hist[0][0])[b] = 0ull;
+    __syncthreads();
+    rp.each([&](const uint32_t (&bits)[EPV]) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t key = LT<T>::key(bits[e]);
+        if (fixed > 0 && (key >> (shift + 8)) != prefix) continue;
+        atomicAdd(&myh[(key >> shift) & 255u], 1ull);
+      }
+    });
+    __syncthreads();
+    for (int b = tid; b < 256; b += kSampNT) {          // add the warps' histograms
+      unsigned long long t = 0;
+#pragma unroll
+      for (int x = 0; x < kSampNW; ++x) t += sm.hist[x][b];
+      sm.hist[0][b] = t;
+    }
+    __syncthreads();
+    if (tid < 32) {                  // warp 0: the largest bin whose upper count reaches k
+      unsigned long long h[8], own = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { h[q] = sm.hist[0][8 * tid + q]; own += h[q]; }
+      unsigned long long suf = own;  // inclusive suffix over lanes >= tid
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_down_sync(0xffffffffu, suf, o);
+        if (tid + o < 32) suf += y;
+      }
+      unsigned long long run = above + suf - own;
+      int best = -1;
+      unsigned long long best_above = 0;
+#pragma unroll
+      for (int q = 7; q >= 0; --q) {
+        if (best < 0 && run + h[q] >= target) {
+          best = 8 * tid + q;
+          best_above = run;
+        }
+        run += h[q];
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, best >= 0);
+      const int src = hit ? 31 - __clz(hit) : 0;        // the highest lane holds the largest bin
+      best = __shfl_sync(0xffffffffu, best, src);
+      best_above = __shfl_sync(0xffffffffu, best_above, src);
+      if (tid == 0) {
+        if (best < 0) { best = 0; best_above = above; }
+        sm.sel[0] = (static_cast<unsigned long long>(prefix) << 8) | static_cast<unsigned>(best);
+        sm.sel[1] = best_above;
+      }
+    }
+    __syncthreads();
+    prefix = static_cast<uint32_t>(sm.sel[0]);
+    above = sm.sel[1];
+    __syncthreads();
+  }
+  return prefix;
 }
 
 // --------------------------------------------------------------------------
@@ -663,28 +744,6 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
 // The row is read once from HBM into shared memory (or streamed from L2 when
 // longer than 64 KB), then max, top-k key, sum and the nucleus cut run on chip.
 // --------------------------------------------------------------------------
-// Order-preserving key of the k-th largest element of the row (largest key
-// with at least k elements at or above it), by a bitwise search with one
-// counting pass per key bit.
-template <typename T>
-__device__ uint32_t topk_key(const RowPass<T> &rp, int k, SampSmem &sm) {
-  constexpr int EPV = LT<T>::EPV;
-  uint32_t tau = 0;
-  for (int bit = LT<T>::KEY_BITS - 1; bit >= 0; --bit) {
-    const uint32_t cand = tau | (1u << bit);
-    unsigned long long mine = 0;
-    rp.each([&](const uint32_t (&bits)[EPV]) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) mine += LT<T>::key(bits[e]) >= cand ? 1ull : 0ull;
-    });
-    unsigned long long total;
-    block_exclusive_scan_u64<kSampNT>(mine, sm.red64, &total);
-    if (total >= static_cast<unsigned long long>(k)) tau = cand;
-    __syncthreads();
-  }
-  return tau;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) {
   const PdlTail tail{P.pdl_secondary};
