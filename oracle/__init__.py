@@ -13,6 +13,8 @@ Modules (each cites the passages it follows):
   attention  ragged verify attention (plus the shared-prefix arrangement)
   append     ragged append of accepted K/V rows
   step       the three composed
+  draft      the draft side: draft-token draw (Philox stream 1) and one draft
+             position (single-row attention, append, draw)
 """
 from .philox import philox4x32, verify_uniforms, word_to_uniform
 from .sampling import (process_row, accept, residual, sample_index, verify_sequence,
@@ -22,3 +24,4 @@ from .sampling import (process_row, accept, residual, sample_index, verify_seque
 from .attention import attention_row, verify_attention
 from .append import kv_append
 from .step import verify_step
+from .draft import draft_sample, draft_step

@@ -181,6 +181,44 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
     return inp
 
 
+def make_draft_inputs(w, positions=1):
+    """Inputs of `positions` consecutive draft positions for workload `w`.
+
+    Each position is one decode step of the draft model: one block row per
+    sequence (cu_q = 0..B).  The cache is laid out as in make_inputs (drawn
+    with K_i = 0) with room for `positions` more rows per sequence.  Returns
+    (base, steps): base is the input dict of position 0 with its
+    `draft_logits` [B, V] (standing in for the draft model's outputs); steps[t]
+    holds position t's q [B, Hq, D], k_new / v_new [B, Hkv, D] and
+    draft_logits, position 0's equal to base's, later ones drawn afresh.
+    """
+    wd = replace(w, K_fixed=(0,) * w.B, cap_slack=w.cap_slack + positions - 1)
+    base = make_inputs(wd)
+    base["draft_logits"] = base.pop("target_logits")
+    base.pop("draft_tokens", None)
+    steps = [{k: base[k] for k in ("q", "k_new", "v_new", "draft_logits")}]
+    for t in range(1, positions):
+        rng = np.random.Generator(np.random.PCG64([w.gen_seed, t]))
+        st = {"q": _normal(rng, (w.B, w.Hq, w.D), 1.0, w.dtype),
+              "k_new": _normal(rng, (w.B, w.Hkv, w.D), 1.0, w.dtype),
+              "v_new": _normal(rng, (w.B, w.Hkv, w.D), 1.0, w.dtype)}
+        lg = rng.standard_normal(size=(w.B, w.V), dtype=np.float32) * np.float32(w.logit_std)
+        st["draft_logits"] = f32_to_bf16_bits(lg) if w.dtype == "bf16" else lg
+        steps.append(st)
+    return base, steps
+
+
+def draft_step_bytes(inp):
+    """Algorithmic HBM bytes of one draft position on these inputs: the KV
+    rows read once, q, the new K/V row and the output, the draft logits rows,
+    and the append's read + write of one row per sequence."""
+    esz = 4 if inp["dtype"] == "f32" else 2
+    Hq, Hkv, D, B = inp["num_q_heads"], inp["num_kv_heads"], inp["head_dim"], inp["B"]
+    kv_rows = int(np.sum(inp["kv_len"]))
+    attn = kv_rows * Hkv * D * esz * 2 + B * (2 * Hq + 2 * Hkv) * D * esz
+    return attn + B * inp["V"] * esz + 2 * B * 2 * Hkv * D * esz
+
+
 def step_bytes(inp):
     """Algorithmic HBM bytes of one verify step on these inputs.
 
