@@ -1,5 +1,8 @@
 """Benchmark of the fused verify step (spec_verify_step) on the bass_b8 workload.
 
+`--path draft` measures the draft side instead: K consecutive draft positions
+per step (single-row attention, append, draft-token draw).
+
 Default: 1 GPU.  Under torchrun, one rank per GPU, each with its own batch of
 8 sequences (global sequence ids offset by rank): weak scaling, no data-path
 collective; the barrier and the max-over-ranks timing use torch.distributed.
@@ -147,17 +150,33 @@ def run_reference(args, rank):
     over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
                               ("top_p", args.top_p)) if v is not None}
     w = W.workload(args.workload, **over)
-    inp = W.make_inputs(w)
     import oracle
+    if args.path == "draft":
+        P = args.positions or w.K_hi
+        base, dsteps = W.make_draft_inputs(w, positions=P)
+
+        def one():
+            inp = dict(base)
+            for st in dsteps:
+                inp.update(st)
+                r = oracle.draft_step(inp)
+                inp.update(k_cache=r["k_cache"], v_cache=r["v_cache"], kv_len=r["new_kv_len"])
+        metric = DRAFT_METRIC
+    else:
+        inp = W.make_inputs(w)
+
+        def one():
+            oracle.verify_step(inp)
+        metric = METRIC
     for _ in range(min(args.warmup, 1)):
-        oracle.verify_step(inp)
+        one()
     steps = max(1, min(args.steps, 3))
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.verify_step(inp)
+        one()
     el = time.perf_counter() - t0
     v = steps / el
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * el / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": workload_desc(w)},
@@ -165,6 +184,143 @@ def run_reference(args, rank):
                              "sample": f"{steps} whole steps (the requested count, capped at 3)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+DRAFT_METRIC = ("draft-side steps/s (K positions of single-row attention + append + draft "
+                "draw) at B=8 7.8B-shape; achieved HBM GB/s vs peak")
+
+
+def draft_cpu_baseline(base, steps, budget_s=12.0):
+    """The oracle's draft positions, as they stand, until the budget is used
+    (at least one whole draft-side step of len(steps) positions)."""
+    import oracle
+    n, t0 = 0, time.perf_counter()
+    while True:
+        inp = dict(base)
+        for st in steps:
+            inp.update(st)
+            r = oracle.draft_step(inp)
+            inp.update(k_cache=r["k_cache"], v_cache=r["v_cache"], kv_len=r["new_kv_len"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole draft-side steps of {len(steps)} positions, {el:.1f} s, "
+                      "OMP/BLAS threads 1"}
+
+
+def run_draft(args, w, api, shard, dist, world, rank, local_rank):
+    """The draft side of the loop: K consecutive draft positions per step."""
+    import torch
+    from speculative_decoding_verify_09_gb300.buffers import DraftBuffers
+    P = args.positions or w.K_hi
+    base, steps = W.make_draft_inputs(w, positions=P)
+    lo, _ = shard.rank_range(world * w.B, rank, world)
+    base["seq_ids"] = base["seq_ids"] + lo
+    sets = [DraftBuffers(base, api, positions=P, steps=steps) for _ in range(args.sets)]
+    stream = torch.cuda.current_stream()
+    per_pos = W.draft_step_bytes(base)
+    esz = 4 if w.dtype == "f32" else 2
+    attn_bytes = per_pos - w.B * w.V * esz - 2 * w.B * 2 * w.Hkv * w.D * esz
+
+    def timed(fn, n_launch):
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for d in sets:
+                    fn(d)
+            torch.cuda.synchronize()
+        reps = max(1, n_launch // len(sets))
+        for _ in range(2):
+            graph.replay() if graph else [fn(d) for d in sets]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            if graph:
+                graph.replay()
+            else:
+                for d in sets:
+                    fn(d)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return shard.max_over_ranks(ev0.elapsed_time(ev1), dist, device="cuda"), reps * len(sets)
+
+    for k in range(max(args.warmup, 3)):
+        sets[k % len(sets)].run_all()
+    torch.cuda.synchronize()
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
+    clk = Clocks(gpu_index)
+    time.sleep(0.3)
+    ms_step, n_steps = timed(lambda d: d.run_all(), args.steps)
+    clocks = clk.stop()
+
+    def attn0(d):
+        api.spec_verify_attn(d.attn[0], d.ws_attn)
+
+    ms_attn, n_attn = timed(attn0, args.attn_steps)
+    attn_us = 1e3 * ms_attn / n_attn
+    peak, peak_kind = peaks()
+    achieved = attn_bytes / (attn_us * 1e-6) / 1e9
+    sha = src_sha()
+    per_step_ms = ms_step / n_steps
+    step_total = P * per_pos
+
+    # end to end: every step uploads all positions' inputs (one pinned arena),
+    # runs the positions and downloads their outputs (one pinned arena)
+    d = sets[0]
+    d.stage(steps)
+    for it in range(3 + args.e2e_steps):
+        if it == 3:
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        d.upload()
+        d.run_all()
+        d.download()
+        stream.synchronize()
+    e2e_s = shard.max_over_ranks(time.perf_counter() - t0, dist, device="cuda")
+    e2e = {"value": world * args.e2e_steps / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": d.in_bytes, "d2h_bytes_per_step": d.out_bytes}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = draft_cpu_baseline(base, steps)
+    if rank == 0:
+        line = {
+            "metric": DRAFT_METRIC, "value": world * n_steps / (ms_step / 1e3), "unit": UNIT,
+            "n_gpus": world, "steps": n_steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded; random-init tensors of the workload's shapes)",
+            "config": {"workload": workload_desc(w) + f"; draft side: {P} positions of one "
+                       "query row per sequence (draft attention layer of the same shape)",
+                       "parallelism": f"dp{world} (sequence shards)", "global_batch": world * w.B,
+                       "l2": f"{len(sets)} rotating input sets; each position reads "
+                             f"{per_pos / 1e6:.0f} MB (the K positions of a step re-read one "
+                             "cache, as a draft model does)",
+                       "launch": "CUDA graph of the C-ABI calls per input set"
+                       if not args.no_graph else "direct launches"},
+            "draft_tok_s": world * w.B * P * n_steps / (ms_step / 1e3),
+            "step_bytes": step_total,
+            "step_hbm_gbs": step_total / (per_step_ms * 1e-3) / 1e9,
+            "step_frac_of_peak": step_total / (per_step_ms * 1e-3) / 1e9 / peak,
+            "roofline": {"kernel": "attention, one query row per sequence", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                         "traffic": traffic_record(sha, "draft_" + args.workload),
+                         "algorithmic_bytes_per_launch": attn_bytes,
+                         "avg_launch_us": attn_us, "kernel_src": sha},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 3 * P * n_steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -184,6 +340,11 @@ def main():
     ap.add_argument("--temperature", type=float, default=None, help="override (0 = greedy)")
     ap.add_argument("--top-k", type=int, default=None, help="override (0 = off)")
     ap.add_argument("--top-p", type=float, default=None, help="override")
+    ap.add_argument("--path", default="verify", choices=["verify", "draft"],
+                    help="verify: the fused verify step (default); draft: the draft side "
+                         "(K single-row positions per step)")
+    ap.add_argument("--positions", type=int, default=None,
+                    help="draft positions per draft-side step (default: the workload's K)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -210,6 +371,12 @@ def main():
     over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
                               ("top_p", args.top_p)) if v is not None}
     w = W.workload(args.workload, **over)
+    if args.path == "draft":
+        run_draft(args, w, api, shard, dist, world, rank, local_rank)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
     inp = W.make_inputs(w)
     lo, _ = shard.rank_range(world * w.B, rank, world)
     inp["seq_ids"] = inp["seq_ids"] + lo

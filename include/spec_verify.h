@@ -54,7 +54,7 @@ extern "C" {
 #endif
 
 #define SV_API __attribute__((visibility("default")))
-#define SV_ABI_VERSION 2
+#define SV_ABI_VERSION 3
 
 typedef enum sv_status {
   SV_OK = 0,
@@ -225,6 +225,53 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
                                   const int32_t *kv_cap, int32_t *new_kv_len, void *ws,
                                   size_t ws_bytes, void *stream);
 
+/* Draft-token draw (added in ABI 3): the sampling half of one draft
+ * position of the speculative-sampling loop.  The speculative-sampling
+ * paper's algorithm has the draft model propose its K tokens one at a time,
+ * each drawn from the draft distribution given the context and the drafts so
+ * far; by section "Modified rejection sampling" (compatibility with standard
+ * sampling methods) the draw is from the processed draft row p_hat
+ * (temperature, top-k, top-p as in sv_sample_args), the same p_hat the verify
+ * step's accept rule uses.  The draft model's single-row attention and the
+ * append of its row are spec_verify_attn and kv_append_ragged with one block
+ * row per sequence (cu_q = 0..B, num_accepted all 0).
+ *
+ * For sequence i the token drawn from row i sits at index kv_len[i] + 1
+ * (kv_len[i] = the draft cache's length before this position's append): the
+ * inverse CDF of p_hat in vocabulary order (first x whose cumulative weight
+ * exceeds u * Z) with u = word 1 of Philox4x32-10 at counter (kv_len[i] + 1,
+ * seq_ids[i], stream 1) under key seed, so draft draws never reuse a verify
+ * step uniform (stream 0).  A sequence whose row holds NaN or +inf, or only
+ * -inf, or whose per-sequence parameter is invalid gets draft_tokens[i] = -1
+ * with SV_DEV_NONFINITE (plus SV_DEV_BAD_PARAM for a parameter). */
+typedef struct sv_draft_args {
+  int32_t batch;            /* B >= 0 */
+  int32_t vocab;            /* V >= 1 */
+  int32_t dtype;            /* sv_dtype of draft_logits */
+  int32_t top_k;            /* >= 0; 0 disables */
+  float temperature;        /* >= 0; 0 = greedy (first argmax) */
+  float top_p;              /* (0, 1]; >= 1 disables the nucleus */
+  uint64_t seed;            /* Philox key (the verify step's seed) */
+  const void *draft_logits; /* [dev] [B, V] one row per sequence */
+  const int32_t *kv_len;    /* [dev] [B] cache length before this position's append */
+  const int64_t *seq_ids;   /* [dev] [B] Philox sequence ids; NULL -> i */
+  const float *temperatures;/* [dev] [B] per-sequence temperature or NULL */
+  const float *top_ps;      /* [dev] [B] per-sequence top_p or NULL */
+  const int32_t *top_ks;    /* [dev] [B] per-sequence top_k or NULL */
+  int32_t *draft_tokens;    /* [dev] [B] out */
+  uint32_t *dev_status;     /* [dev] one word */
+} sv_draft_args;
+
+/* Workspace bytes of spec_draft_sample (0 if the arguments are invalid).  The
+ * workspace follows the same rule as the others: zeroed once before first use
+ * (sv_workspace_init), left zero by every call that runs to completion. */
+SV_API size_t sv_draft_workspace_bytes(const sv_draft_args *draft);
+
+/* Draws draft_tokens (asynchronous on stream; host-checkable problems return
+ * SV_ERR_* and launch nothing). */
+SV_API sv_status spec_draft_sample(const sv_draft_args *draft, void *ws, size_t ws_bytes,
+                                   void *stream);
+
 /* Thread-local description of the last non-OK status returned on this
  * thread ("" if none). */
 SV_API const char *sv_last_error(void);
@@ -232,8 +279,9 @@ SV_API const char *sv_last_error(void);
 /* SV_ABI_VERSION of the loaded library. */
 SV_API int32_t sv_abi_version(void);
 
-/* sizeof(sv_attn_args) for which = 0, sizeof(sv_sample_args) for which = 1
- * (lets a binding check its struct mirrors). */
+/* sizeof(sv_attn_args) for which = 0, sizeof(sv_sample_args) for which = 1,
+ * sizeof(sv_draft_args) for which = 2 (lets a binding check its struct
+ * mirrors). */
 SV_API size_t sv_struct_size(int32_t which);
 
 #ifdef __cplusplus

@@ -47,6 +47,17 @@ class SampleArgs(ctypes.Structure):
     ]
 
 
+class DraftArgs(ctypes.Structure):
+    """Mirror of sv_draft_args."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("vocab", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("top_k", ctypes.c_int32), ("temperature", ctypes.c_float), ("top_p", ctypes.c_float),
+        ("seed", ctypes.c_uint64), ("draft_logits", _p), ("kv_len", _p), ("seq_ids", _p),
+        ("temperatures", _p), ("top_ps", _p), ("top_ks", _p), ("draft_tokens", _p),
+        ("dev_status", _p),
+    ]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -64,6 +75,10 @@ def _load():
     lib.spec_verify_attn_static.restype = ctypes.c_int
     lib.spec_reject_sample.argtypes = [P(SampleArgs), _p, ctypes.c_size_t, _p]
     lib.spec_reject_sample.restype = ctypes.c_int
+    lib.sv_draft_workspace_bytes.argtypes = [P(DraftArgs)]
+    lib.sv_draft_workspace_bytes.restype = ctypes.c_size_t
+    lib.spec_draft_sample.argtypes = [P(DraftArgs), _p, ctypes.c_size_t, _p]
+    lib.spec_draft_sample.restype = ctypes.c_int
     lib.kv_append_ragged.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64] + [_p] * 5 + \
         [ctypes.c_int64] + [_p] * 7
     lib.kv_append_ragged.restype = ctypes.c_int
@@ -76,7 +91,8 @@ def _load():
     lib.sv_struct_size.argtypes = [ctypes.c_int32]
     lib.sv_struct_size.restype = ctypes.c_size_t
     if lib.sv_struct_size(0) != ctypes.sizeof(AttnArgs) or \
-            lib.sv_struct_size(1) != ctypes.sizeof(SampleArgs):
+            lib.sv_struct_size(1) != ctypes.sizeof(SampleArgs) or \
+            lib.sv_struct_size(2) != ctypes.sizeof(DraftArgs):
         raise ImportError("libspecverify.so struct layout does not match this binding")
     return lib
 

@@ -8,7 +8,7 @@ import ctypes
 
 import torch
 
-from ._binding import (AttnArgs, SampleArgs, SV_BF16, SV_F32, _check, lib)
+from ._binding import (AttnArgs, DraftArgs, SampleArgs, SV_BF16, SV_F32, _check, lib)
 
 
 def _ptr(t):
@@ -95,6 +95,33 @@ def sample_args(target_logits, draft_logits, draft_tokens, cu_q, kv_len, num_acc
     return s
 
 
+def draft_args(draft_logits, kv_len, draft_tokens, *, temperature, top_p, seed, seq_ids=None,
+               dev_status=None, top_k=0, temperatures=None, top_ps=None, top_ks=None):
+    """sv_draft_args for draft_logits [B, V] (one row per sequence), kv_len [B]
+    (cache lengths before this position's append: row i's token sits at index
+    kv_len[i] + 1), output draft_tokens [B] int32; parameters as in
+    sample_args."""
+    d = DraftArgs()
+    B, V = draft_logits.shape
+    d.batch, d.vocab, d.dtype = B, V, _dt(draft_logits)
+    d.top_k = int(top_k)
+    d.temperature, d.top_p = float(temperature), float(top_p)
+    d.seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    d.draft_logits, d.kv_len, d.seq_ids = _ptr(draft_logits), _ptr(kv_len), _ptr(seq_ids)
+    d.temperatures, d.top_ps, d.top_ks = _ptr(temperatures), _ptr(top_ps), _ptr(top_ks)
+    d.draft_tokens, d.dev_status = _ptr(draft_tokens), _ptr(dev_status)
+    d._keep = (draft_logits, kv_len, seq_ids, temperatures, top_ps, top_ks, draft_tokens,
+               dev_status)
+    return d
+
+
+def draft_workspace_bytes(draft):
+    n = lib.sv_draft_workspace_bytes(ctypes.byref(draft))
+    if n == 0:
+        _check(1)
+    return n
+
+
 def workspace_bytes(attn=None, sample=None):
     n = lib.sv_workspace_bytes(ctypes.byref(attn) if attn is not None else None,
                                ctypes.byref(sample) if sample is not None else None)
@@ -133,6 +160,11 @@ def spec_verify_attn_static(attn, stream=None):
 def spec_reject_sample(sample, ws, stream=None):
     _check(lib.spec_reject_sample(ctypes.byref(sample), ctypes.c_void_p(ws.ptr), ws.nbytes,
                                   _stream(stream)))
+
+
+def spec_draft_sample(draft, ws, stream=None):
+    _check(lib.spec_draft_sample(ctypes.byref(draft), ctypes.c_void_p(ws.ptr), ws.nbytes,
+                                 _stream(stream)))
 
 
 def kv_append_ragged(cu_q, k_new, v_new, k_cache, v_cache, kv_start, kv_len, kv_cap,

@@ -179,3 +179,141 @@ class StagedStep:
 
     def result(self, name):
         return self._out[0][name]
+
+
+def _arena(specs):
+    """One device buffer and a pinned host mirror holding tensors of the given
+    (name, shape, torch dtype), each at a 256-byte aligned offset.  Returns
+    (bytes, device buffer, host buffer, device views, host views)."""
+    offs, off = {}, 0
+    for name, shape, dt in specs:
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dt).element_size()
+        offs[name] = (off, n)
+        off += (n + 255) // 256 * 256
+    devb = torch.empty(max(off, 256), dtype=torch.uint8, device="cuda")
+    host = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+    dv, hv = {}, {}
+    for name, shape, dt in specs:
+        o, n = offs[name]
+        dv[name] = devb[o:o + n].view(dt).view(shape)
+        hv[name] = host[o:o + n].view(dt).view(shape)
+    return off, devb, host, dv, hv
+
+
+def _put(t, a):
+    """Copy host array `a` (bf16 as uint16 bits) into tensor `t`."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t.view(torch.int16).copy_(torch.from_numpy(a.view(np.int16)).view(t.shape))
+    else:
+        t.copy_(torch.from_numpy(a).view(t.shape))
+
+
+class DraftBuffers:
+    """Device state for `positions` consecutive draft positions of a batch:
+    the draft model's single-row attention (spec_verify_attn with cu_q =
+    0..B), the append of that row (kv_append_ragged with num_accepted all 0)
+    and the draft-token draw (spec_draft_sample).  `base` is position 0's host
+    input dict (bf16 as uint16 bits); `steps` holds every position's q,
+    k_new, v_new and draft_logits (default: base's for all).
+
+    Per-position inputs (q, k_new, v_new, draft_logits) sit in one device
+    arena and the outputs (out, tokens, the lengths each position writes) in
+    another, each with a pinned host mirror (`upload` / `download` copy them
+    whole).  Position t reads kv_lens[t] and writes kv_lens[t + 1]; kv_lens[0]
+    holds the starting lengths and is never written, so `rewind` restarts the
+    chain and nothing but the library's kernels runs between positions.  The
+    KV pool copies are the live caches the positions append to."""
+
+    def __init__(self, base, api, seed=None, positions=1, steps=None):
+        self.api = api
+        B, P = base["B"], int(positions)
+        self.B, self.positions = B, P
+        steps = steps if steps is not None else [base] * P
+        dt = torch.bfloat16 if base["q"].dtype == np.uint16 else torch.float32
+        Hq, Hkv, D, V = base["num_q_heads"], base["num_kv_heads"], base["head_dim"], base["V"]
+        self.in_bytes, self.dev_in, self.host_in, self.inputs, self.host_inputs = _arena([
+            ("q", (P, B, Hq, D), dt), ("k_new", (P, B, Hkv, D), dt),
+            ("v_new", (P, B, Hkv, D), dt), ("draft_logits", (P, B, V), dt)])
+        self.out_bytes, self.dev_out, self.host_out, self.outputs, self.host_outputs = _arena([
+            ("out", (P, B, Hq, D), dt), ("tokens", (P, B), torch.int32),
+            ("new_len", (P, B), torch.int32)])
+        for t, st in enumerate(steps[:P]):
+            for name in ("q", "k_new", "v_new", "draft_logits"):
+                _put(self.inputs[name][t], st[name])
+        self.outputs["out"].fill_(float("nan"))
+        self.outputs["tokens"].fill_(-7)
+        self.outputs["new_len"].fill_(-7)
+        self.q, self.k_new, self.v_new = (self.inputs[k] for k in ("q", "k_new", "v_new"))
+        self.logits = self.inputs["draft_logits"]
+        self.out, self.tokens = self.outputs["out"], self.outputs["tokens"]
+        self.cu_q = dev(np.arange(B + 1, dtype=np.int32))
+        self.kv_start = dev(base["kv_start"])
+        self.kv_lens = [dev(base["kv_len"])] + [self.outputs["new_len"][t] for t in range(P)]
+        self.kv_cap = dev(base["kv_cap"])
+        self.seq_ids = dev(base["seq_ids"])
+        self.zeros = torch.zeros(B, dtype=torch.int32, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.k_cache, self.v_cache = dev(base["k_cache"]), dev(base["v_cache"])
+        self.per_seq = {k: dev(np.asarray(base[k])) for k in ("temperatures", "top_ps", "top_ks")
+                        if base.get(k) is not None}
+        self.rows_bound = int(np.sum(base["kv_cap"]))      # no length grows past its cap
+        self.attn, self.draft = [], []
+        for t in range(P):
+            kv = self.kv_lens[t]
+            self.attn.append(api.attn_args(
+                self.q[t], self.k_new[t], self.v_new[t], self.k_cache, self.v_cache, self.cu_q,
+                self.kv_start, kv, self.out[t], max_q_rows=1, kv_rows_bound=self.rows_bound,
+                scale=base.get("scale") or 0.0, dev_status=self.status))
+            self.draft.append(api.draft_args(
+                self.logits[t], kv, self.tokens[t], temperature=base["temperature"],
+                top_p=base["top_p"], seed=base["seed"] if seed is None else seed,
+                seq_ids=self.seq_ids, dev_status=self.status, top_k=base.get("top_k", 0),
+                **self.per_seq))
+        self.ws_attn = api.Workspace.for_args(self.attn[0])
+        self.ws_draft = api.Workspace(api.draft_workspace_bytes(self.draft[0]))
+        self.cur = 0
+
+    @property
+    def kv_len(self):
+        """The cache lengths the next position starts from."""
+        return self.kv_lens[self.cur]
+
+    def rewind(self):
+        self.cur = 0
+
+    def stage(self, steps):
+        """Write every position's inputs into the pinned host arena."""
+        for t, st in enumerate(steps[:self.positions]):
+            for name in ("q", "k_new", "v_new", "draft_logits"):
+                _put(self.host_inputs[name][t], st[name])
+
+    def upload(self):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def download(self):
+        self.host_out.copy_(self.dev_out, non_blocking=True)
+
+    def run(self, stream=None):
+        """The next draft position on the current stream: attention, append,
+        draw."""
+        c = self.cur
+        if c >= self.positions:
+            raise IndexError(f"all {self.positions} draft positions have run; rewind first")
+        api = self.api
+        api.spec_verify_attn(self.attn[c], self.ws_attn, stream)
+        api.kv_append_ragged(self.cu_q, self.k_new[c], self.v_new[c], self.k_cache, self.v_cache,
+                             self.kv_start, self.kv_lens[c], self.kv_cap, self.zeros,
+                             self.kv_lens[c + 1], max_q_rows=1, dev_status=self.status,
+                             stream=stream)
+        api.spec_draft_sample(self.draft[c], self.ws_draft, stream)
+        self.cur = c + 1
+
+    def run_all(self, stream=None):
+        """Every position from the starting lengths (one draft-side step)."""
+        self.rewind()
+        for _ in range(self.positions):
+            self.run(stream)
+
+    def status_bits(self):
+        return int(self.status.item()) & 0xFFFFFFFF

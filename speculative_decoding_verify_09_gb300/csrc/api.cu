@@ -111,6 +111,50 @@ sv_status check_sample(const sv_sample_args *a) {
   return SV_OK;
 }
 
+sv_status check_draft(const sv_draft_args *d) {
+  if (!d) return fail(SV_ERR_INVALID, "draft args: null");
+  if (d->batch < 0) return fail(SV_ERR_INVALID, "draft: batch %d", d->batch);
+  if (d->dtype != SV_F32 && d->dtype != SV_BF16)
+    return fail(SV_ERR_INVALID, "draft: dtype %d", d->dtype);
+  if (d->vocab < 1 || d->vocab > sv::sampler_max_vocab(d->dtype))
+    return fail(SV_ERR_UNSUPPORTED, "draft: vocab %d outside [1, %d]", d->vocab,
+                sv::sampler_max_vocab(d->dtype));
+  if (!(d->temperature >= 0.0f) || !std::isfinite(d->temperature))
+    return fail(SV_ERR_INVALID, "draft: temperature must be finite and >= 0 (0 = greedy)");
+  if (d->top_k < 0) return fail(SV_ERR_INVALID, "draft: top_k must be >= 0");
+  if (!(d->top_p > 0.0f) || std::isnan(d->top_p))
+    return fail(SV_ERR_INVALID, "draft: top_p must be > 0");
+  if (d->batch > 0 && (!d->draft_logits || !d->kv_len || !d->draft_tokens))
+    return fail(SV_ERR_INVALID, "draft: null device pointer");
+  return SV_OK;
+}
+
+// A draft draw as a sampling call: one block row per sequence (null cu_q, so
+// the kernels take cu_q[i] = i), the draft logits in the target-row slot, no
+// draft rows; every sequence then takes the bonus draw on its row.
+sv_sample_args draft_as_sample(const sv_draft_args *d) {
+  sv_sample_args s{};
+  s.batch = d->batch;
+  s.vocab = d->vocab;
+  s.dtype = d->dtype;
+  s.max_q_rows = 1;
+  s.num_rows = d->batch;
+  s.temperature = d->temperature;
+  s.top_p = d->top_p;
+  s.seed = d->seed;
+  s.target_logits = d->draft_logits;
+  s.draft_logits = d->draft_logits;   // never read (no draft rows); keeps row pointers non-null
+  s.kv_len = d->kv_len;
+  s.seq_ids = d->seq_ids;
+  s.out_tokens = d->draft_tokens;
+  s.dev_status = d->dev_status;
+  s.top_k = d->top_k;
+  s.temperatures = d->temperatures;
+  s.top_ps = d->top_ps;
+  s.top_ks = d->top_ks;
+  return s;
+}
+
 struct Layout {
   size_t cnt_attn, row_cnt, seq_cnt1, seq_cnt2, stats, parts, draw_parts;
   size_t part_o, part_ml, pre_o, pre_ml, total;
@@ -381,6 +425,34 @@ SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size
   return SV_OK;
 }
 
+SV_API size_t sv_draft_workspace_bytes(const sv_draft_args *draft) {
+  if (check_draft(draft) != SV_OK) return 0;
+  const sv_sample_args s = draft_as_sample(draft);
+  const size_t t = layout(nullptr, &s).total + round_up(static_cast<size_t>(draft->batch) * 4);
+  return t > 0 ? t : kAlign;
+}
+
+SV_API sv_status spec_draft_sample(const sv_draft_args *draft, void *ws, size_t ws_bytes,
+                                   void *stream) {
+  sv_status st = check_draft(draft);
+  if (st != SV_OK) return st;
+  const sv_sample_args s = draft_as_sample(draft);
+  const Layout L = layout(nullptr, &s);
+  const size_t acc = L.total;     // [B] scratch for the (always 0) accepted counts
+  if ((st = check_ws(ws, ws_bytes, acc + round_up(static_cast<size_t>(draft->batch) * 4))) !=
+      SV_OK)
+    return st;
+  if (draft->batch == 0) return SV_OK;
+  sv::SamplerLaunch SL = sampler_launch(&s, L, ws);
+  SL.a.num_accepted = at<int32_t>(ws, acc);
+  SL.do_append = false;
+  SL.pdl_secondary = false;
+  SL.philox_stream = 1;
+  cudaError_t e = sv::launch_sampler(SL, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "draft sampler launch");
+  return SV_OK;
+}
+
 SV_API sv_status kv_append_ragged(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t dtype, int32_t max_q_rows, int64_t num_rows,
                                   const int32_t *cu_q, const void *k_new, const void *v_new,
@@ -464,7 +536,8 @@ SV_API const char *sv_last_error(void) { return g_err.c_str(); }
 SV_API int32_t sv_abi_version(void) { return SV_ABI_VERSION; }
 
 SV_API size_t sv_struct_size(int32_t which) {
-  return which == 0 ? sizeof(sv_attn_args) : which == 1 ? sizeof(sv_sample_args) : 0;
+  return which == 0 ? sizeof(sv_attn_args) : which == 1 ? sizeof(sv_sample_args)
+         : which == 2 ? sizeof(sv_draft_args) : 0;
 }
 
 }  // extern "C"

@@ -66,6 +66,7 @@ struct SamplerLaunch {
   bool do_append;
   AppendView app;
   bool pdl_secondary;       // launched early behind the attention: wait for it at the end
+  uint32_t philox_stream;   // 0: the verify step's uniforms; 1: draft-token draws
 };
 
 SamplerPlan plan_sampler(const sv_sample_args &a);

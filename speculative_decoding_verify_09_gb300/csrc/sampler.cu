@@ -212,6 +212,7 @@ struct SampParams {
   AppendView app;
   float c_hi, c_lo;   // log2(e)/T as two floats
   int pdl_secondary;  // launched early behind another grid (see PdlTail)
+  uint32_t stream;    // Philox counter word 3: 0 verify, 1 draft-token draws
 };
 
 // A launch that may start before the previous grid on its stream has finished
@@ -241,9 +242,15 @@ struct SampSmem {
 
 constexpr size_t kSmemRowOff = (sizeof(SampSmem) + 127) / 128 * 128;
 
+// Block-row offset of sequence i.  A null cu_q means one row per sequence
+// (K_i = 0), the layout of a draft-token draw.
+__device__ __forceinline__ int cuq(const sv_sample_args &a, int i) {
+  return a.cu_q ? a.cu_q[i] : i;
+}
+
 // Validity of sequence i's row bookkeeping against the host bounds.
 __device__ __forceinline__ bool seq_rows_ok(const sv_sample_args &a, int i) {
-  const int r0 = a.cu_q[i], r1 = a.cu_q[i + 1];
+  const int r0 = cuq(a, i), r1 = cuq(a, i + 1);
   const int Ri = r1 - r0;
   return r0 >= i && Ri >= 1 && Ri <= a.max_q_rows && r1 <= a.num_rows &&
          (r1 - (i + 1)) <= a.num_rows - a.batch;
@@ -522,7 +529,7 @@ __device__ void accept_sequence(const SampParams &P, int i) {
   const sv_sample_args &a = P.a;
   const int lane = threadIdx.x & 31;
   const int V = a.vocab, R = static_cast<int>(a.num_rows);
-  const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
+  const int r0 = cuq(a, i), K = cuq(a, i + 1) - r0 - 1, p0 = r0 - i;
   const int L = a.kv_len[i];
   const RowStats *st = P.ws.stats;
   int ok = 1;
@@ -554,7 +561,7 @@ __device__ void accept_sequence(const SampParams &P, int i) {
       const RowProb pp = rowprob_of(&st[R + p0 + lane]);
       const float qh = row_prob<T>(pq, LT<T>::bits(tgt[static_cast<int64_t>(r0 + lane) * V + d]), d);
       const float ph = row_prob<T>(pp, LT<T>::bits(drf[static_cast<int64_t>(p0 + lane) * V + d]), d);
-      const U4 w = philox4x32_10(U4{static_cast<uint32_t>(L + lane + 1), sid_lo, sid_hi, 0u}, k0, k1);
+      const U4 w = philox4x32_10(U4{static_cast<uint32_t>(L + lane + 1), sid_lo, sid_hi, P.stream}, k0, k1);
       const float u = static_cast<float>(u24(w.x)) * 0x1p-24f;          // exact
       rej = !(__fmul_rn(u, ph) < qh);
     }
@@ -574,7 +581,7 @@ template <typename T>
 __device__ __forceinline__ void arrive_sequence(const SampParams &P, int i, int *flag) {
   if (threadIdx.x == 0) {
     __threadfence();
-    const int nrows = 2 * (P.a.cu_q[i + 1] - P.a.cu_q[i]) - 1;
+    const int nrows = 2 * (cuq(P.a, i + 1) - cuq(P.a, i)) - 1;
     const unsigned old = atomicInc(&P.ws.seq_cnt1[i], static_cast<unsigned>(nrows - 1));
     *flag = old == static_cast<unsigned>(nrows - 1) ? 1 : 0;
   }
@@ -591,7 +598,7 @@ __device__ __forceinline__ int row_seq(const sv_sample_args &a, int r, const voi
   if (r < R) {
     row_off = static_cast<int64_t>(r) * a.vocab;
     base = a.target_logits;
-    return seq_of_target_row(a.cu_q, a.batch, r);
+    return a.cu_q ? seq_of_target_row(a.cu_q, a.batch, r) : r;
   }
   row_off = static_cast<int64_t>(r - R) * a.vocab;
   base = a.draft_logits;
@@ -949,7 +956,7 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const int tid = threadIdx.x;
   if (!seq_rows_ok(a, i)) return;                 // flagged in phase 1
   const int V = a.vocab, R = static_cast<int>(a.num_rows);
-  const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
+  const int r0 = cuq(a, i), K = cuq(a, i + 1) - r0 - 1, p0 = r0 - i;
   const int L = a.kv_len[i];
   const int n = a.num_accepted[i];
   if (n < 0 || n > K) {                           // failed sequence: nothing to draw
@@ -1019,7 +1026,7 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
   const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + n + 1),
                                  static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                 static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), P.stream},
                               static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
   const unsigned long long ku = u24(wv.y);
   int use_mode = mode;
@@ -1175,7 +1182,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     return;
   }
   const int V = a.vocab;
-  const int r0 = a.cu_q[i], K = a.cu_q[i + 1] - r0 - 1, p0 = r0 - i;
+  const int r0 = cuq(a, i), K = cuq(a, i + 1) - r0 - 1, p0 = r0 - i;
   const int nrows = 2 * K + 1;
   const int L = a.kv_len[i];
   const T *tgt = static_cast<const T *>(a.target_logits);
@@ -1344,7 +1351,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
       } else {
         const U4 wq = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
                                        static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                       static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), P.stream},
                                     static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
         const float u = static_cast<float>(u24(wq.x)) * 0x1p-24f;     // exact
         rej = !(__fmul_rn(u, sm.pdraft[K + 1 + l]) < sm.pdraft[l]);
@@ -1367,7 +1374,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
     const U4 wv = philox4x32_10(U4{static_cast<uint32_t>(L + l + 1),
                                    static_cast<uint32_t>(static_cast<unsigned long long>(sid)),
-                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), 0u},
+                                   static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32), P.stream},
                                 static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
     sm.draw_u24[l] = u24(wv.y);
   }
@@ -1619,6 +1626,7 @@ cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s) {
   P.c_hi = static_cast<float>(c);
   P.c_lo = static_cast<float>(c - static_cast<double>(P.c_hi));
   P.pdl_secondary = L.pdl_secondary ? 1 : 0;
+  P.stream = L.philox_stream;
   if (2 * L.a.num_rows - L.a.batch <= 0) return cudaSuccess;
   return L.a.dtype == SV_BF16 ? launch_t<uint16_t>(P, s) : launch_t<float>(P, s);
 }

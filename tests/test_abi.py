@@ -44,9 +44,10 @@ def test_exports_exactly_the_declared_symbols(binding):
 
 
 def test_struct_mirrors_and_version(binding):
-    assert binding.lib.sv_abi_version() == 2
+    assert binding.lib.sv_abi_version() == 3
     assert binding.lib.sv_struct_size(0) == ctypes.sizeof(binding.AttnArgs)
     assert binding.lib.sv_struct_size(1) == ctypes.sizeof(binding.SampleArgs)
+    assert binding.lib.sv_struct_size(2) == ctypes.sizeof(binding.DraftArgs)
 
 
 def _attn(b, **kw):
@@ -144,3 +145,34 @@ def test_binding_module_has_no_fallback():
     assert "oracle" not in src and "import numpy" not in src
     for f in glob.glob(os.path.join(ROOT, "speculative_decoding_verify_09_gb300", "*.py")):
         assert "import oracle" not in open(f).read() and "from oracle" not in open(f).read()
+
+
+def _draft(b, **kw):
+    d = b.DraftArgs()
+    d.batch, d.vocab, d.dtype = 4, 1000, b.SV_BF16
+    d.temperature, d.top_p, d.seed = 1.0, 1.0, 0
+    for k in ("draft_logits", "kv_len", "draft_tokens"):
+        setattr(d, k, 4096)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("temperature", -1.0, 1), ("temperature", float("nan"), 1), ("top_p", 0.0, 1),
+    ("top_k", -2, 1), ("vocab", 0, 4), ("vocab", 10 ** 7, 4), ("dtype", 9, 1),
+    ("draft_logits", 0, 1), ("draft_tokens", 0, 1), ("batch", -1, 1),
+])
+def test_draft_host_validation(binding, field, value, status):
+    d = _draft(binding, **{field: value})
+    st = binding.lib.spec_draft_sample(ctypes.byref(d), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == status, binding.last_error()
+    assert binding.lib.sv_draft_workspace_bytes(ctypes.byref(d)) == 0
+
+
+def test_draft_workspace_checks(binding):
+    d = _draft(binding)
+    need = binding.lib.sv_draft_workspace_bytes(ctypes.byref(d))
+    assert need > 0 and need % 256 == 0
+    st = binding.lib.spec_draft_sample(ctypes.byref(d), ctypes.c_void_p(4096), need - 1, None)
+    assert st == binding.SV_ERR_WORKSPACE
