@@ -124,6 +124,9 @@ struct AttnCfg {
   static constexpr int kMergeO = 2 * kRows * kOStride * 4;      // two key-slice sums
   static constexpr int kMergeML = kCW * kRowsW * 8;
   static constexpr int kFinal = kRows * 8;
+  // The final piece's merge keeps every key slice's O rows in the (then idle)
+  // K/V stages: needs kKW row blocks within the smallest ring (2 stages).
+  static constexpr bool kFinalFits = kKW * kRows * kOStride * 4 <= 2 * kStageB;
   static_assert(kMaxBatch * 16 <= 2 * kStageB, "unit tile and cost bases staged in the ring");
 
   static SmemMap map(int ns, int units_cap, int groups_cap, int b_cap) {
@@ -175,6 +178,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Fold one piece of a split segment -- its (max, row sum) v and four O columns
+// ov, relative to that max -- into a running combination (mm, den, acc).  Every
+// merge site folds the pieces in CTA order with this one routine, so the bits
+// do not depend on which piece happens to merge.
+__device__ __forceinline__ void fold_piece(float &mm, float &den, float4 &acc, float2 v,
+                                           float4 ov) {
+  const float mn = fmaxf(mm, v.x);
+  const float mu = mn == -INFINITY ? 0.0f : mn;
+  const float fa = fast_exp2(mm - mu), fb = fast_exp2(v.x - mu);
+  den = den * fa + v.y * fb;
+  acc.x = acc.x * fa + ov.x * fb;
+  acc.y = acc.y * fa + ov.y * fb;
+  acc.z = acc.z * fa + ov.z * fb;
+  acc.w = acc.w * fa + ov.w * fb;
+  mm = mn;
+}
+
 // Wait for the phase of parity `parity` to complete; false after kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (uint32_t it = 0; it < kSpinLimit; ++it)
@@ -561,45 +581,24 @@ __device__ __forceinline__ void attn_merge_jobs(const AttnParams &P, const Ring 
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       __threadfence();
-      // per row, the pieces' (max, sum) folded into one
-      for (int m = lane; m < jb.Mi; m += 32) {
-        float mm = -INFINITY, den = 0.0f;
-#pragma unroll 4
-        for (int c = 0; c < jb.npieces; ++c) {
-          const float2 v = __ldcg(&P.part_ml[(jb.c_first + c + jb.seg) * rows_m + m]);
-          const float mn = fmaxf(mm, v.x);
-          const float mu = mn == -INFINITY ? 0.0f : mn;
-          den = den * fast_exp2(mm - mu) + v.y * fast_exp2(v.x - mu);
-          mm = mn;
-        }
-        mfin[m] = make_float2(mm, den);
-      }
-      __syncwarp();
-      // the weighted sum of the pieces' O rows, four columns at a time
 #pragma unroll 2
       for (int e = lane; e < jb.Mi * (D / 4); e += 32) {
         const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
-        const float mm = mfin[m].x, den = mfin[m].y;
-        const float mu = mm == -INFINITY ? 0.0f : mm;
-        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        float mm = -INFINITY, den = 0.0f;
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
         for (int c = 0; c < jb.npieces; ++c) {
           const int64_t slot2 = jb.c_first + c + jb.seg;
-          const float f = fast_exp2(__ldcg(&P.part_ml[slot2 * rows_m + m].x) - mu);
-          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d));
-          acc.x = fmaf(f, ov.x, acc.x);
-          acc.y = fmaf(f, ov.y, acc.y);
-          acc.z = fmaf(f, ov.z, acc.z);
-          acc.w = fmaf(f, ov.w, acc.w);
+          fold_piece(mm, den, acc, __ldcg(&P.part_ml[slot2 * rows_m + m]),
+                     __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d)));
         }
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
         const int j = m / g, hg = m - j * g;
         uint2 pk;
         pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(jb.r0 + j) * P.Hq + jb.hk * g + hg) * D + d) = pk;
       }
-      __syncwarp();
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(rg.jempty + 8 * js);
@@ -756,6 +755,104 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     if (lane == 0) mbar_arrive(rg.qempty + 8 * (nq & 1));
     ++nq;
   };
+  // Thread 0, a split segment's piece with its partial written: counts the
+  // piece (release at gpu scope, then an increment that wraps to zero); 1 if
+  // it is the last piece to arrive, which then merges every piece.
+  auto settle_final = [&](int npieces, int seg) -> int {
+    __threadfence();
+    const unsigned old = atomicInc(&P.counters[seg], static_cast<unsigned>(npieces - 1));
+    return old == static_cast<unsigned>(npieces - 1) ? 1 : 0;
+  };
+  // The CTA's final piece in plain mode, after its last tile (configurations
+  // whose kKW x kRows O rows fit in two stages).  Once every consumer warp is
+  // past its last tile (warps trail each other by up to NS tiles), every warp's
+  // key-slice state (unnormalized O rows, running max, row sum) goes to the
+  // idle K/V stages and one pass folds the slices: the output of a whole
+  // segment, else this piece's partial, after which the last piece of the
+  // segment to arrive folds every piece in CTA order.
+  auto final_piece = [&]() {
+    constexpr int R = C::kRows;
+    float *fo = reinterpret_cast<float *>(smem);
+    const int Mi = cs.M, seg = cs.seg;
+    const int64_t c_first = cta_of_tile(seg_cost + kSegCost, Wc, G);
+    const int64_t c_last = cta_of_tile(seg_cost + kSegCost + cs.nt - 1, Wc, G);
+    const int npieces = static_cast<int>(c_last - c_first + 1);
+    csync();                          // every warp is past its last tile: the stages are free
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float lv = l_run[nb][e];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        const int m = row_w0 + nb * 8 + 2 * q + e;
+        if (r == 0) merge_ml[ks * R + m] = make_float2(m_run[nb][e], lv);
+        float *dst = fo + (ks * R + m) * OS;
+#pragma unroll
+        for (int dm = 0; dm < DM; ++dm) {
+          dst[dm * 16 + r] = o[dm][nb][e];
+          dst[dm * 16 + r + 8] = o[dm][nb][2 + e];
+        }
+      }
+    csync();
+    const int64_t own = static_cast<int64_t>(blockIdx.x) + seg;   // this piece's partial slot
+    for (int e = tid; e < Mi * (D / 4); e += NC) {
+      const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w2 = 0; w2 < kKW; ++w2) mm = fmaxf(mm, merge_ml[w2 * R + m].x);
+      const float mu = mm == -INFINITY ? 0.0f : mm;
+      float den = 0.0f;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+      for (int w2 = 0; w2 < kKW; ++w2) {
+        const float2 ml = merge_ml[w2 * R + m];
+        const float f = fast_exp2(ml.x - mu);
+        const float4 v = *reinterpret_cast<const float4 *>(fo + (w2 * R + m) * OS + d);
+        den = fmaf(ml.y, f, den);
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
+      }
+      if (npieces > 1) {
+        __stcg(reinterpret_cast<float4 *>(P.part_o + (own * R + m) * D + d), acc);
+        if (d == 0) __stcg(&P.part_ml[own * R + m], make_float2(mm, den));
+        continue;
+      }
+      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+      const int j = m / g, hg = m - j * g;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) = pk;
+    }
+    if (npieces == 1) return;
+    csync();                          // every thread's partial writes
+    if (tid == 0) misc[0] = settle_final(npieces, seg);
+    csync();
+    if (!misc[0]) return;
+    __threadfence();                  // the other pieces' partials, after their publication
+    for (int e = tid; e < Mi * (D / 4); e += NC) {
+      const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
+      float mm = -INFINITY, den = 0.0f;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+      for (int64_t c = c_first; c <= c_last; ++c) {
+        const int64_t slot = c + seg;
+        fold_piece(mm, den, acc, __ldcg(&P.part_ml[slot * R + m]),
+                   __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot * R + m) * D + d)));
+      }
+      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+      const int j = m / g, hg = m - j * g;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2 *>(P.out + (static_cast<int64_t>(cs.r0 + j) * P.Hq + cs.hk * g + hg) * D + d) = pk;
+    }
+  };
+
   ok = begin_segment();
 
   for (int k = 0; k < ntiles && ok; ++k) {
@@ -848,6 +945,12 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       continue;
     }
     end_segment();
+    if constexpr (C::kFinalFits) {
+      if (last && P.mode == 0) {
+        final_piece();
+        break;
+      }
+    }
     // ================= end of a piece: merge the key-slice warps =================
     const int Mi = cs.M;
 #pragma unroll
@@ -939,47 +1042,25 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
         // plain mode, mid-range: the merger warp counts the piece; the last merges
         post_job(MergeJob{seg, npieces, Mi, cs.r0, cs.hk, c_first});
       } else if (npieces > 1 && P.mode == 0) {
-        // the CTA's final piece: the consumer warps (idle from here on) count it
-        // and, if it is the last to arrive, merge with all their threads and every
-        // piece's loads in flight together
+        // the CTA's final piece: the consumer warps (idle from here on) count
+        // it and, if it is the last to arrive, merge with all their threads and
+        // every piece's loads in flight together
         csync();
-        if (tid == 0) {
-          __threadfence();
-          const unsigned old = atomicInc(&P.counters[seg], static_cast<unsigned>(npieces - 1));
-          misc[0] = old == static_cast<unsigned>(npieces - 1) ? 1 : 0;
-        }
+        if (tid == 0) misc[0] = settle_final(npieces, seg);
         csync();
         if (misc[0]) {
           __threadfence();
-          if (tid < Mi) {                  // fin is free: the partial is written
-            float mm = -INFINITY, den = 0.0f;
-#pragma unroll 4
-            for (int c = 0; c < npieces; ++c) {
-              const float2 v = __ldcg(&P.part_ml[(c_first + c + seg) * rows_m + tid]);
-              const float mn = fmaxf(mm, v.x);
-              const float mu = mn == -INFINITY ? 0.0f : mn;
-              den = den * fast_exp2(mm - mu) + v.y * fast_exp2(v.x - mu);
-              mm = mn;
-            }
-            fin[tid] = make_float2(mm, den);
-          }
-          csync();
           for (int e = tid; e < Mi * (D / 4); e += NC) {
             const int m = e / (D / 4), d = (e - m * (D / 4)) * 4;
-            const float mm = fin[m].x, den = fin[m].y;
-            const float mu = mm == -INFINITY ? 0.0f : mm;
-            const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+            float mm = -INFINITY, den = 0.0f;
             float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
             for (int c = 0; c < npieces; ++c) {
               const int64_t slot2 = c_first + c + seg;
-              const float f = fast_exp2(__ldcg(&P.part_ml[slot2 * rows_m + m].x) - mu);
-              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d));
-              acc.x = fmaf(f, ov.x, acc.x);
-              acc.y = fmaf(f, ov.y, acc.y);
-              acc.z = fmaf(f, ov.z, acc.z);
-              acc.w = fmaf(f, ov.w, acc.w);
+              fold_piece(mm, den, acc, __ldcg(&P.part_ml[slot2 * rows_m + m]),
+                         __ldcg(reinterpret_cast<const float4 *>(P.part_o + (slot2 * rows_m + m) * D + d)));
             }
+            const float inv = den > 0.0f ? 1.0f / den : 0.0f;
             const int j = m / g, hg = m - j * g;
             uint2 pk;
             pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
