@@ -144,11 +144,19 @@ def cpu_baseline(inp, budget_s=12.0):
                       f"{el:.1f} s, OMP/BLAS threads 1"}
 
 
+def overrides(args):
+    """Workload overrides from the command line (sampling parameters, K)."""
+    over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
+                              ("top_p", args.top_p)) if v is not None}
+    if args.k is not None:
+        over.update(K_lo=args.k, K_hi=args.k, K_fixed=())
+    return over
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
-    over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
-                              ("top_p", args.top_p)) if v is not None}
+    over = overrides(args)
     w = W.workload(args.workload, **over)
     import oracle
     if args.path == "draft":
@@ -340,6 +348,8 @@ def main():
     ap.add_argument("--temperature", type=float, default=None, help="override (0 = greedy)")
     ap.add_argument("--top-k", type=int, default=None, help="override (0 = off)")
     ap.add_argument("--top-p", type=float, default=None, help="override")
+    ap.add_argument("--k", type=int, default=None,
+                    help="override: every sequence drafts K tokens (K sweep)")
     ap.add_argument("--path", default="verify", choices=["verify", "draft"],
                     help="verify: the fused verify step (default); draft: the draft side "
                          "(K single-row positions per step)")
@@ -368,8 +378,7 @@ def main():
     # weak scaling: rank r owns global sequences [r*B, (r+1)*B) of a batch of
     # world*B sequences (the same shapes on every rank, uniforms keyed by the
     # global sequence id); no exchange on the data path
-    over = {k: v for k, v in (("temperature", args.temperature), ("top_k", args.top_k),
-                              ("top_p", args.top_p)) if v is not None}
+    over = overrides(args)
     w = W.workload(args.workload, **over)
     if args.path == "draft":
         run_draft(args, w, api, shard, dist, world, rank, local_rank)
