@@ -95,7 +95,8 @@ def draft_step(inp, attention=True):
     if attention:
         out = verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
                                inp["v_cache"], inp["cu_q"], inp["kv_start"],
-                               inp["kv_len"], inp["num_kv_heads"], inp.get("scale"), None)
+                               inp["kv_len"], inp["num_kv_heads"], inp.get("scale"), None,
+                               inp.get("k_scale", 1.0), inp.get("v_scale", 1.0))
     s = draft_sample(inp["draft_logits"], inp["kv_len"], inp["temperature"], inp["top_p"],
                      inp["seed"], inp.get("seq_ids"), inp.get("top_k", 0),
                      inp.get("temperatures"), inp.get("top_ps"), inp.get("top_ks"))

@@ -78,11 +78,31 @@ def bf16_bits_to_f64(bits):
     return b.view(np.float32).astype(np.float64)
 
 
+def e4m3_to_f64(codes):
+    """8-bit E4M3 codes (uint8) -> float64, exactly.
+
+    The format (the 8-bit floating point KV caches use; the OCP FP8 "E4M3"
+    layout): sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent
+    0 holds the subnormals m/8 * 2^-6; no infinities, and S.1111.111 is NaN, so
+    the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
 def to_f64(x):
-    """Stored tensor (float32 array, or uint16 bfloat16 bits) -> float64 exactly."""
+    """Stored tensor (float32 array, uint16 bfloat16 bits or uint8 E4M3 codes)
+    -> float64 exactly."""
     x = np.asarray(x)
     if x.dtype == np.uint16:
         return bf16_bits_to_f64(x)
+    if x.dtype == np.uint8:
+        return e4m3_to_f64(x)
     return x.astype(np.float64)
 
 

@@ -30,7 +30,7 @@ def verify_step(inp, attention=True):
         out = verify_attention(inp["q"], inp["k_new"], inp["v_new"], inp["k_cache"],
                                inp["v_cache"], inp["cu_q"], inp["kv_start"],
                                inp["kv_len"], inp["num_kv_heads"], inp.get("scale"),
-                               prefix)
+                               prefix, inp.get("k_scale", 1.0), inp.get("v_scale", 1.0))
     s = reject_sample(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
                       inp["cu_q"], inp["kv_len"], inp["temperature"], inp["top_p"],
                       inp["seed"], inp.get("seq_ids"), inp.get("top_k", 0),

@@ -55,6 +55,8 @@ class Workload:
     prefix_lens: tuple = ()    # per-group prefix lengths (overrides prefix_len)
     cap_slack: int = 0         # extra pool rows per sequence beyond L + K + 1
     gen_seed: int = 0
+    kv_dtype: str = ""         # "" (same as dtype) | "e4m3": 8-bit K/V codes
+    kv_scale: float = 0.0625   # per-tensor K/V scale of an e4m3 cache (code value x scale)
 
 
 # The five workloads (sizes as the pages' setting suggests; see module doc).
@@ -102,6 +104,22 @@ def _normal(rng, shape, std, dtype):
     if std != 1.0:
         x *= np.float32(std)
     return f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+
+def f32_to_e4m3_codes(x):
+    """float32 -> E4M3 codes (uint8), round to nearest even, by torch's
+    float8_e4m3fn conversion (finite inputs within +-448)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _kv(rng, shape, w):
+    """K or V rows: N(0, 1) draws, stored as the workload's K/V type."""
+    if w.kv_dtype == "e4m3":
+        x = rng.standard_normal(size=shape, dtype=np.float32)
+        return f32_to_e4m3_codes(x / np.float32(w.kv_scale))
+    return _normal(rng, shape, 1.0, w.dtype)
 
 
 def _as_f32(x):
@@ -155,10 +173,12 @@ def make_inputs(w, with_attention=True, with_logits=True, guard_rows=8):
                    prefix_len=plen.astype(np.int32))
     if with_attention:
         inp["q"] = _normal(rng, (R, w.Hq, w.D), 1.0, w.dtype)
-        inp["k_new"] = _normal(rng, (R, w.Hkv, w.D), 1.0, w.dtype)
-        inp["v_new"] = _normal(rng, (R, w.Hkv, w.D), 1.0, w.dtype)
-        inp["k_cache"] = _normal(rng, (P, w.Hkv, w.D), 1.0, w.dtype)
-        inp["v_cache"] = _normal(rng, (P, w.Hkv, w.D), 1.0, w.dtype)
+        inp["k_new"] = _kv(rng, (R, w.Hkv, w.D), w)
+        inp["v_new"] = _kv(rng, (R, w.Hkv, w.D), w)
+        inp["k_cache"] = _kv(rng, (P, w.Hkv, w.D), w)
+        inp["v_cache"] = _kv(rng, (P, w.Hkv, w.D), w)
+        if w.kv_dtype == "e4m3":
+            inp.update(kv_dtype="e4m3", k_scale=w.kv_scale, v_scale=w.kv_scale)
     if with_logits:
         tgt = rng.standard_normal(size=(R, w.V), dtype=np.float32) * np.float32(w.logit_std)
         # draft row j of sequence i sits next to target row j of the same sequence
@@ -228,14 +248,15 @@ def step_bytes(inp):
     an upper bound on n_i + 1).
     """
     esz = 4 if inp["dtype"] == "f32" else 2
+    kvsz = 1 if inp.get("kv_dtype") == "e4m3" else esz
     Hq, Hkv, D = inp["num_q_heads"], inp["num_kv_heads"], inp["head_dim"]
     R = int(inp["cu_q"][-1])
     B = inp["B"]
     kv_rows = int(np.sum(inp["kv_len"]))
     if inp.get("group") is not None:
         kv_rows += int(np.sum(inp["prefix_len"]))
-    attn = kv_rows * Hkv * D * esz * 2 + R * (2 * Hq + 2 * Hkv) * D * esz
+    attn = kv_rows * Hkv * D * kvsz * 2 + R * 2 * Hq * D * esz + R * 2 * Hkv * D * kvsz
     logits = (2 * R - B) * inp["V"] * esz
-    append = 2 * R * Hkv * D * esz * 2
+    append = 2 * R * Hkv * D * kvsz * 2
     return dict(attention=attn, sampler=logits, append=append,
                 total=attn + logits + append)
