@@ -43,8 +43,9 @@ FALLBACK_HBM_GBS = 6800.0
 def workload_desc(w):
     K = f"K={w.K_lo}" if w.K_lo == w.K_hi else f"K in [{w.K_lo},{w.K_hi}]"
     pre = f", shared prefix {w.prefix_len}" if w.prefix_len else ""
+    kv = f", K/V {w.kv_dtype} (scale {w.kv_scale})" if w.kv_dtype else ""
     return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, KV len {w.L_dist} "
-            f"[{w.L_lo},{w.L_hi}]{pre}, {K}, V={w.V}, {w.dtype}, T={w.temperature}, "
+            f"[{w.L_lo},{w.L_hi}]{pre}, {K}, V={w.V}, {w.dtype}{kv}, T={w.temperature}, "
             f"top_p={w.top_p}, top_k={w.top_k}")
 
 
@@ -150,6 +151,8 @@ def overrides(args):
                               ("top_p", args.top_p)) if v is not None}
     if args.k is not None:
         over.update(K_lo=args.k, K_hi=args.k, K_fixed=())
+    if args.kv_dtype is not None:
+        over.update(kv_dtype=args.kv_dtype)
     return over
 
 
@@ -348,6 +351,8 @@ def main():
     ap.add_argument("--temperature", type=float, default=None, help="override (0 = greedy)")
     ap.add_argument("--top-k", type=int, default=None, help="override (0 = off)")
     ap.add_argument("--top-p", type=float, default=None, help="override")
+    ap.add_argument("--kv-dtype", default=None, choices=["e4m3"],
+                    help="override: E4M3 K/V (8-bit cache, per-tensor scales)")
     ap.add_argument("--k", type=int, default=None,
                     help="override: every sequence drafts K tokens (K sweep)")
     ap.add_argument("--path", default="verify", choices=["verify", "draft"],
@@ -407,7 +412,8 @@ def main():
     n_acc = sets[0].num_accepted.cpu().numpy()
     emitted = int(np.sum(n_acc + 1))
     esz = 4 if w.dtype == "f32" else 2
-    append_bytes = 2 * 2 * emitted * w.Hkv * w.D * esz        # K and V, read + write
+    kvsz = 1 if w.kv_dtype == "e4m3" else esz
+    append_bytes = 2 * 2 * emitted * w.Hkv * w.D * kvsz       # K and V, read + write
     step_total = nbytes["attention"] + nbytes["sampler"] + append_bytes
 
     def timed(fn, n_launch):

@@ -54,7 +54,7 @@ extern "C" {
 #endif
 
 #define SV_API __attribute__((visibility("default")))
-#define SV_ABI_VERSION 3
+#define SV_ABI_VERSION 4
 
 typedef enum sv_status {
   SV_OK = 0,
@@ -64,7 +64,11 @@ typedef enum sv_status {
   SV_ERR_UNSUPPORTED = 4   /* valid but not built: e.g. head_dim not 64/128 */
 } sv_status;
 
-typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+/* SV_E4M3: 8-bit floating point K/V codes (sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, subnormals at exponent 0, no infinities, S.1111.111 NaN;
+ * the OCP FP8 "E4M3" layout), read as code value times a per-tensor scale.
+ * Only as sv_attn_args.kv_dtype and as the dtype of kv_append_ragged. */
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1, SV_E4M3 = 2 } sv_dtype;
 
 /* Bits OR-ed into *dev_status by the kernels. */
 enum {
@@ -119,6 +123,18 @@ typedef struct sv_attn_args {
   const int32_t *prefix_len;   /* [dev] [G] */
   void *out;                /* [dev] [R, Hq, D] */
   uint32_t *dev_status;     /* [dev] one word */
+  /* Added in ABI 4: an 8-bit KV cache.  The speculative-sampling paper (end
+   * of section "Modified rejection sampling") notes the method composes with
+   * memory-saving techniques such as quantization, since it leaves the
+   * transformer body alone.  kv_dtype SV_E4M3: k_new, v_new, k_cache and
+   * v_cache hold E4M3 codes (one byte per element, same [rows, Hkv, D]
+   * layout; the step's own rows come in the cache's format), read as
+   * code * k_scale and code * v_scale; q and out stay bf16.  Built for dtype
+   * SV_BF16, head_dim 128, no shared prefix and (Hq/Hkv)*max_q_rows <= 16;
+   * other combinations return SV_ERR_UNSUPPORTED. */
+  int32_t kv_dtype;         /* 0 (K/V in dtype) or SV_E4M3 */
+  float k_scale;            /* E4M3 K scale; 0 -> 1 */
+  float v_scale;            /* E4M3 V scale; 0 -> 1 */
 } sv_attn_args;
 
 /* Rejection sampling (a2-a5, a7).  Per sequence: processes its target rows
@@ -202,7 +218,8 @@ SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream)
 SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,
                                     void *stream);
 
-/* Ragged append of accepted rows (a6).  For every sequence with
+/* Ragged append of accepted rows (a6).  dtype SV_F32, SV_BF16 or SV_E4M3
+ * (one byte per element: an 8-bit cache).  For every sequence with
  * num_accepted[i] = n >= 0 and kv_len[i] + n + 1 <= kv_cap[i]: copies block
  * rows cu_q[i] .. cu_q[i] + n of k_new / v_new to pool rows kv_start[i] +
  * kv_len[i] .. + n, and writes new_kv_len[i] = kv_len[i] + n + 1; otherwise

@@ -12,7 +12,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
 
 SV_OK, SV_ERR_INVALID, SV_ERR_WORKSPACE, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = range(5)
-SV_F32, SV_BF16 = 0, 1
+SV_F32, SV_BF16, SV_E4M3 = 0, 1, 2
 DEV_CAPACITY, DEV_BAD_TOKEN, DEV_NONFINITE, DEV_EMPTY_RESIDUAL, DEV_BAD_LENGTH = 1, 2, 4, 8, 16
 DEV_TIMEOUT, DEV_BAD_PARAM = 32, 64
 
@@ -31,6 +31,7 @@ class AttnArgs(ctypes.Structure):
         ("cu_q", _p), ("q", _p), ("k_new", _p), ("v_new", _p), ("k_cache", _p),
         ("v_cache", _p), ("kv_start", _p), ("kv_len", _p), ("group", _p),
         ("prefix_start", _p), ("prefix_len", _p), ("out", _p), ("dev_status", _p),
+        ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
 

@@ -8,7 +8,7 @@ import ctypes
 
 import torch
 
-from ._binding import (AttnArgs, DraftArgs, SampleArgs, SV_BF16, SV_F32, _check, lib)
+from ._binding import (AttnArgs, DraftArgs, SampleArgs, SV_BF16, SV_E4M3, SV_F32, _check, lib)
 
 
 def _ptr(t):
@@ -26,7 +26,9 @@ def _dt(t):
         return SV_BF16
     if t.dtype == torch.float32:
         return SV_F32
-    raise ValueError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+    if t.dtype == torch.uint8:          # E4M3 codes (an 8-bit KV cache)
+        return SV_E4M3
+    raise ValueError(f"unsupported dtype {t.dtype} (bfloat16, float32 or uint8 E4M3 codes)")
 
 
 def _stream(stream):
@@ -36,12 +38,13 @@ def _stream(stream):
 
 def attn_args(q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, *, max_q_rows,
               kv_rows_bound, scale=0.0, dev_status=None, group=None, prefix_start=None,
-              prefix_len=None, prefix_rows_bound=0):
+              prefix_len=None, prefix_rows_bound=0, k_scale=0.0, v_scale=0.0):
     """sv_attn_args for q [R, Hq, D], k_new / v_new [R, Hkv, D], caches
     [P, Hkv, D], cu_q [B+1] int32, kv_start [B] int64, kv_len [B] int32,
     out [R, Hq, D]; max_q_rows / kv_rows_bound are host bounds.  Shared
     prefixes: group [B] int32 (non-decreasing), prefix_start [G] int64,
-    prefix_len [G] int32 and the host bound prefix_rows_bound."""
+    prefix_len [G] int32 and the host bound prefix_rows_bound.  uint8 K/V
+    tensors are E4M3 codes read as code * k_scale / code * v_scale."""
     a = AttnArgs()
     R, Hq, D = q.shape
     a.batch = cu_q.shape[0] - 1
@@ -58,6 +61,8 @@ def attn_args(q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, *,
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
     a.kv_start, a.kv_len, a.out = _ptr(kv_start), _ptr(kv_len), _ptr(out)
     a.dev_status = _ptr(dev_status)
+    a.kv_dtype = SV_E4M3 if k_cache.dtype == torch.uint8 else 0
+    a.k_scale, a.v_scale = float(k_scale), float(v_scale)
     a.group, a.prefix_start, a.prefix_len = _ptr(group), _ptr(prefix_start), _ptr(prefix_len)
     a._keep = (q, k_new, v_new, k_cache, v_cache, cu_q, kv_start, kv_len, out, dev_status,
                group, prefix_start, prefix_len)

@@ -65,7 +65,8 @@ class StepBuffers:
                                       max_q_rows=self.max_q_rows,
                                       kv_rows_bound=int(np.sum(inp["kv_len"])),
                                       scale=inp.get("scale") or 0.0, dev_status=self.status,
-                                      **pre)
+                                      k_scale=inp.get("k_scale", 0.0),
+                                      v_scale=inp.get("v_scale", 0.0), **pre)
         else:
             self.attn = None
         if "target_logits" in inp:
@@ -153,7 +154,8 @@ class StagedStep:
         self.attn = b.attn = api.attn_args(
             b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.cu_q, b.kv_start, b.kv_len, b.out,
             max_q_rows=b.attn.max_q_rows, kv_rows_bound=b.attn.kv_rows_bound,
-            scale=b.attn.scale, dev_status=b.status, **pre)
+            scale=b.attn.scale, dev_status=b.status, k_scale=b.attn.k_scale,
+            v_scale=b.attn.v_scale, **pre)
         s = b.sample
         self.sample = b.sample = api.sample_args(
             b.tgt, b.drf, b.drafts, b.cu_q, b.kv_len, b.num_accepted, b.out_tokens,
@@ -231,10 +233,11 @@ class DraftBuffers:
         self.B, self.positions = B, P
         steps = steps if steps is not None else [base] * P
         dt = torch.bfloat16 if base["q"].dtype == np.uint16 else torch.float32
+        kvdt = torch.uint8 if base["k_new"].dtype == np.uint8 else dt      # E4M3 codes
         Hq, Hkv, D, V = base["num_q_heads"], base["num_kv_heads"], base["head_dim"], base["V"]
         self.in_bytes, self.dev_in, self.host_in, self.inputs, self.host_inputs = _arena([
-            ("q", (P, B, Hq, D), dt), ("k_new", (P, B, Hkv, D), dt),
-            ("v_new", (P, B, Hkv, D), dt), ("draft_logits", (P, B, V), dt)])
+            ("q", (P, B, Hq, D), dt), ("k_new", (P, B, Hkv, D), kvdt),
+            ("v_new", (P, B, Hkv, D), kvdt), ("draft_logits", (P, B, V), dt)])
         self.out_bytes, self.dev_out, self.host_out, self.outputs, self.host_outputs = _arena([
             ("out", (P, B, Hq, D), dt), ("tokens", (P, B), torch.int32),
             ("new_len", (P, B), torch.int32)])
@@ -264,7 +267,8 @@ class DraftBuffers:
             self.attn.append(api.attn_args(
                 self.q[t], self.k_new[t], self.v_new[t], self.k_cache, self.v_cache, self.cu_q,
                 self.kv_start, kv, self.out[t], max_q_rows=1, kv_rows_bound=self.rows_bound,
-                scale=base.get("scale") or 0.0, dev_status=self.status))
+                scale=base.get("scale") or 0.0, dev_status=self.status,
+                k_scale=base.get("k_scale", 0.0), v_scale=base.get("v_scale", 0.0)))
             self.draft.append(api.draft_args(
                 self.logits[t], kv, self.tokens[t], temperature=base["temperature"],
                 top_p=base["top_p"], seed=base["seed"] if seed is None else seed,

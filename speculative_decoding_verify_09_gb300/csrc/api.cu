@@ -63,6 +63,18 @@ sv_status check_attn(const sv_attn_args *a) {
   if (a->num_groups < 0 || a->num_groups > sv::attention_max_groups())
     return fail(SV_ERR_INVALID, "attention: num_groups %d outside [0, %d]", a->num_groups,
                 sv::attention_max_groups());
+  if (a->kv_dtype != 0 && a->kv_dtype != SV_E4M3)
+    return fail(SV_ERR_INVALID, "attention: kv_dtype %d", a->kv_dtype);
+  if (a->kv_dtype == SV_E4M3) {
+    if (a->dtype != SV_BF16 || a->head_dim != 128 || a->num_groups > 0 ||
+        a->max_q_rows * g > 16)
+      return fail(SV_ERR_UNSUPPORTED,
+                  "attention: E4M3 K/V built for bf16 q/out, head_dim 128, no shared prefix, "
+                  "(Hq/Hkv)*max_q_rows <= 16");
+    if (!std::isfinite(a->k_scale) || a->k_scale < 0.0f || !std::isfinite(a->v_scale) ||
+        a->v_scale < 0.0f)
+      return fail(SV_ERR_INVALID, "attention: k_scale / v_scale must be finite and >= 0");
+  }
   if (a->num_groups > 0) {
     if (a->dtype != SV_BF16)
       return fail(SV_ERR_UNSUPPORTED, "attention: shared prefix built for bf16 only");
@@ -461,9 +473,9 @@ SV_API sv_status kv_append_ragged(int32_t batch, int32_t num_kv_heads, int32_t h
                                   const int32_t *kv_cap, const int32_t *num_accepted,
                                   int32_t *new_kv_len, uint32_t *dev_status, void *stream) {
   if (batch < 0) return fail(SV_ERR_INVALID, "append: batch %d", batch);
-  if (num_kv_heads < 1 || head_dim < 1 || (dtype != SV_F32 && dtype != SV_BF16))
+  if (num_kv_heads < 1 || head_dim < 1 || (dtype != SV_F32 && dtype != SV_BF16 && dtype != SV_E4M3))
     return fail(SV_ERR_INVALID, "append: bad shape or dtype");
-  const int esz = dtype == SV_F32 ? 4 : 2;
+  const int esz = dtype == SV_F32 ? 4 : dtype == SV_E4M3 ? 1 : 2;
   const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * esz;
   if (row_bytes % 16 || row_bytes > (1 << 30))
     return fail(SV_ERR_UNSUPPORTED, "append: row bytes %lld not a multiple of 16",
@@ -513,7 +525,7 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   sv::SamplerLaunch SL = sampler_launch(sample, L, ws);
   SL.do_append = true;
   SL.pdl_secondary = true;
-  const int esz = attn->dtype == SV_F32 ? 4 : 2;
+  const int esz = attn->kv_dtype == SV_E4M3 ? 1 : attn->dtype == SV_F32 ? 4 : 2;
   SL.app.k_new = attn->k_new;
   SL.app.v_new = attn->v_new;
   SL.app.k_cache = const_cast<void *>(attn->k_cache);

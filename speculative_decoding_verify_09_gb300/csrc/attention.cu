@@ -78,7 +78,8 @@ struct MergeJob {
 struct AttnParams {
   int B, Hq, Hkv, g, max_q_rows;
   int64_t num_rows, pool_rows;
-  float sl2;                      // scale * log2(e)
+  float sl2;                      // scale * log2(e) (times k_scale for E4M3 K)
+  float v_scale;                  // E4M3 V: output scale (1 otherwise)
   const int32_t *cu_q;
   const uint16_t *q, *k_new, *v_new, *k_cache, *v_cache;
   const int64_t *kv_start;
@@ -109,14 +110,15 @@ __host__ __device__ constexpr int sched_bytes(int units_cap, int groups_cap, int
 // Warps: 4 key slices (16 keys of each 64-key tile) x RS row groups (8*NB
 // packed query rows each), then the producer warp.  Packed row m = j*g + hg
 // for block row j and query head hk*g + hg; a CTA holds up to RS*8*NB rows.
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 struct AttnCfg {
+  static constexpr int kKVB = KV8 ? 1 : 2;                      // bytes per K/V element
   static constexpr int kCW = kKW * RS;                          // consumer warps
   static constexpr int kThreads = (kCW + 2) * 32;               // + producer + merger
   static constexpr int kRowsW = 8 * NB;                         // rows per warp
   static constexpr int kRows = RS * kRowsW;                     // rows per CTA
   static constexpr int kRowB = D * 2 + 16;                      // padded Q row
-  static constexpr int kTileB = kTileKeys * D * 2;              // one K or V tile (swizzled)
+  static constexpr int kTileB = kTileKeys * D * kKVB;           // one K or V tile (swizzled)
   static constexpr int kStageB = 2 * kTileB;
   static constexpr int kQHead = 64;                             // segment header
   static constexpr int kQSlotB = kQHead + kRows * kRowB;
@@ -178,6 +180,24 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void lds_u64(uint32_t addr, uint32_t &a, uint32_t &b) {
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(a), "=r"(b) : "r"(addr));
+}
+
+// Output column of O^T accumulator row r (hi = 0) or r + 8 (hi = 1) of m-tile
+// dm.  With E4M3 V the A operand is built by transposing 8x8 blocks of V rows
+// read four codes at a time, which puts column 16 dm + 4 (r / 2) + r % 2 (+ 2
+// for the second block) on row r.
+template <bool KV8>
+__device__ __forceinline__ int o_col(int dm, int r, int hi) {
+  return KV8 ? dm * 16 + 4 * (r >> 1) + (r & 1) + 2 * hi : dm * 16 + r + 8 * hi;
+}
+
 // Fold one piece of a split segment -- its (max, row sum) v and four O columns
 // ov, relative to that max -- into a running combination (mm, den, acc).  Every
 // merge site folds the pieces in CTA order with this one routine, so the bits
@@ -455,11 +475,11 @@ struct Ring {            // shared-memory addresses of the pipeline
 };
 
 // Producer warp: Q slots and K/V stages for the CTA's tiles [0, ntiles).
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S, Cursor ld,
                                              int ntiles, const Ring &rg, unsigned char *smem,
                                              volatile int *abort_flag) {
-  using C = AttnCfg<D, RS, NB>;
+  using C = AttnCfg<D, RS, NB, KV8>;
   const int lane = threadIdx.x & 31;
   const int NS = P.sm.ns;
   const uint64_t pol = policy_evict_first();
@@ -488,7 +508,47 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
       ++nq;
     }
     if (!mbar_wait(rg.empty + 8 * st, ph ^ 1)) { ok = false; break; }
-    {
+    if constexpr (KV8) {
+      // E4M3 rows of D bytes: lane owns 16-byte chunk lane % 8 of rows lane / 8
+      // + 4 * p; chunk c of row r lands at chunk c ^ (r % 8) (bank spread for
+      // the consumers' 4-byte reads)
+      constexpr int CH = D / 16, RPP = 32 / CH, NPASS = kTileKeys / RPP;
+      const int ch = lane % CH, rr = lane / CH;
+      const uint32_t kdst = rg.base + st * C::kStageB, vdst = kdst + C::kTileB;
+      const int key0 = ld.lt * kTileKeys;
+      const uint8_t *kc = reinterpret_cast<const uint8_t *>(P.k_cache);
+      const uint8_t *vc = reinterpret_cast<const uint8_t *>(P.v_cache);
+      const uint8_t *kn = reinterpret_cast<const uint8_t *>(P.k_new);
+      const uint8_t *vn = reinterpret_cast<const uint8_t *>(P.v_new);
+      if (key0 + kTileKeys <= s.L) {            // whole tile inside the cache
+        const int64_t off = ((s.kv0 + key0 + rr) * P.Hkv + s.hk) * D + ch * 16;
+        const int64_t step = static_cast<int64_t>(RPP) * P.Hkv * D;
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p) {
+          const int row = rr + p * RPP;
+          const uint32_t o = static_cast<uint32_t>(row * D + ((ch ^ (row & 7)) << 4));
+          cp_async16_hint(kdst + o, kc + off + p * step, 16, pol);
+          cp_async16_hint(vdst + o, vc + off + p * step, 16, pol);
+        }
+      } else
+#pragma unroll 4
+      for (int p = 0; p < NPASS; ++p) {
+        const int row = rr + p * RPP, key = key0 + row;
+        const uint32_t o = static_cast<uint32_t>(row * D + ((ch ^ (row & 7)) << 4));
+        if (key < s.L) {                        // cache row (read once: evict first)
+          const int64_t off = ((s.kv0 + key) * P.Hkv + s.hk) * D + ch * 16;
+          cp_async16_hint(kdst + o, kc + off, 16, pol);
+          cp_async16_hint(vdst + o, vc + off, 16, pol);
+        } else {                                // block row, or zeros past the segment
+          const bool blk = key < s.L + s.Ri;
+          const int64_t off =
+              blk ? (static_cast<int64_t>(s.r0 + key - s.L) * P.Hkv + s.hk) * D + ch * 16 : 0;
+          cp_async16(kdst + o, kn + off, blk ? 16 : 0);
+          cp_async16(vdst + o, vn + off, blk ? 16 : 0);
+        }
+      }
+      cp_async_arrive(rg.full + 8 * st);
+    } else {
       // K and V rows of the tile: lane owns chunk lane % CH of rows lane / CH + RPP * p
       constexpr int CH = D / 8;                 // 16-byte chunks per row
       constexpr int RPP = 32 / CH;              // rows per pass of the warp
@@ -554,11 +614,11 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
 // the piece (release of the partial at gpu scope, then an atomic increment
 // that wraps to zero); the last piece to arrive combines all pieces' partials
 // into the output.  Off the consumers' path, so their next segment proceeds.
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 __device__ __forceinline__ void attn_merge_jobs(const AttnParams &P, const Ring &rg,
                                                 MergeJob *jobs, float2 *mfin,
                                                 volatile int *abort_flag) {
-  using C = AttnCfg<D, RS, NB>;
+  using C = AttnCfg<D, RS, NB, KV8>;
   constexpr int rows_m = C::kRows;
   const int lane = threadIdx.x & 31, g = P.g;
   for (int nj = 0;; ++nj) {
@@ -605,9 +665,9 @@ __device__ __forceinline__ void attn_merge_jobs(const AttnParams &P, const Ring 
   }
 }
 
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned char *smem) {
-  using C = AttnCfg<D, RS, NB>;
+  using C = AttnCfg<D, RS, NB, KV8>;
   constexpr int KS = D / 16;          // k-steps of K.Q^T
   constexpr int DM = D / 16;          // m-tiles of V^T.P^T
   constexpr int RW = C::kRowsW;
@@ -690,11 +750,11 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   __syncthreads();
 
   if (warp == C::kCW) {
-    attn_produce<D, RS, NB>(P, S, cur, ntiles, rg, smem, abort_flag);
+    attn_produce<D, RS, NB, KV8>(P, S, cur, ntiles, rg, smem, abort_flag);
     return;
   }
   if (warp == C::kCW + 1) {
-    attn_merge_jobs<D, RS, NB>(P, rg, jobs, mfin, abort_flag);
+    attn_merge_jobs<D, RS, NB, KV8>(P, rg, jobs, mfin, abort_flag);
     return;
   }
 
@@ -731,6 +791,10 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   SeqInfo cs;
   uint32_t qslot = 0;
   bool active = false;
+  // E4M3 K with one 8-row group: the segment's Q fragments (f16, in the
+  // permuted k order of the K operand) are converted once and kept
+  constexpr bool kHoldQ = KV8 && NB == 1;
+  uint32_t qf[kHoldQ ? KS : 1][2];
   auto begin_segment = [&]() -> bool {
     const int slot = nq & 1;
     if (!mbar_wait(rg.qfull + 8 * slot, (nq >> 1) & 1)) return false;
@@ -738,6 +802,16 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
     cs = *reinterpret_cast<const SeqInfo *>(smem + (qslot - rg.base));
     active = row_w0 < cs.M;
     reset_state();
+    if constexpr (kHoldQ) {
+      const uint32_t qrow = qslot + C::kQHead + prow<D>(row_w0 + r, 0) + q * 8;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t q0, q1;
+        lds_u64(qrow + kk * 32, q0, q1);
+        qf[kk][0] = bf16x2_to_f16x2(q0);
+        qf[kk][1] = bf16x2_to_f16x2(q1);
+      }
+    }
     return true;
   };
   int njob = 0;
@@ -791,8 +865,8 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
         float *dst = fo + (ks * R + m) * OS;
 #pragma unroll
         for (int dm = 0; dm < DM; ++dm) {
-          dst[dm * 16 + r] = o[dm][nb][e];
-          dst[dm * 16 + r + 8] = o[dm][nb][2 + e];
+          dst[o_col<KV8>(dm, r, 0)] = o[dm][nb][e] * P.v_scale;
+          dst[o_col<KV8>(dm, r, 1)] = o[dm][nb][2 + e] * P.v_scale;
         }
       }
     csync();
@@ -865,7 +939,33 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
       float sacc[NB][4];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.0f;
-      {
+      if constexpr (KV8) {
+        // E4M3 K: lane (r, q) reads codes 16 kk + 4q .. +3 of keys r and r + 8
+        // of its slice; the head dimension is permuted inside each k-step (the
+        // A operand's column pairs 2q, 2q+8 hold d 4q, 4q+2) and Q's B operand
+        // is read with the same permutation, so the dot products are unchanged
+        const int kr0 = ks * 16 + r, kr1 = kr0 + 8;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t w0 = lds_u32(kbase + kr0 * D + ((kk ^ (kr0 & 7)) << 4) + 4 * q);
+          const uint32_t w1 = lds_u32(kbase + kr1 * D + ((kk ^ (kr1 & 7)) << 4) + 4 * q);
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(w0);
+          a[1] = e4m3x2_to_f16x2(w1);
+          a[2] = e4m3x2_to_f16x2(w0 >> 16);
+          a[3] = e4m3x2_to_f16x2(w1 >> 16);
+          if constexpr (kHoldQ) {
+            mma_f16_16816(sacc[0], a, qf[kk][0], qf[kk][1]);
+          } else {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              uint32_t q0, q1;
+              lds_u64(qrows + prow<D>(row_w0 + nb * 8 + r, 0) + kk * 32 + q * 8, q0, q1);
+              mma_f16_16816(sacc[nb], a, bf16x2_to_f16x2(q0), bf16x2_to_f16x2(q1));
+            }
+          }
+        }
+      } else {
         const int krow = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
         for (int kk = 0; kk < KS; kk += 2) {
@@ -919,11 +1019,33 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
             }
           }
         }
-        pb[nb][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));   // keys 0-7 of the slice
-        pb[nb][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));   // keys 8-15
+        if constexpr (KV8) {
+          pb[nb][0] = movmatrix_trans(pack_f16x2(pv[0], pv[1]));
+          pb[nb][1] = movmatrix_trans(pack_f16x2(pv[2], pv[3]));
+        } else {
+          pb[nb][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));   // keys 0-7 of the slice
+          pb[nb][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));   // keys 8-15
+        }
       }
       // ---- O^T += V^T P^T
-      {
+      if constexpr (KV8) {
+        // E4M3 V: lane (r, q) reads codes 16 dm + 4q .. +3 of keys r and r + 8;
+        // each f16 pair is one lane's share of an 8x8 (key, d) block whose
+        // transpose is the A operand's (d, key) fragment (rows: see o_col)
+        const int vr0 = ks * 16 + r, vr1 = vr0 + 8;
+#pragma unroll
+        for (int dm = 0; dm < DM; ++dm) {
+          const uint32_t w0 = lds_u32(vbase + vr0 * D + ((dm ^ (vr0 & 7)) << 4) + 4 * q);
+          const uint32_t w1 = lds_u32(vbase + vr1 * D + ((dm ^ (vr1 & 7)) << 4) + 4 * q);
+          uint32_t a[4];
+          a[0] = movmatrix_trans(e4m3x2_to_f16x2(w0));
+          a[1] = movmatrix_trans(e4m3x2_to_f16x2(w0 >> 16));
+          a[2] = movmatrix_trans(e4m3x2_to_f16x2(w1));
+          a[3] = movmatrix_trans(e4m3x2_to_f16x2(w1 >> 16));
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16_16816(o[dm][nb], a, pb[nb][0], pb[nb][1]);
+        }
+      } else {
         const int vrow = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int dm = 0; dm < DM; ++dm) {
@@ -991,18 +1113,18 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
           for (int e = 0; e < 2; ++e) {
             const int m = row_w0 + nb * 8 + 2 * q + e;
             const float mm = fin[m].x;
-            const float sc = fast_exp2(m_run[nb][e] - (mm == -INFINITY ? 0.0f : mm));
+            const float sc = fast_exp2(m_run[nb][e] - (mm == -INFINITY ? 0.0f : mm)) * P.v_scale;
             float *dst = merge_o + (ks >> 1) * C::kRows * OS + m * OS;
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm) {
-              const int d0 = dm * 16 + r;
+              const int d0 = o_col<KV8>(dm, r, 0), d1 = o_col<KV8>(dm, r, 1);
               const float a0 = o[dm][nb][e] * sc, a1 = o[dm][nb][2 + e] * sc;
               if (step == 0) {
                 dst[d0] = a0;
-                dst[d0 + 8] = a1;
+                dst[d1] = a1;
               } else {
                 dst[d0] += a0;
-                dst[d0 + 8] += a1;
+                dst[d1] += a1;
               }
             }
           }
@@ -1083,12 +1205,12 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   post_job(MergeJob{-1, 0, 0, 0, 0, 0});
 }
 
-template <int D, int RS, int NB>
-__global__ void __launch_bounds__(AttnCfg<D, RS, NB>::kThreads)
+template <int D, int RS, int NB, bool KV8>
+__global__ void __launch_bounds__(AttnCfg<D, RS, NB, KV8>::kThreads)
     attn_bf16_kernel(const AttnParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  attn_bf16_body<D, RS, NB>(P, smem);
+  attn_bf16_body<D, RS, NB, KV8>(P, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -1294,33 +1416,33 @@ __global__ void __launch_bounds__(kF32NT) attn_f32_kernel(const AttnParams P, co
 }
 
 
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 SmemMap smem_map_for(const AttnParams &P, int ns) {
-  using C = AttnCfg<D, RS, NB>;
+  using C = AttnCfg<D, RS, NB, KV8>;
   return P.mode == 2 ? C::map(ns, P.G, P.G, P.B) : C::map(ns, P.B, 1, P.B);
 }
 
 // Ring stages for a launch: as many as fit in smem_cap (2..kMaxStages).
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 int stages_for(const AttnParams &P, int smem_cap) {
   int ns = kMaxStages;
-  while (ns > 2 && smem_map_for<D, RS, NB>(P, ns).total > smem_cap) --ns;
+  while (ns > 2 && smem_map_for<D, RS, NB, KV8>(P, ns).total > smem_cap) --ns;
   return ns;
 }
 
-template <int D, int RS, int NB>
+template <int D, int RS, int NB, bool KV8>
 cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int *grid_used,
                         cudaStream_t s) {
-  using C = AttnCfg<D, RS, NB>;
+  using C = AttnCfg<D, RS, NB, KV8>;
   AttnLaunchOpts opt = o;
   // a budget that leaves room for another kernel's CTA must still hold 2 stages
-  if (opt.smem_min > 0 && smem_map_for<D, RS, NB>(P, 2).total > opt.smem_cap) {
+  if (opt.smem_min > 0 && smem_map_for<D, RS, NB, KV8>(P, 2).total > opt.smem_cap) {
     opt.smem_cap = kSmemMax;
     opt.smem_min = 0;
   }
-  P.sm = smem_map_for<D, RS, NB>(P, stages_for<D, RS, NB>(P, opt.smem_cap));
+  P.sm = smem_map_for<D, RS, NB, KV8>(P, stages_for<D, RS, NB, KV8>(P, opt.smem_cap));
   const int bytes = std::max(P.sm.total, opt.smem_min);
-  auto kern = attn_bf16_kernel<D, RS, NB>;
+  auto kern = attn_bf16_kernel<D, RS, NB, KV8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   if (e != cudaSuccess) return e;
   // all of the SM's unified L1 as shared memory (the loads bypass L1): an SM
@@ -1352,12 +1474,19 @@ template <int D>
 cudaError_t launch_d(const AttnParams &P, const AttnLaunchOpts &o, int rc, int max_grid, int *grid,
                      cudaStream_t s) {
   switch (rc) {
-    case 0: return launch_bf16<D, 1, 1>(P, o, max_grid, grid, s);
-    case 1: return launch_bf16<D, 1, 2>(P, o, max_grid, grid, s);
-    case 2: return launch_bf16<D, 2, 2>(P, o, max_grid, grid, s);
-    case 3: return launch_bf16<D, 3, 2>(P, o, max_grid, grid, s);
-    default: return launch_bf16<D, 4, 2>(P, o, max_grid, grid, s);
+    case 0: return launch_bf16<D, 1, 1, false>(P, o, max_grid, grid, s);
+    case 1: return launch_bf16<D, 1, 2, false>(P, o, max_grid, grid, s);
+    case 2: return launch_bf16<D, 2, 2, false>(P, o, max_grid, grid, s);
+    case 3: return launch_bf16<D, 3, 2, false>(P, o, max_grid, grid, s);
+    default: return launch_bf16<D, 4, 2, false>(P, o, max_grid, grid, s);
   }
+}
+
+// E4M3 K/V: D = 128 and one row group (up to 16 packed rows).
+cudaError_t launch_e4m3(const AttnParams &P, const AttnLaunchOpts &o, int rc, int max_grid,
+                        int *grid, cudaStream_t s) {
+  return rc == 0 ? launch_bf16<128, 1, 1, true>(P, o, max_grid, grid, s)
+                 : launch_bf16<128, 1, 2, true>(P, o, max_grid, grid, s);
 }
 
 }  // namespace
@@ -1409,6 +1538,12 @@ cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const Att
   P.pool_rows = a.pool_rows;
   const float scale = a.scale != 0.0f ? a.scale : 1.0f / sqrtf(static_cast<float>(a.head_dim));
   P.sl2 = scale * kLog2e;
+  P.v_scale = 1.0f;
+  const bool kv8 = a.kv_dtype == SV_E4M3;
+  if (kv8) {                      // code * k_scale in the scores, code * v_scale in the output
+    P.sl2 *= a.k_scale != 0.0f ? a.k_scale : 1.0f;
+    P.v_scale = a.v_scale != 0.0f ? a.v_scale : 1.0f;
+  }
   P.cu_q = a.cu_q;
   P.q = static_cast<const uint16_t *>(a.q);
   P.k_new = static_cast<const uint16_t *>(a.k_new);
@@ -1452,6 +1587,10 @@ cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const Att
   }
   const bool d64 = a.head_dim == 64;
   int grid = 0, pgrid = 0;
+  if (kv8) {                      // head_dim 128, one row group, no prefix (checked on the host)
+    P.pdl_primary = opts.pdl_primary ? 1 : 0;
+    return launch_e4m3(P, opts, p.row_cfg, static_cast<int>(p.grid), &grid, s);
+  }
   if (!p.prefix) {
     P.pdl_primary = opts.pdl_primary ? 1 : 0;
     const int mg = static_cast<int>(p.grid);

@@ -44,7 +44,7 @@ def test_exports_exactly_the_declared_symbols(binding):
 
 
 def test_struct_mirrors_and_version(binding):
-    assert binding.lib.sv_abi_version() == 3
+    assert binding.lib.sv_abi_version() == 4
     assert binding.lib.sv_struct_size(0) == ctypes.sizeof(binding.AttnArgs)
     assert binding.lib.sv_struct_size(1) == ctypes.sizeof(binding.SampleArgs)
     assert binding.lib.sv_struct_size(2) == ctypes.sizeof(binding.DraftArgs)
@@ -176,3 +176,23 @@ def test_draft_workspace_checks(binding):
     assert need > 0 and need % 256 == 0
     st = binding.lib.spec_draft_sample(ctypes.byref(d), ctypes.c_void_p(4096), need - 1, None)
     assert st == binding.SV_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kv_dtype=2, head_dim=64), 4),                  # E4M3 built for head_dim 128
+    (dict(kv_dtype=2, dtype=0), 4),                      # E4M3 K/V with fp32 q/out
+    (dict(kv_dtype=2, num_q_heads=16, num_kv_heads=2), 4),   # 8 x 5 rows > 16
+    (dict(kv_dtype=2, num_groups=1, group=4096, prefix_start=4096, prefix_len=4096), 4),
+    (dict(kv_dtype=2, num_q_heads=4, k_scale=float("nan")), 1),
+    (dict(kv_dtype=2, num_q_heads=4, v_scale=-1.0), 1),
+    (dict(kv_dtype=7), 1),
+])
+def test_e4m3_attention_host_validation(binding, kw, status):
+    a = _attn(binding, **kw)
+    st = binding.lib.spec_verify_attn(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert st == status, binding.last_error()
+
+
+def test_e4m3_attention_accepted_shapes_size_a_workspace(binding):
+    a = _attn(binding, kv_dtype=2, num_q_heads=4, num_kv_heads=2, k_scale=0.5, v_scale=0.25)
+    assert binding.lib.sv_workspace_bytes(ctypes.byref(a), None) > 0
