@@ -458,7 +458,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
     sha = src_sha()
-    traffic = traffic_record(sha, args.workload)
+    traffic = traffic_record(sha, args.workload + ("_e4m3" if w.kv_dtype == "e4m3" else ""))
 
     # end to end through the C ABI: every step copies its inputs (one pinned
     # host arena -> one device arena), runs the fused call and copies its
