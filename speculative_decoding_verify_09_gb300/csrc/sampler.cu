@@ -101,7 +101,6 @@ __device__ __forceinline__ void load_bits(const T *row, int V, int v, bool align
 
 constexpr int kRowSmemBytes = 64 * 1024;  // a row up to this size is cached in smem
 constexpr int kStream = 4;                 // vectors per thread loaded together when streaming
-constexpr int kDrawBatch = 4;              // vectors per thread loaded together by the draw
 
 // A logits row as seen by one CTA: vector v = k * kSampNT + tid for k = 0..
 // A row of at most kRowSmemBytes is copied once from HBM into shared memory
@@ -277,15 +276,15 @@ __device__ __forceinline__ int seq_of_draft_row(const int32_t *cu_q, int B, int 
 // --------------------------------------------------------------------------
 // Nucleus cut: the largest key tau such that the weight of {key >= tau} is at
 // least top_p * S (ties kept together).  Coarse pass over weight-exponent bins
-// picks a candidate set that surely contains the cut; the exact bitwise search
-// then runs over those candidates in shared memory (or, if there are too
-// many, over the whole row).
+// finds the bin holding the cut; the exact bitwise search then runs over that
+// bin's elements in shared memory, with the heavier bins' mass added (or, if
+// the bin has too many elements, over the whole row).
 // --------------------------------------------------------------------------
 template <typename T>
 __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf0, uint32_t kmin, double S,
                             float top_p, SampSmem &sm, uint32_t &tau_out, double &ssum_out) {
   constexpr int EPV = LT<T>::EPV;
-  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const int tid = threadIdx.x;
   const double target = static_cast<double>(top_p) * S;
   // weights of the elements kept by top-k (keys below kmin weigh 0)
   struct Masked {
@@ -314,19 +313,35 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf0, uint32_t 
 #pragma unroll
   for (int k = 0; k < 8; ++k) bins[k] = ff_make(acc[k]);
   block_sum_ff<8>(bins, sm.red[0]);
+  // Candidates: bins klo..kb around the cut, where klo is the first bin whose
+  // cumulative mass reaches top_p * S * (1 - 1e-5) and kb the first reaching
+  // (1 + 1e-5) (the float bin sums are far more accurate than that), so the
+  // heavier bins' mass `heavy` is surely below the target and bins up to kb
+  // surely reach it.  A heavier bin holds larger weights, hence larger logits
+  // and keys, than every candidate, so for a probe key inside the candidates'
+  // range the mass at or above it is heavy plus the candidates' at or above
+  // it; for probes above that range heavy alone stays below the target, and
+  // for probes below it heavy plus every candidate reaches it: the exact
+  // search takes the same decisions as over the whole row.
   const FF tgt_safe = ff_from_double(target * (1.0 + 1e-5));
-  FF cum = ff_make(0.0f);
-  int kb = 7;
+  const FF tgt_low = ff_from_double(target * (1.0 - 1e-5));
+  FF cum = ff_make(0.0f), heavy = ff_make(0.0f);
+  int kb = 7, klo = 7;
 #pragma unroll
   for (int k = 0; k < 7; ++k) {
-    cum = ff_add(cum, bins[k]);
-    if (kb == 7 && ff_ge(cum, tgt_safe)) kb = k;
+    const FF next = ff_add(cum, bins[k]);
+    if (klo == 7 && ff_ge(next, tgt_low)) {
+      klo = k;
+      heavy = cum;
+    }
+    if (kb == 7 && ff_ge(next, tgt_safe)) kb = k;
+    cum = next;
   }
-  // candidates: bin <= kb (every element when kb == 7)
+  if (klo == 7) heavy = cum;          // the cut lies in the tail bin
   auto is_cand = [&](float x) {
-    if (kb == 7) return true;
     const int ex = 127 - static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);
-    return (max(ex, 0) >> 2) <= kb;
+    const int b = min(max(ex, 0) >> 2, 7);
+    return b >= klo && b <= kb;
   };
   int mine = 0;
   rp.each([&](const uint32_t (&bits)[EPV]) {
@@ -376,11 +391,13 @@ __device__ void nucleus_cut(const RowPass<T> &rp, const WeightFn &wf0, uint32_t 
     const uint32_t cand = tau | (1u << bit);
     FF W[1] = {ff_make(partial(cand))};
     block_sum_ff<1>(W, sm.red[buf]);
+    if (in_smem) W[0] = ff_add(W[0], heavy);
     if (ff_ge(W[0], tgt)) tau = cand;
     buf ^= 1;
   }
   FF ss[1] = {ff_make(partial(tau))};
   block_sum_ff<1>(ss, sm.red[buf]);
+  if (in_smem) ss[0] = ff_add(ss[0], heavy);
   ssum_out = ff_to_double(ss[0]);
   tau_out = tau;
 }
