@@ -197,6 +197,53 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def timed_replays(torch, sets, fn, n_launch, stream, dist, shard, no_graph, percentiles):
+    """Time n_launch calls of fn over the rotating input sets with CUDA events on
+    the launching stream (one CUDA graph holding one call per set, unless
+    no_graph); the barrier and max over ranks make it the job's time.  Returns
+    (ms, calls, pct): pct (with percentiles) holds p10 / p50 / p90 of the time
+    per call over 200 single graph replays, each bracketed by its own events."""
+    graph = None
+    if not no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for d in sets:
+                fn(d)
+        torch.cuda.synchronize()
+    reps = max(1, n_launch // len(sets))
+    for _ in range(2):
+        graph.replay() if graph else [fn(d) for d in sets]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        if graph:
+            graph.replay()
+        else:
+            for d in sets:
+                fn(d)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = shard.max_over_ranks(ev0.elapsed_time(ev1), dist, device="cuda")
+    pct = None
+    if percentiles and graph is not None:
+        n = 200
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+        for i in range(n):
+            evs[2 * i].record(stream)
+            graph.replay()
+            evs[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = np.array([evs[2 * i].elapsed_time(evs[2 * i + 1]) * 1e3 / len(sets)
+                        for i in range(n)])
+        pct = {"p10": float(np.percentile(per, 10)), "p50": float(np.percentile(per, 50)),
+               "p90": float(np.percentile(per, 90)), "unit": "us per call",
+               "replays": n, "calls_per_replay": len(sets)}
+    return ms, reps * len(sets), pct
+
+
 DRAFT_METRIC = ("draft-side steps/s (K positions of single-row attention + append + draft "
                 "draw) at B=8 7.8B-shape; achieved HBM GB/s vs peak")
 
@@ -235,31 +282,9 @@ def run_draft(args, w, api, shard, dist, world, rank, local_rank):
     esz = 4 if w.dtype == "f32" else 2
     attn_bytes = per_pos - w.B * w.V * esz - 2 * w.B * 2 * w.Hkv * w.D * esz
 
-    def timed(fn, n_launch):
-        graph = None
-        if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for d in sets:
-                    fn(d)
-            torch.cuda.synchronize()
-        reps = max(1, n_launch // len(sets))
-        for _ in range(2):
-            graph.replay() if graph else [fn(d) for d in sets]
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            if graph:
-                graph.replay()
-            else:
-                for d in sets:
-                    fn(d)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        return shard.max_over_ranks(ev0.elapsed_time(ev1), dist, device="cuda"), reps * len(sets)
+    def timed(fn, n_launch, percentiles=False):
+        return timed_replays(torch, sets, fn, n_launch, stream, dist, shard, args.no_graph,
+                             percentiles)
 
     for k in range(max(args.warmup, 3)):
         sets[k % len(sets)].run_all()
@@ -268,13 +293,13 @@ def run_draft(args, w, api, shard, dist, world, rank, local_rank):
         if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
     clk = Clocks(gpu_index)
     time.sleep(0.3)
-    ms_step, n_steps = timed(lambda d: d.run_all(), args.steps)
+    ms_step, n_steps, pct = timed(lambda d: d.run_all(), args.steps, percentiles=True)
     clocks = clk.stop()
 
     def attn0(d):
         api.spec_verify_attn(d.attn[0], d.ws_attn)
 
-    ms_attn, n_attn = timed(attn0, args.attn_steps)
+    ms_attn, n_attn, _ = timed(attn0, args.attn_steps)
     attn_us = 1e3 * ms_attn / n_attn
     peak, peak_kind = peaks()
     achieved = attn_bytes / (attn_us * 1e-6) / 1e9
@@ -318,6 +343,7 @@ def run_draft(args, w, api, shard, dist, world, rank, local_rank):
                        "launch": "CUDA graph of the C-ABI calls per input set"
                        if not args.no_graph else "direct launches"},
             "draft_tok_s": world * w.B * P * n_steps / (ms_step / 1e3),
+            "step_time_percentiles": pct,
             "step_bytes": step_total,
             "step_hbm_gbs": step_total / (per_step_ms * 1e-3) / 1e9,
             "step_frac_of_peak": step_total / (per_step_ms * 1e-3) / 1e9 / peak,
@@ -416,40 +442,17 @@ def main():
     append_bytes = 2 * 2 * emitted * w.Hkv * w.D * kvsz       # K and V, read + write
     step_total = nbytes["attention"] + nbytes["sampler"] + append_bytes
 
-    def timed(fn, n_launch):
-        graph = None
-        if not args.no_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for d in sets:
-                    fn(d)
-            torch.cuda.synchronize()
-        reps = max(1, n_launch // len(sets))
-        for _ in range(2):
-            graph.replay() if graph else [fn(d) for d in sets]
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            if graph:
-                graph.replay()
-            else:
-                for d in sets:
-                    fn(d)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        ms = shard.max_over_ranks(ev0.elapsed_time(ev1), dist, device="cuda")
-        return ms, reps * len(sets)
+    def timed(fn, n_launch, percentiles=False):
+        return timed_replays(torch, sets, fn, n_launch, stream, dist, shard, args.no_graph,
+                             percentiles)
 
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local_rank)
     clk = Clocks(gpu_index)
     time.sleep(0.3)
-    ms_step, n_steps = timed(step, args.steps)
+    ms_step, n_steps, pct = timed(step, args.steps, percentiles=True)
     clocks = clk.stop()
-    ms_attn, n_attn = timed(attn_only, args.attn_steps)
+    ms_attn, n_attn, _ = timed(attn_only, args.attn_steps)
 
     emitted_all = int(shard.sum_over_ranks(emitted, dist, device="cuda"))
     per_step_ms = ms_step / n_steps
@@ -499,6 +502,7 @@ def main():
                        "launch": "CUDA graph of the C-ABI call per input set" if not args.no_graph
                        else "direct launches"},
             "accepted_tok_s": emitted_all * n_steps / (ms_step / 1e3),
+            "step_time_percentiles": pct,
             "mean_accepted_per_seq": float(np.mean(n_acc)),
             "step_bytes": step_total,
             "step_hbm_gbs": step_total / (per_step_ms * 1e-3) / 1e9,
