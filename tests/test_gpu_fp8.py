@@ -150,3 +150,28 @@ def test_e4m3_append_alone(api):
                                      na.cpu().numpy())
     assert np.array_equal(d.new_kv_len.cpu().numpy(), nl)
     assert np.array_equal(host_bits(d.k_cache), k2) and np.array_equal(host_bits(d.v_cache), v2)
+
+
+def test_e4m3_draft_positions(api):
+    """Three draft positions (single-row attention, append of the row, draft
+    draw) over an E4M3 cache against the oracle's draft_step with the scales."""
+    from speculative_decoding_verify_09_gb300.buffers import DraftBuffers
+    w = W.workload("bass_b8", B=6, L_lo=100, L_hi=900, kv_dtype="e4m3", gen_seed=91)
+    base, steps = W.make_draft_inputs(w, positions=3)
+    assert all(st["k_new"].dtype == np.uint8 for st in steps)
+    d = DraftBuffers(base, api, positions=3, steps=steps)
+    inp = dict(base)
+    for t, st in enumerate(steps):
+        inp.update(st)
+        d.run()
+        torch.cuda.synchronize()
+        ref = oracle.draft_step(inp)
+        err = float(np.max(np.abs(d.out[t].float().cpu().numpy() - ref["out"])))
+        assert err < TOL, err
+        got = d.tokens[t].cpu().numpy()
+        for i in range(w.B):
+            if not ref["tie"][i]:
+                assert int(got[i]) == int(ref["tokens"][i])
+        assert np.array_equal(host_bits(d.k_cache), ref["k_cache"])
+        assert list(d.kv_len.cpu().numpy()) == list(ref["new_kv_len"])
+        inp.update(k_cache=ref["k_cache"], v_cache=ref["v_cache"], kv_len=ref["new_kv_len"])

@@ -220,8 +220,8 @@ def make_draft_inputs(w, positions=1):
     for t in range(1, positions):
         rng = np.random.Generator(np.random.PCG64([w.gen_seed, t]))
         st = {"q": _normal(rng, (w.B, w.Hq, w.D), 1.0, w.dtype),
-              "k_new": _normal(rng, (w.B, w.Hkv, w.D), 1.0, w.dtype),
-              "v_new": _normal(rng, (w.B, w.Hkv, w.D), 1.0, w.dtype)}
+              "k_new": _kv(rng, (w.B, w.Hkv, w.D), w),
+              "v_new": _kv(rng, (w.B, w.Hkv, w.D), w)}
         lg = rng.standard_normal(size=(w.B, w.V), dtype=np.float32) * np.float32(w.logit_std)
         st["draft_logits"] = f32_to_bf16_bits(lg) if w.dtype == "bf16" else lg
         steps.append(st)
