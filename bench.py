@@ -49,6 +49,12 @@ def workload_desc(w):
             f"top_p={w.top_p}, top_k={w.top_k}")
 
 
+def compute_dtype(w):
+    """What the path computes in: bf16 / fp32 operands, or E4M3 K/V codes
+    widened to f16 tensor-core operands (fp32 accumulation throughout)."""
+    return "e4m3 K/V -> f16 mma, bf16 q/out" if w.kv_dtype == "e4m3" else w.dtype
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -332,7 +338,7 @@ def run_draft(args, w, api, shard, dist, world, rank, local_rank):
             "metric": DRAFT_METRIC, "value": world * n_steps / (ms_step / 1e3), "unit": UNIT,
             "n_gpus": world, "steps": n_steps, "warmup": max(args.warmup, 3),
             "ms_per_step": per_step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype,
+            "vs_baseline": None, "dtype": compute_dtype(w),
             "data": "synthetic (seeded; random-init tensors of the workload's shapes)",
             "config": {"workload": workload_desc(w) + f"; draft side: {P} positions of one "
                        "query row per sequence (draft attention layer of the same shape)",
@@ -493,7 +499,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_steps,
             "warmup": max(args.warmup, 3), "ms_per_step": per_step_ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype(w),
             "data": "synthetic (seeded; random-init tensors of the workload's shapes)",
             "config": {"workload": workload_desc(w), "parallelism": f"dp{world} (sequence shards)",
                        "global_batch": world * w.B,
