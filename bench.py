@@ -471,25 +471,66 @@ def main():
 
     # end to end through the C ABI: every step copies its inputs (one pinned
     # host arena -> one device arena), runs the fused call and copies its
-    # results back (one device arena -> pinned host), then synchronizes
+    # results back (one device arena -> pinned host).  Serial: the host waits
+    # for each step.  Two batches in flight (a two-micro-batch serving loop):
+    # the host waits for a batch's previous result before issuing its next
+    # step, while the other batch's copies and step run.
     from speculative_decoding_verify_09_gb300.buffers import StagedStep
-    d = sets[0]
-    staged = StagedStep(d)
-    staged.pack(inp)
-    h2d, d2h = staged.in_bytes, staged.out_bytes
-    for it in range(3 + args.e2e_steps):
-        if it == 3:
-            if dist:
-                dist.barrier()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-        staged.upload()
-        api.spec_verify_step(staged.attn, staged.sample, d.kv_cap, d.new_kv_len, d.ws)
-        staged.download()
-        stream.synchronize()
-    e2e_s = shard.max_over_ranks(time.perf_counter() - t0, dist, device="cuda")
-    e2e = {"value": world * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+    if len(sets) < 2:
+        sets.append(StepBuffers(inp, api))
+    staged = [StagedStep(sets[0]), StagedStep(sets[1])]
+    for x in staged:
+        x.pack(inp)
+    h2d, d2h = staged[0].in_bytes, staged[0].out_bytes
+
+    def e2e_run(pipelined):
+        # uploads and downloads on their own streams: a batch's upload never
+        # waits behind the other batch's download (which waits for its step)
+        cs_up, cs_dn = torch.cuda.Stream(), torch.cuda.Stream()
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        dl = [torch.cuda.Event() for _ in range(2)]
+
+        def issue(i):
+            b = i % 2 if pipelined else 0
+            x, d = staged[b], sets[b]
+            if pipelined:
+                with torch.cuda.stream(cs_up):
+                    x.upload()
+                    up[b].record(cs_up)
+                stream.wait_event(up[b])
+            else:
+                x.upload()
+            api.spec_verify_step(x.attn, x.sample, d.kv_cap, d.new_kv_len, d.ws)
+            if pipelined:
+                done[b].record(stream)
+                with torch.cuda.stream(cs_dn):
+                    cs_dn.wait_event(done[b])
+                    x.download()
+                    dl[b].record(cs_dn)
+            else:
+                x.download()
+                stream.synchronize()
+
+        for i in range(4):
+            issue(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(args.e2e_steps):
+            if pipelined:
+                dl[i % 2].synchronize()        # this batch's previous result is on the host
+            issue(i)
+        torch.cuda.synchronize()
+        el = shard.max_over_ranks(time.perf_counter() - t0, dist, device="cuda")
+        return {"value": world * args.e2e_steps / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h}
+
+    e2e_serial = e2e_run(False)
+    e2e = e2e_run(True)
+    e2e["mode"] = "two independent batches in flight (copies of one overlap the other's step)"
+    e2e_serial["mode"] = "one step at a time, host waits for each"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -520,6 +561,7 @@ def main():
                          "avg_launch_us": attn_us, "kernel_src": sha},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "e2e_serial": e2e_serial,
             "gpu_launches": 2 * n_steps,
             "clocks": clocks,
         }
