@@ -82,12 +82,19 @@ def traffic_record(kernel_src_sha, workload=WORKLOAD):
 
 
 def src_sha():
+    """Hash of the attention kernel's sources with comments and whitespace
+    removed (a comment edit leaves the compiled kernel, and so its recorded
+    DRAM traffic, unchanged)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_09_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith("attention") or f.endswith((".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            text = open(os.path.join(csrc, f)).read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(f.encode() + b"\0" + "".join(text.split()).encode())
     return h.hexdigest()[:12]
 
 

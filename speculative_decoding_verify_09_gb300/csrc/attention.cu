@@ -14,11 +14,13 @@
 //    (K_i + 1) x (Hq/Hkv) query rows sharing that KV head are packed as the N
 //    dimension, so every KV byte is read once for all of them (GQA).
 //  * Stream-K split: the global tile sequence (segments in order) is cut into
-//    gridDim.x equal contiguous ranges, one per persistent CTA (one CTA per
-//    SM), regardless of segment boundaries.  A CTA that covers a whole segment
-//    writes the output directly; otherwise each piece writes a partial
-//    (unnormalized O, row max, row sum) and the last piece to arrive (atomic
-//    count, no waiting) merges them.
+//    gridDim.x contiguous ranges of equal cost (a segment costs its tiles plus
+//    kSegCost), one per persistent CTA (two CTAs per SM), regardless of
+//    segment boundaries.  A CTA that covers a whole segment writes the output
+//    directly; otherwise each piece writes a partial (unnormalized O, row max,
+//    row sum) and the last piece to arrive (atomic count, no waiting) folds
+//    every piece in CTA order (one routine at every merge site, so the bits do
+//    not depend on which piece merges).
 //  * Warp specialization: one producer warp walks the CTA's tile range and
 //    streams every K and V tile into a ring of shared-memory stages guarded by
 //    full / empty mbarriers, running ahead across segment boundaries: 16-byte
@@ -29,9 +31,13 @@
 //    segment's packed Q rows (bulk copies into 16-byte-padded rows) and a
 //    segment header into one of two Q slots.
 //  * Consumer warps (4 key slices x RS row groups) compute S^T = K Q^T and
-//    O^T += V^T P^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate) and an
-//    online softmax per warp; no CTA-wide barrier per tile.  At the end of a
-//    piece the key-slice states are merged in shared memory.
+//    O^T += V^T P^T with mma.sync m16n8k16 (bf16 in, or f16 built in registers
+//    from E4M3 K/V codes; fp32 accumulate) and an online softmax per warp; no
+//    CTA-wide barrier per tile.  At the end of a piece in the middle of a
+//    CTA's range the key-slice states are merged in shared memory and a
+//    merger warp counts the piece and, if last, folds the pieces; the CTA's
+//    final piece is closed by the consumers, with the slices in the (then
+//    idle) stages and one folding pass.
 //  * Every wait is bounded: a wait that runs out sets SV_DEV_TIMEOUT and the
 //    CTA drains its copies in flight and leaves.
 //
