@@ -18,7 +18,10 @@ Layouts (all host numpy arrays):
   seq_ids [B] int64; group [B] int32, prefix_start [G] int64, prefix_len [G]
   int32 (shared-prefix mode only)
 Float tensors are float32 arrays, or bfloat16 stored as uint16 bit patterns
-(rounded to nearest even from float32 draws).
+(rounded to nearest even from float32 draws).  With kv_dtype "e4m3" the K/V
+tensors (cache and block rows) are E4M3 codes (uint8) of float32 N(0, 1)
+draws divided by kv_scale, rounded to nearest even; the input dict then also
+holds kv_dtype, k_scale and v_scale.
 
 Draft tokens are drawn from softmax(draft_logits / T) over the full vocabulary
 (Gumbel-max with this module's RNG; the row's argmax when T = 0), standing in
