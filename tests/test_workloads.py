@@ -39,3 +39,38 @@ def test_step_bytes_bass_shape():
     a = W.make_inputs(W.workload("bass_b8"), with_attention=False, with_logits=False)
     nb = W.step_bytes(a)
     assert nb["attention"] > 8 * 512 * 32 * 128 * 4
+
+
+def test_step_bytes_count_every_tensor_once():
+    """Algorithmic bytes written out by hand for a small batch: the KV rows
+    read once, the block's q, out and new K/V, every logits row, and the
+    append's read + write of all block rows; an E4M3 cache counts one byte
+    per K/V element and leaves q, out and the logits unchanged."""
+    w = W.workload("bass_b8", B=3, Hq=4, Hkv=2, D=64, V=100, L_lo=10, L_hi=30, K_lo=2, K_hi=2,
+                   gen_seed=9)
+    a = W.make_inputs(w, with_attention=False, with_logits=False)
+    L = int(np.sum(a["kv_len"]))
+    R = 9                                           # 3 sequences x (K + 1)
+    kv = L * 2 * 64 * 2 * 2                         # K and V cache rows, bf16
+    block = R * (2 * 4 * 64 * 2 + 2 * 2 * 64 * 2)   # q + out, k_new + v_new
+    nb = W.step_bytes(a)
+    assert nb["attention"] == kv + block
+    assert nb["sampler"] == (2 * R - 3) * 100 * 2
+    assert nb["append"] == 2 * R * 2 * 64 * 2 * 2
+    a8 = dict(a, kv_dtype="e4m3")
+    nb8 = W.step_bytes(a8)
+    assert nb8["attention"] == kv // 2 + R * 2 * 4 * 64 * 2 + R * 2 * 2 * 64
+    assert nb8["sampler"] == nb["sampler"] and nb8["append"] == nb["append"] // 2
+
+
+def test_draft_inputs_positions_and_bytes():
+    w = W.workload("bass_b8", B=4, Hq=4, Hkv=4, D=64, V=50, L_lo=5, L_hi=20, gen_seed=3)
+    base, steps = W.make_draft_inputs(w, positions=3)
+    assert list(base["cu_q"]) == [0, 1, 2, 3, 4]
+    assert np.all(base["kv_cap"] == base["kv_len"] + 3)       # room for three positions
+    assert all(st["q"].shape == (4, 4, 64) and st["draft_logits"].shape == (4, 50)
+               for st in steps)
+    assert not np.array_equal(steps[0]["q"], steps[1]["q"])
+    L = int(np.sum(base["kv_len"]))
+    assert W.draft_step_bytes(base) == (L * 4 * 64 * 2 * 2 + 4 * (2 * 4 + 2 * 4) * 64 * 2
+                                        + 4 * 50 * 2 + 2 * 4 * 2 * 4 * 64 * 2)
