@@ -21,9 +21,9 @@
 //    accept tests; then the draw kernel (per-sequence chunks of row n_i) draws
 //    and, in the fused step, appends the accepted K/V rows.
 //
-// Precision: per-element weights 2^((l - lmax) log2(e)/T) in fp32 (the two
-// statistics paths: exp2f and float-float sums; the cluster path: the SFU's
-// approximate exp2 and fp32 (max, sum) merges, relative error below ~2e-6);
+// Precision: per-element weights 2^((l - lmax) log2(e)/T) in fp32 by the SFU's
+// approximate exp2 (the two statistics paths: float-float sums; the cluster
+// path: fp32 (max, sum) merges, relative error below ~2e-6);
 // the accept test compares u * p_hat < q_hat in fp32; the inverse-CDF draw
 // accumulates exact 64-bit fixed-point weights (2^-52 units), so the chosen
 // index does not depend on the summation order.  The near-tie windows of the
@@ -192,14 +192,15 @@ __device__ __forceinline__ void block_sum_ff(FF (&v)[N], FF *red) {
   }
 }
 
-// exp((l - lmax) / T) in fp32, with c = log2(e) / T split as c_hi + c_lo.
-// Explicit round-to-nearest intrinsics: every pass recomputes identical bits.
+// exp((l - lmax) / T) in fp32, with c = log2(e) / T split as c_hi + c_lo, by
+// the SFU's exp2 (relative error ~2^-22).  Explicit round-to-nearest
+// intrinsics: every pass recomputes identical bits.
 struct WeightFn {
   float lmax, c_hi, c_lo;
   __device__ __forceinline__ float operator()(float l) const {
     if (l == -INFINITY) return 0.0f;
     const float dl = __fsub_rn(l, lmax);
-    return exp2f(__fmaf_rn(dl, c_hi, __fmul_rn(dl, c_lo)));
+    return fast_exp2(__fmaf_rn(dl, c_hi, __fmul_rn(dl, c_lo)));
   }
 };
 
