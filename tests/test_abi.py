@@ -196,3 +196,33 @@ def test_e4m3_attention_host_validation(binding, kw, status):
 def test_e4m3_attention_accepted_shapes_size_a_workspace(binding):
     a = _attn(binding, kv_dtype=2, num_q_heads=4, num_kv_heads=2, k_scale=0.5, v_scale=0.25)
     assert binding.lib.sv_workspace_bytes(ctypes.byref(a), None) > 0
+
+
+def test_empty_batches_are_no_ops(binding):
+    """B = 0 passes every host check and launches nothing (no device needed)."""
+    ws = ctypes.c_void_p(4096)
+    a = binding.AttnArgs()
+    a.batch, a.num_q_heads, a.num_kv_heads, a.head_dim = 0, 4, 4, 128
+    a.dtype, a.max_q_rows = binding.SV_BF16, 1
+    assert binding.lib.spec_verify_attn(ctypes.byref(a), ws, 1 << 20, None) == binding.SV_OK
+    s = binding.SampleArgs()
+    s.batch, s.vocab, s.dtype, s.max_q_rows, s.num_rows = 0, 100, binding.SV_BF16, 1, 0
+    s.temperature, s.top_p = 1.0, 1.0
+    assert binding.lib.spec_reject_sample(ctypes.byref(s), ws, 1 << 20, None) == binding.SV_OK
+    d = binding.DraftArgs()
+    d.batch, d.vocab, d.dtype, d.temperature, d.top_p = 0, 100, binding.SV_BF16, 1.0, 1.0
+    assert binding.lib.spec_draft_sample(ctypes.byref(d), ws, 1 << 20, None) == binding.SV_OK
+    assert binding.lib.sv_draft_workspace_bytes(ctypes.byref(d)) > 0
+
+
+def test_api_refuses_host_tensors():
+    """The torch-facing calls take CUDA tensors only: there is no CPU path."""
+    import torch
+    from speculative_decoding_verify_09_gb300 import build
+    build()
+    from speculative_decoding_verify_09_gb300 import api
+    x = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.attn_args(x, x, x, x, x, torch.zeros(3, dtype=torch.int32),
+                      torch.zeros(2, dtype=torch.int64), torch.zeros(2, dtype=torch.int32), x,
+                      max_q_rows=2, kv_rows_bound=0)
