@@ -49,6 +49,16 @@ def workload_desc(w):
             f"top_p={w.top_p}, top_k={w.top_k}")
 
 
+def kernels_per_step(w):
+    """Kernels one fused step launches: the attention (prefix row-blocks,
+    decode partials and their merge with a shared prefix) and the sampler (one
+    cluster kernel without processing beyond a temperature, else statistics +
+    draw kernels)."""
+    attn = 3 if w.prefix_len or w.prefix_lens else 1
+    cluster = w.top_p >= 1.0 and w.top_k == 0 and w.temperature > 0.0
+    return attn + (1 if cluster else 2)
+
+
 def compute_dtype(w):
     """What the path computes in: bf16 / fp32 operands, or E4M3 K/V codes
     widened to f16 tensor-core operands (fp32 accumulation throughout)."""
@@ -367,7 +377,7 @@ def run_draft(args, w, api, shard, dist, world, rank, local_rank):
                          "algorithmic_bytes_per_launch": attn_bytes,
                          "avg_launch_us": attn_us, "kernel_src": sha},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 3 * P * n_steps,
+            "gpu_launches": (2 + kernels_per_step(w) - 1) * P * n_steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -569,7 +579,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "e2e_serial": e2e_serial,
-            "gpu_launches": 2 * n_steps,
+            "gpu_launches": kernels_per_step(w) * n_steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
