@@ -74,3 +74,18 @@ def test_draft_inputs_positions_and_bytes():
     L = int(np.sum(base["kv_len"]))
     assert W.draft_step_bytes(base) == (L * 4 * 64 * 2 * 2 + 4 * (2 * 4 + 2 * 4) * 64 * 2
                                         + 4 * 50 * 2 + 2 * 4 * 2 * 4 * 64 * 2)
+
+
+def test_padded_step_bytes_by_hand():
+    """Padding every cache to the longest and every block to the largest K:
+    written out for three sequences."""
+    w = W.workload("bass_b8", B=3, Hq=4, Hkv=2, D=64, V=100, L_dist="fixed",
+                   L_fixed=(10, 40, 25), K_fixed=(1, 4, 2), gen_seed=5)
+    a = W.make_inputs(w, with_attention=False, with_logits=False)
+    nb = W.padded_step_bytes(a)
+    assert nb["attention"] == 3 * 40 * 2 * 64 * 2 * 2 + 3 * 5 * (2 * 4 + 2 * 2) * 64 * 2
+    assert nb["sampler"] == (2 * 15 - 3) * 100 * 2
+    assert nb["append"] == 2 * 15 * 2 * 64 * 2 * 2
+    flat = W.step_bytes(a)
+    assert flat["attention"] == 75 * 2 * 64 * 2 * 2 + 10 * (2 * 4 + 2 * 2) * 64 * 2
+    assert nb["total"] > flat["total"]

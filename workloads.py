@@ -242,6 +242,27 @@ def draft_step_bytes(inp):
     return attn + B * inp["V"] * esz + 2 * B * 2 * Hkv * D * esz
 
 
+def padded_step_bytes(inp):
+    """Bytes the same verify step would move with padding (the vanilla
+    multi-sample method of the EMS-SD abstract): every sequence's cache read
+    to the batch's longest, every block and logits range to the largest draft
+    count, and the append of the longest block for every sequence.  Returned
+    like step_bytes, for comparison with it; no kernel runs this way."""
+    esz = 4 if inp["dtype"] == "f32" else 2
+    kvsz = 1 if inp.get("kv_dtype") == "e4m3" else esz
+    Hq, Hkv, D, B = inp["num_q_heads"], inp["num_kv_heads"], inp["head_dim"], inp["B"]
+    Lmax = int(np.max(inp["kv_len"])) if B else 0
+    Rmax = int(np.max(np.diff(inp["cu_q"]))) if B else 0
+    kv_rows = B * Lmax
+    if inp.get("group") is not None:
+        kv_rows += int(np.sum(inp["prefix_len"]))
+    R = B * Rmax
+    attn = kv_rows * Hkv * D * kvsz * 2 + R * 2 * Hq * D * esz + R * 2 * Hkv * D * kvsz
+    logits = (2 * R - B) * inp["V"] * esz
+    append = 2 * R * Hkv * D * kvsz * 2
+    return dict(attention=attn, sampler=logits, append=append, total=attn + logits + append)
+
+
 def step_bytes(inp):
     """Algorithmic HBM bytes of one verify step on these inputs.
 
