@@ -226,3 +226,23 @@ def test_api_refuses_host_tensors():
         api.attn_args(x, x, x, x, x, torch.zeros(3, dtype=torch.int32),
                       torch.zeros(2, dtype=torch.int64), torch.zeros(2, dtype=torch.int32), x,
                       max_q_rows=2, kv_rows_bound=0)
+
+
+@pytest.mark.parametrize("std,compiler,lang", [("c99", "gcc", "c"), ("c++17", "g++", "c++")])
+def test_header_compiles_as_plain_c_and_cxx(tmp_path, std, compiler, lang):
+    """include/spec_verify.h is a C ABI: it must compile as strict C99 (and as
+    C++), with every argument struct usable from C."""
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "spec_verify.h"\n'
+                   "int main(void) {\n"
+                   "  sv_attn_args a; sv_sample_args s; sv_draft_args d;\n"
+                   "  sv_status (*step)(const sv_attn_args *, const sv_sample_args *,\n"
+                   "                    const int32_t *, int32_t *, void *, size_t, void *)\n"
+                   "      = spec_verify_step;\n"
+                   "  (void)a; (void)s; (void)d; (void)step;\n"
+                   "  return 0;\n"
+                   "}\n")
+    r = subprocess.run([compiler, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-x", lang, "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
