@@ -19,9 +19,10 @@ high32(seq_id), stream), the key is (low32(seed), high32(seed)); word 0 gives
 the acceptance uniform and word 1 the sampling uniform, each as
 u = (w >> 8) * 2^-24, a 24-bit value exact in fp32 and fp64.
 
-Parity status: absolute agreement with published known-answer vectors is
-unpinned (no such vectors are available offline); the tests pin invertibility
-of the rounds, the constants, and the statistical properties the method needs.
+Pins: the known-answer vectors published with the generator's reference
+implementation (Random123: counter and key all zero, all ones, and the
+pi-digit counter/key) are matched exactly; the tests also pin invertibility of
+the rounds, the constants, and the statistical properties the method needs.
 """
 import numpy as np
 

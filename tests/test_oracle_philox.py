@@ -1,9 +1,12 @@
 """Pins of the oracle's Philox4x32-10 (Salmon et al., SC'11, section "Philox").
 
-Absolute known-answer vectors are not available offline, so these pin the
-published constants and round structure through an independently written
-inverse, plus the statistical properties the rejection sampler relies on.
+Absolute output: the known-answer vectors distributed with the generator's
+reference implementation (Random123), stored in tests/golden.  Besides them:
+the published constants and round structure through an independently written
+inverse, and the statistical properties the rejection sampler relies on.
 """
+import os
+
 import numpy as np
 import pytest
 from scipy import stats
@@ -33,6 +36,30 @@ def _inverse(y, key, rounds=10):
         c1 = y0 ^ hi1 ^ k0
         y0, y1, y2, y3 = c0, c1, c2, c3
     return y0, y1, y2, y3
+
+
+def _kat_rows():
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    rows = []
+    for line in open(path):
+        line = line.split("#", 1)[0].split()
+        if line:
+            rows.append((int(line[0]), [int(x, 16) for x in line[1:]]))
+    return rows
+
+
+@pytest.mark.parametrize("rounds,words", _kat_rows())
+def test_known_answer_vectors(rounds, words):
+    """Random123's published philox4x32-10 answers: counter 0 / key 0, all
+    ones, and the pi-digit counter and key."""
+    c, k, want = words[0:4], words[4:6], words[6:10]
+    got = [int(w) for w in philox4x32(*c, *k, rounds=rounds)]
+    assert got == want, [hex(x) for x in got]
+    assert _inverse(want, k, rounds) == tuple(c)
+
+
+def test_known_answer_vectors_present():
+    assert len(_kat_rows()) == 3
 
 
 def test_inverse_recovers_counter():
