@@ -197,10 +197,13 @@ SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_
  * supply the workspace spec_verify_attn takes.  The split-KV partials and
  * merge counters live instead in a fixed SV_STATIC_SCRATCH_BYTES array inside
  * the library's device image, one per device, held until the process exits.
- *   - Setup: the first call on a device (the current one) looks the array up
- *     and clears it to zero, synchronizing the device; make that first call
- *     before any stream capture and outside code that must not synchronize.
- *     Later calls only launch kernels on `stream`.
+ *   - Setup: the first call in a CUDA context (the current one: normally a
+ *     device's primary context) looks the array up and clears it to zero,
+ *     synchronizing the device; make that first call before any stream
+ *     capture and outside code that must not synchronize.  Later calls in
+ *     that context only launch kernels on `stream`.  The looked-up address is
+ *     kept per context, so a context made after cudaDeviceReset (or one that
+ *     a driver-API caller created) gets its own lookup and clearing.
  *   - Limits: the first 64 KiB hold only the merge counters (batch *
  *     num_kv_heads <= 16384); the scratch of the call
  *     (sv_workspace_bytes(attn, NULL)) plus those 64 KiB must fit in
@@ -208,11 +211,21 @@ SV_API sv_status spec_verify_attn(const sv_attn_args *attn, void *ws, size_t ws_
  *     SV_ERR_WORKSPACE and launches nothing.
  *   - Zero state: the merge counters must be zero when a call starts; setup
  *     zeroes them and every call that runs to completion leaves them zero.
- *   - Concurrency: all calls on one device share the array, so calls that can
- *     overlap on the GPU (other streams, other host threads without ordering)
- *     race and corrupt each other's partials; order them on one stream.
- * Results are those of spec_verify_attn on the same arguments. */
+ *     A call that ends with SV_DEV_TIMEOUT in *dev_status can leave counts
+ *     behind: call sv_static_scratch_reset before the next static call.
+ *   - Concurrency: all calls in one context share the array, so calls that
+ *     can overlap on the GPU (other streams, other host threads without
+ *     ordering) race and corrupt each other's partials; order them on one
+ *     stream.
+ * Results are those of spec_verify_attn on the same arguments (same kernels,
+ * same merge order: equal bits). */
 SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream);
+
+/* Zero the merge counters of the static array (64 KiB, cudaMemsetAsync on
+ * `stream`; allocates nothing; the first call in a context also runs the setup
+ * described above).  Needed only after a static call reported SV_DEV_TIMEOUT;
+ * like spec_verify_attn_static it has no counterpart in the papers. */
+SV_API sv_status sv_static_scratch_reset(void *stream);
 
 /* Rejection sampling only: writes num_accepted and out_tokens. */
 SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,

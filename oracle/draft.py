@@ -47,7 +47,9 @@ def draft_sample(draft_logits, kv_len, temperature, top_p, seed, seq_ids=None, t
     (-1 for a failed sequence), seq_status [B], status, and the near-tie audit:
     tie [B] bool (u within TIE_EPS of an end of the chosen token's CDF
     interval, or a nucleus boundary mass within NUCLEUS_TIE_EPS of top_p) and
-    tie_alts {i: tokens a tied draw may also yield}.
+    tie_alts {i: tokens a tied draw may also yield} for every tied sequence:
+    the weighted tokens whose normalized CDF interval lies within TIE_EPS of u,
+    and for a nucleus tie also those of the draw under the neighbouring cut.
     """
     B = int(np.asarray(kv_len).shape[0])
     kv_len = np.asarray(kv_len, dtype=np.int64)
@@ -74,8 +76,13 @@ def draft_sample(draft_logits, kv_len, temperature, top_p, seed, seq_ids=None, t
         m, _, nb = _cdf_margin(row.probs, x, float(u))
         if m < TIE_EPS or row.margin < NUCLEUS_TIE_EPS:
             tie[i] = True
-            if row.margin >= NUCLEUS_TIE_EPS:
-                tie_alts[i] = {x} | {t for t in nb if t is not None}
+            alts = set(nb)
+            if row.margin < NUCLEUS_TIE_EPS:
+                alt = process_row(to_f64(draft_logits[i]), T_i, tp_i, tk_i, alt=True)
+                xa = sample_index(alt.probs, float(u))
+                _, _, nba = _cdf_margin(alt.probs, xa, float(u))
+                alts |= set(nba)
+            tie_alts[i] = alts
     status = int(np.bitwise_or.reduce(seq_status)) if B else 0
     return dict(tokens=tokens, seq_status=seq_status, status=status, tie=tie,
                 tie_alts=tie_alts)

@@ -57,10 +57,9 @@ DEV_BAD_PARAM = 64
 # Near-tie audit windows.  Decisions this close to a boundary may legitimately
 # differ between an fp32 GPU path and this fp64 oracle; they are counted and
 # excluded from bit-exact comparison (with everything after them in that
-# sequence).  RESIDUAL_MASS_MIN: below it the residual is a difference of nearly
-# equal probabilities whose normalized CDF fp32 cannot resolve to TIE_EPS.
+# sequence).  TIE_EPS is the stated window of the accept compare and of the
+# residual / bonus CDF at the drawn token.
 TIE_EPS = 1e-5
-RESIDUAL_MASS_MIN = 1e-2
 # Nucleus cut window: the cut compares a mass with top_p; an fp32 path with
 # fp64 cross-thread sums gets that mass to ~5e-7, so boundaries within 2e-6 of
 # top_p are treated as ties (the 1e-5 windows above are for u comparisons).
@@ -130,11 +129,16 @@ def params_ok(temperature, top_p, top_k):
     return T >= 0.0 and tp > 0.0 and int(top_k) >= 0
 
 
-def process_row(logits, temperature, top_p, top_k=0):
+def process_row(logits, temperature, top_p, top_k=0, alt=False):
     """Temperature, then top-k, then nucleus, on one row of exact float64
     logits; temperature 0 is greedy (one-hot at the first maximum).
 
     temperature and top_p are taken as the float32 values the C-ABI receives.
+    With alt=True, a row whose nucleus boundary mass lies within
+    NUCLEUS_TIE_EPS of top_p is returned with the neighbouring cut instead
+    (one tie class more when the kept mass barely reaches top_p, one fewer
+    when the mass above the cut barely misses it): the row a path whose mass
+    sums differ by rounding may build.  Other rows are returned unchanged.
     """
     T = float(np.float32(temperature))
     tp = float(np.float32(top_p))
@@ -166,6 +170,11 @@ def process_row(logits, temperature, top_p, top_k=0):
     tau = vals[k]
     above = M[k] - tp
     below = tp - (M[k - 1] if k > 0 else 0.0)
+    if alt and min(abs(above), abs(below)) < NUCLEUS_TIE_EPS:
+        if abs(above) <= abs(below) and k + 1 < vals.shape[0]:
+            tau = vals[k + 1]
+        elif k > 0:
+            tau = vals[k - 1]
     keep = z >= tau
     wk = np.where(keep, w, 0.0)
     return ProcessedRow(wk / wk.sum(), True, tau, min(abs(above), abs(below)))
@@ -199,17 +208,19 @@ def sample_index(weights, u):
 
 
 def _cdf_margin(weights, x, u):
-    """Distance of u from the two ends of x's CDF interval, Z, and the nearest
-    indices on either side of x that carry weight (None at the ends)."""
-    c = np.cumsum(weights)
+    """Distance of u from the two ends of x's normalized CDF interval, Z, and
+    the weighted tokens whose normalized CDF interval meets [u - TIE_EPS,
+    u + TIE_EPS] (the draws a path whose CDF is off by less than TIE_EPS can
+    make; x among them)."""
+    w = np.asarray(weights, dtype=np.float64)
+    c = np.cumsum(w)
     Z = c[-1]
     hi = c[x] / Z
     lo = c[x - 1] / Z if x > 0 else 0.0
-    nz = np.flatnonzero(np.asarray(weights, dtype=np.float64) > 0)
-    k = int(np.searchsorted(nz, x))
-    prev_x = int(nz[k - 1]) if k > 0 else None
-    next_x = int(nz[k + 1]) if k + 1 < nz.shape[0] else None
-    return min(u - lo, hi - u), Z, (prev_x, next_x)
+    cn = c / Z
+    lo_all = np.concatenate([[0.0], cn[:-1]])
+    near = (w > 0) & (cn > u - TIE_EPS) & (lo_all <= u + TIE_EPS)
+    return min(u - lo, hi - u), Z, {int(t) for t in np.flatnonzero(near)} | {int(x)}
 
 
 # --------------------------------------------------------------------------
@@ -221,10 +232,10 @@ def verify_sequence(q_rows, p_rows, drafts, u_acc, u_smp, audit=None):
     q_rows: [K+1, V] processed target rows; p_rows: [K, V] processed draft rows;
     drafts: [K] tokens; u_acc, u_smp: [K+1] uniforms for rows 0..K.
     Returns (n_accepted, sampled_token, status_bits).  If `audit` is a list, one
-    (row, kind, margin, neighbours) tuple is appended per decision taken; kind
-    is "accept", "residual", "bonus" or "empty", neighbours (draws only) the
-    nearest weighted indices on either side of the drawn token, or None when a
-    draw within the tie window could land anywhere.
+    (row, kind, margin, window) tuple is appended per decision taken; kind
+    is "accept", "residual", "bonus" or "empty" (a rejection whose residual is
+    zero everywhere: the draw then takes q_hat), window (draws only) the
+    weighted tokens whose normalized CDF interval lies within TIE_EPS of u.
     """
     K = len(drafts)
     V = q_rows.shape[1] if hasattr(q_rows, "shape") else len(q_rows[0])
@@ -264,8 +275,6 @@ def verify_sequence(q_rows, p_rows, drafts, u_acc, u_smp, audit=None):
         x = sample_index(w, u_smp[K])
     if audit is not None:
         m, Z, nb = _cdf_margin(w, x, float(u_smp[n]))
-        if kind == "empty" or (kind == "residual" and not float(Z) >= RESIDUAL_MASS_MIN):
-            m, nb = 0.0, None
         audit.append((n, kind, m, nb))
     return n, x, status
 
@@ -290,15 +299,21 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
     a failed sequence), status (OR of bits), seq_status [B], and the near-tie
     audit:
       tie_row [B]   row of the first decision inside a tie window, or -1;
-      tie_kind [B]  0 none, TIE_ACCEPT (an accept/reject decision: rows before
-                    tie_row are still exact), TIE_DRAW (the final draw: n_i, the
-                    accepted drafts and the append are still exact);
-      tie_alts      {i: set of tokens a draw tie may also yield} (missing: any);
-      tie_count     number of sequences with a tie.
+      tie_kind [B]  0 none, TIE_ACCEPT (an accept/reject decision, or a row
+                    whose nucleus cut is itself a tie: rows before tie_row are
+                    still exact), TIE_DRAW (the final draw: n_i, the accepted
+                    drafts and the append are still exact);
+      tie_alts      {i: set of tokens a draw tie may yield} for every TIE_DRAW
+                    sequence: the weighted tokens whose normalized CDF interval
+                    lies within TIE_EPS of u (the oracle's token among them);
+      tie_count     number of sequences with a tie;
+      tie_clauses   {"accept", "cdf", "nucleus"}: sequences whose first tie is
+                    of that clause;
+      tie_positions decisions inside a tie window along the oracle's own path
+                    (a sequence can hold more than one).
     A decision is inside a tie window when |u - min(1, q/p)| < TIE_EPS, when
-    the draw's normalized CDF interval has an end within TIE_EPS of u, when a
-    residual's mass is below RESIDUAL_MASS_MIN, or when a row it uses has a
-    nucleus boundary mass within NUCLEUS_TIE_EPS of top_p.
+    the draw's normalized CDF interval has an end within TIE_EPS of u, or when
+    a row it uses has a nucleus boundary mass within NUCLEUS_TIE_EPS of top_p.
     """
     cu_q = np.asarray(cu_q, dtype=np.int64)
     B = cu_q.shape[0] - 1
@@ -313,6 +328,8 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
     tie_kind = np.zeros(B, dtype=np.int64)
     tie_alts = {}
     tie_count = 0
+    tie_clauses = {"accept": 0, "cdf": 0, "nucleus": 0}
+    tie_positions = 0
     for i in range(B):
         r0, r1 = int(cu_q[i]), int(cu_q[i + 1])
         K = r1 - r0 - 1
@@ -343,22 +360,32 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
         num_acc[i] = n
         out_tokens[r0:r0 + n] = draft_tokens[p0:p0 + n]
         out_tokens[r0 + n] = x
-        # first decision inside a tie window (including nucleus boundaries of
-        # the rows that decision used)
+        # decisions inside a tie window (including nucleus boundaries of the
+        # rows each decision used); the first one decides what stays exact
+        first = True
         for (j, kind, m, nb) in audit:
             nuc = qp[j].margin if kind == "bonus" else min(
                 qp[j].margin, pp[j].margin if j < K else np.inf)
-            if m < TIE_EPS or nuc < NUCLEUS_TIE_EPS:
-                tie_row[i] = j
-                tie_count += 1
-                if kind == "accept" or nuc < NUCLEUS_TIE_EPS:
-                    tie_kind[i] = TIE_ACCEPT
-                else:
-                    tie_kind[i] = TIE_DRAW
-                    if nb is not None:
-                        tie_alts[i] = {x} | {t for t in nb if t is not None}
-                break
+            if not (m < TIE_EPS or nuc < NUCLEUS_TIE_EPS):
+                continue
+            tie_positions += 1
+            if not first:
+                continue
+            first = False
+            tie_row[i] = j
+            tie_count += 1
+            if nuc < NUCLEUS_TIE_EPS:
+                tie_kind[i] = TIE_ACCEPT
+                tie_clauses["nucleus"] += 1
+            elif kind == "accept":
+                tie_kind[i] = TIE_ACCEPT
+                tie_clauses["accept"] += 1
+            else:
+                tie_kind[i] = TIE_DRAW
+                tie_clauses["cdf"] += 1
+                tie_alts[i] = set(nb)
     status = int(np.bitwise_or.reduce(seq_status)) if B else 0
     return dict(num_accepted=num_acc, out_tokens=out_tokens, status=status,
                 seq_status=seq_status, tie_row=tie_row, tie_kind=tie_kind,
-                tie_alts=tie_alts, tie_count=tie_count)
+                tie_alts=tie_alts, tie_count=tie_count, tie_clauses=tie_clauses,
+                tie_positions=tie_positions)

@@ -42,4 +42,5 @@ def verify_step(inp, attention=True):
                 new_kv_len=new_len, k_cache=kc, v_cache=vc, status=s["status"] | st,
                 seq_status=s["seq_status"], tie_row=s["tie_row"],
                 tie_kind=s["tie_kind"], tie_alts=s["tie_alts"],
-                tie_count=s["tie_count"])
+                tie_count=s["tie_count"], tie_clauses=s["tie_clauses"],
+                tie_positions=s["tie_positions"])

@@ -74,6 +74,8 @@ def _load():
     lib.spec_verify_attn.restype = ctypes.c_int
     lib.spec_verify_attn_static.argtypes = [P(AttnArgs), _p]
     lib.spec_verify_attn_static.restype = ctypes.c_int
+    lib.sv_static_scratch_reset.argtypes = [_p]
+    lib.sv_static_scratch_reset.restype = ctypes.c_int
     lib.spec_reject_sample.argtypes = [P(SampleArgs), _p, ctypes.c_size_t, _p]
     lib.spec_reject_sample.restype = ctypes.c_int
     lib.sv_draft_workspace_bytes.argtypes = [P(DraftArgs)]

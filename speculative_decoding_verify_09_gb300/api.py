@@ -162,6 +162,12 @@ def spec_verify_attn_static(attn, stream=None):
     _check(lib.spec_verify_attn_static(ctypes.byref(attn), _stream(stream)))
 
 
+def sv_static_scratch_reset(stream=None):
+    """Zero the static scratch's merge counters on `stream` (after a static call
+    reported SV_DEV_TIMEOUT); allocates nothing."""
+    _check(lib.sv_static_scratch_reset(_stream(stream)))
+
+
 def spec_reject_sample(sample, ws, stream=None):
     _check(lib.spec_reject_sample(ctypes.byref(sample), ctypes.c_void_p(ws.ptr), ws.nbytes,
                                   _stream(stream)))

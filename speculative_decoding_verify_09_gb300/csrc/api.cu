@@ -8,6 +8,8 @@
 #include <mutex>
 #include <string>
 
+#include <cuda.h>
+
 #include "kernels.h"
 
 namespace {
@@ -340,28 +342,79 @@ namespace {
 // Front zone of g_static_scratch that holds only merge counters (B * Hkv words).
 constexpr size_t kStaticCounterBytes = 64 * 1024;
 
-std::mutex g_static_mu;
-void *g_static_ptr[64] = {};
+// The array's device address belongs to a CUDA context, not to a device
+// ordinal: after cudaDeviceReset, or under a context that a driver-API caller
+// created and made current, the same ordinal has a new context with its own
+// copy of the array.  So the looked-up address and the "cleared" state are
+// kept per context, keyed by the driver's context id (unique for the life of
+// the process, never reused).  The two driver calls are fetched through the
+// runtime, so the library does not link the driver library itself.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
-// Device address of g_static_scratch on the current device.  The first call on
-// each device looks the symbol up and clears the array (synchronously, before
-// returning); later calls only read the cached address.
+struct StaticEntry {
+  unsigned long long ctx_id;
+  void *ptr;
+};
+
+std::mutex g_static_mu;
+constexpr int kStaticCtxCap = 64;
+StaticEntry g_static_tab[kStaticCtxCap] = {};
+int g_static_used = 0, g_static_next = 0;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+sv_status current_context_id(unsigned long long *id) {
+  if (!g_ctx_current || !g_ctx_id) {
+    void *f0 = nullptr, *f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0{}, q1{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000,
+                                                     cudaEnableDefault, &q0);
+    if (e == cudaSuccess)
+      e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch: driver entry points");
+    if (q0 != cudaDriverEntryPointSuccess || q1 != cudaDriverEntryPointSuccess || !f0 || !f1)
+      return fail(SV_ERR_CUDA, "static scratch: cuCtxGetCurrent / cuCtxGetId not available");
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f0);
+    g_ctx_id = reinterpret_cast<CtxGetIdFn>(f1);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx)
+    return fail(SV_ERR_CUDA, "static scratch: no current CUDA context");
+  if (g_ctx_id(ctx, id) != CUDA_SUCCESS) return fail(SV_ERR_CUDA, "static scratch: cuCtxGetId");
+  return SV_OK;
+}
+
+// Device address of g_static_scratch in the current context.  The first call
+// in each context makes the runtime current on it, looks the symbol up and
+// clears the array (synchronously, before returning); later calls in that
+// context only read the cached address.
 sv_status static_scratch(void **out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);   // also initializes the runtime's context
   if (e != cudaSuccess) return cuda_fail(e, "static scratch: cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(SV_ERR_CUDA, "static scratch: device %d out of range", dev);
+  e = cudaFree(nullptr);                 // binds the primary context if none is current
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch: context setup");
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "static scratch: cudaGetSymbolAddress");
-    e = cudaMemset(p, 0, SV_STATIC_SCRATCH_BYTES);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "static scratch: clearing");
-    g_static_ptr[dev] = p;
-  }
-  *out = g_static_ptr[dev];
+  unsigned long long id = 0;
+  sv_status st = current_context_id(&id);
+  if (st != SV_OK) return st;
+  for (int k = 0; k < g_static_used; ++k)
+    if (g_static_tab[k].ctx_id == id) {
+      *out = g_static_tab[k].ptr;
+      return SV_OK;
+    }
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch: cudaGetSymbolAddress");
+  e = cudaMemset(p, 0, SV_STATIC_SCRATCH_BYTES);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch: clearing");
+  // a full table drops its oldest entry (a context that long ago went away)
+  const int slot = g_static_used < kStaticCtxCap ? g_static_used++ : g_static_next;
+  if (slot == g_static_next) g_static_next = (g_static_next + 1) % kStaticCtxCap;
+  g_static_tab[slot] = StaticEntry{id, p};
+  *out = p;
   return SV_OK;
 }
 
@@ -420,6 +473,15 @@ SV_API sv_status spec_verify_attn_static(const sv_attn_args *attn, void *stream)
   void *ws = nullptr;
   if ((st = static_scratch(&ws)) != SV_OK) return st;
   return run_attention(attn, L, ws, opts_alone(), static_cast<cudaStream_t>(stream));
+}
+
+SV_API sv_status sv_static_scratch_reset(void *stream) {
+  void *ws = nullptr;
+  sv_status st = static_scratch(&ws);
+  if (st != SV_OK) return st;
+  cudaError_t e = cudaMemsetAsync(ws, 0, kStaticCounterBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch reset");
+  return SV_OK;
 }
 
 SV_API sv_status spec_reject_sample(const sv_sample_args *sample, void *ws, size_t ws_bytes,

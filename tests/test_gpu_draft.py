@@ -35,9 +35,8 @@ def compare_draft(ref, got):
     for i, tok in enumerate(got):
         if ref["tie"][i]:
             ties += 1
-            alts = ref["tie_alts"].get(i)
-            if alts is not None:
-                assert int(tok) in alts, f"seq {i}: {tok} not in tie set {alts}"
+            alts = ref["tie_alts"][i]
+            assert int(tok) in alts, f"seq {i}: {tok} not in tie set {alts}"
             continue
         assert int(tok) == int(ref["tokens"][i]), f"seq {i}: {tok} != {ref['tokens'][i]}"
     return ties
