@@ -9,10 +9,19 @@ collective; the barrier and the max-over-ranks timing use torch.distributed.
 
 Prints one JSON line (rank 0).  `value` = verify steps/s of the whole job with
 inputs resident in HBM (CUDA-graph replays of the C-ABI call, three rotating
-input sets so every step reads ~176 MB > L2); `e2e` = the same metric through
-the C-ABI call with pinned host buffers copied in and results copied out every
-step; `roofline` = the attention kernel (the dominant one) timed alone;
-`cpu_baseline` = the CPU oracle timed on a bounded sample.
+input sets so every step reads ~157 MB > L2; exactly --steps calls timed);
+`e2e` = the same metric through the C-ABI call with pinned host buffers copied
+in and results copied out every step; `roofline` = the attention kernel (the
+dominant one) timed alone; `cpu_baseline` = the CPU oracle timed on a bounded
+sample with one thread, `cpu_baseline_all_cores` with every core of the
+affinity mask.  Draft tokens are drawn from the processed draft rows p_hat on
+the device (the draft model's sampler) unless --gumbel-drafts; the oracle
+draws its own from the same rows and counters.  `oracle_check` compares the
+GPU step's outputs with the oracle's on these inputs, `ties` counts the
+decisions inside the near-tie windows, `acceptance` sets the measured mean
+accepted drafts per sequence (over --acc-seeds Philox seeds) beside the closed
+form sum_j prod_t sum_x min(p_hat, q_hat); `padded` (with --padded) times the
+same batch padded to its longest cache and largest K.
 `--impl reference` times the CPU oracle alone (the reference arm).
 """
 import argparse
@@ -152,9 +161,10 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
-def cpu_baseline(inp, budget_s=12.0):
-    """The oracle, as it stands, on whole bass_b8 steps until the budget is
-    used (at least one step)."""
+def cpu_baseline(inp, budget_s=12.0, cores=1):
+    """The oracle, as it stands, on whole steps of the workload until the
+    budget is used (at least one step); BLAS/OMP threads as the process was
+    started with (`cores`)."""
     import oracle
     n, t0 = 0, time.perf_counter()
     while True:
@@ -163,9 +173,25 @@ def cpu_baseline(inp, budget_s=12.0):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} whole {inp['workload'].name} steps (attention + sampling + append), "
-                      f"{el:.1f} s, OMP/BLAS threads 1"}
+                      f"{el:.1f} s, OMP/BLAS threads {cores}"}
+
+
+def cpu_baseline_all_cores(argv, budget_s=10.0):
+    """The same timing in a child process whose BLAS/OMP threads are all the
+    cores of this process's affinity mask (the thread count is fixed when numpy
+    loads, hence the child)."""
+    ncores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env = dict(os.environ, OMP_NUM_THREADS=str(ncores), OPENBLAS_NUM_THREADS=str(ncores),
+               MKL_NUM_THREADS=str(ncores), CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), *argv, "--cpu-child",
+                            str(ncores), "--cpu-budget", str(budget_s)],
+                           capture_output=True, text=True, env=env, timeout=budget_s * 6 + 120)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:        # reported, never fatal to the GPU measurement
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
 
 def overrides(args):
@@ -176,6 +202,8 @@ def overrides(args):
         over.update(K_lo=args.k, K_hi=args.k, K_fixed=())
     if args.kv_dtype is not None:
         over.update(kv_dtype=args.kv_dtype)
+    if args.draft_noise is not None:
+        over.update(draft_noise=args.draft_noise)
     return over
 
 
@@ -198,6 +226,8 @@ def run_reference(args, rank):
         metric = DRAFT_METRIC
     else:
         inp = W.make_inputs(w)
+        if not args.gumbel_drafts:      # the oracle's own draws from p_hat (untimed setup)
+            inp["draft_tokens"], _ = oracle_drafts(inp)
 
         def one():
             oracle.verify_step(inp)
@@ -221,19 +251,27 @@ def run_reference(args, rank):
 
 
 def timed_replays(torch, sets, fn, n_launch, stream, dist, shard, no_graph, percentiles):
-    """Time n_launch calls of fn over the rotating input sets with CUDA events on
-    the launching stream (one CUDA graph holding one call per set, unless
-    no_graph); the barrier and max over ranks make it the job's time.  Returns
-    (ms, calls, pct): pct (with percentiles) holds p10 / p50 / p90 of the time
-    per call over 200 single graph replays, each bracketed by its own events."""
-    graph = None
+    """Time exactly n_launch calls of fn over the rotating input sets with CUDA
+    events on the launching stream: full replays of one CUDA graph holding one
+    call per set, then (when n_launch is not a multiple of the sets) one replay
+    of a graph holding the first n_launch % len(sets) calls (unless no_graph);
+    the barrier and max over ranks make it the job's time.  Returns (ms, calls,
+    pct): pct (with percentiles) holds p10 / p50 / p90 of the time per call over
+    200 single full replays, each bracketed by its own events."""
+    n_launch = max(1, int(n_launch))
+    reps, rem = divmod(n_launch, len(sets))
+    graph = graph_rem = None
     if not no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for d in sets:
                 fn(d)
+        if rem:
+            graph_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rem):
+                for d in sets[:rem]:
+                    fn(d)
         torch.cuda.synchronize()
-    reps = max(1, n_launch // len(sets))
     for _ in range(2):
         graph.replay() if graph else [fn(d) for d in sets]
     if dist:
@@ -246,6 +284,12 @@ def timed_replays(torch, sets, fn, n_launch, stream, dist, shard, no_graph, perc
             graph.replay()
         else:
             for d in sets:
+                fn(d)
+    if rem:
+        if graph_rem is not None:
+            graph_rem.replay()
+        else:
+            for d in sets[:rem]:
                 fn(d)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -264,7 +308,110 @@ def timed_replays(torch, sets, fn, n_launch, stream, dist, shard, no_graph, perc
         pct = {"p10": float(np.percentile(per, 10)), "p50": float(np.percentile(per, 50)),
                "p90": float(np.percentile(per, 90)), "unit": "us per call",
                "replays": n, "calls_per_replay": len(sets)}
-    return ms, reps * len(sets), pct
+    return ms, n_launch, pct
+
+
+def draft_rows(inp, j):
+    """Sequences with a draft j + 1 and the index of their draft row j."""
+    cu = np.asarray(inp["cu_q"], dtype=np.int64)
+    K = np.diff(cu) - 1
+    seqs = np.flatnonzero(K > j)
+    return seqs, cu[seqs] - seqs + j
+
+
+def draw_drafts_on_device(torch, api, d, inp, seed=None):
+    """Replace the draft tokens of StepBuffers `d` by draws from the processed
+    draft rows (spec_draft_sample: temperature / top-k / top-p, Philox stream
+    1): draft j + 1 of sequence i is drawn from its draft row j, at token index
+    kv_len[i] + j + 1, as the draft model's sampler draws it.  Setup only
+    (untimed).  Returns the tokens as a host array."""
+    K = np.diff(np.asarray(inp["cu_q"])) - 1
+    for j in range(int(K.max()) if K.size else 0):
+        seqs, rows = draft_rows(inp, j)
+        idx = torch.from_numpy(rows).cuda()
+        logits = d.drf.index_select(0, idx).contiguous()
+        kv = torch.from_numpy((np.asarray(inp["kv_len"])[seqs] + j).astype(np.int32)).cuda()
+        sid = d.seq_ids.index_select(0, torch.from_numpy(seqs).cuda()).contiguous()
+        out = torch.empty(len(seqs), dtype=torch.int32, device="cuda")
+        args = api.draft_args(logits, kv, out, temperature=inp["temperature"],
+                              top_p=inp["top_p"], seed=inp["seed"] if seed is None else seed,
+                              seq_ids=sid, dev_status=d.status, top_k=inp.get("top_k", 0))
+        ws = api.Workspace(api.draft_workspace_bytes(args))
+        api.spec_draft_sample(args, ws)
+        d.drafts.index_copy_(0, idx, out)
+        torch.cuda.synchronize()
+    return d.drafts.cpu().numpy()
+
+
+def oracle_drafts(inp):
+    """The oracle's own draws of the same drafts (same rows, indices and
+    Philox stream 1 counters as draw_drafts_on_device); returns (tokens, set of
+    draft rows inside the oracle's draw tie window)."""
+    import oracle
+    toks = np.array(inp["draft_tokens"], copy=True)
+    tied = set()
+    K = np.diff(np.asarray(inp["cu_q"])) - 1
+    for j in range(int(K.max()) if K.size else 0):
+        seqs, rows = draft_rows(inp, j)
+        r = oracle.draft_sample(inp["draft_logits"][rows], np.asarray(inp["kv_len"])[seqs] + j,
+                                inp["temperature"], inp["top_p"], inp["seed"],
+                                np.asarray(inp["seq_ids"])[seqs], inp.get("top_k", 0))
+        toks[rows] = r["tokens"]
+        tied |= {int(x) for x in rows[r["tie"]]}
+    return toks, tied
+
+
+def oracle_check(inp_oracle, gpu_drafts, drafts_tied, num_accepted, out_tokens):
+    """The oracle's step on its own drafts against the GPU's outputs: sequences
+    equal bit for bit, inside a near-tie window (a draft draw or a step
+    decision), or different (must be 0), and the tie counts by clause."""
+    import oracle
+    ref = oracle.verify_step(inp_oracle, attention=False)
+    cu = np.asarray(inp_oracle["cu_q"])
+    exact = tied = bad = 0
+    draft_ties = 0
+    for i in range(len(cu) - 1):
+        r0, r1 = int(cu[i]), int(cu[i + 1])
+        rows = range(r0 - i, r1 - i - 1)
+        if any(r in drafts_tied for r in rows):
+            draft_ties += 1
+            tied += 1
+            continue
+        if any(int(gpu_drafts[r]) != int(inp_oracle["draft_tokens"][r]) for r in rows):
+            bad += 1
+            continue
+        if ref["tie_kind"][i]:
+            tied += 1
+            continue
+        same = int(num_accepted[i]) == int(ref["num_accepted"][i]) and \
+            list(out_tokens[r0:r1]) == list(ref["out_tokens"][r0:r1])
+        exact += same
+        bad += not same
+    return ({"sequences": len(cu) - 1, "exact": exact, "tied": tied, "different": bad},
+            {"sequences": int(ref["tie_count"]) + draft_ties,
+             "positions": int(ref["tie_positions"]) + len(drafts_tied),
+             "clauses": dict(ref["tie_clauses"], draft_draw=draft_ties)})
+
+
+def acceptance_closed_form(inp):
+    """Expected accepted drafts per sequence with drafts drawn from p_hat:
+    sum_j prod_{t <= j} beta_t, beta_t = sum_x min(p_hat_t, q_hat_t) (the
+    speculative-sampling paper's acceptance rate, appendix "Proof")."""
+    from oracle.sampling import process_row, to_f64
+    cu = np.asarray(inp["cu_q"])
+    tot = []
+    for i in range(len(cu) - 1):
+        r0, K = int(cu[i]), int(cu[i + 1] - cu[i] - 1)
+        e, run = 0.0, 1.0
+        for j in range(K):
+            q = process_row(to_f64(inp["target_logits"][r0 + j]), inp["temperature"],
+                            inp["top_p"], inp.get("top_k", 0)).probs
+            p = process_row(to_f64(inp["draft_logits"][r0 - i + j]), inp["temperature"],
+                            inp["top_p"], inp.get("top_k", 0)).probs
+            run *= float(np.minimum(p, q).sum())
+            e += run
+        tot.append(e)
+    return float(np.mean(tot))
 
 
 DRAFT_METRIC = ("draft-side steps/s (K positions of single-row attention + append + draft "
@@ -409,11 +556,29 @@ def main():
                          "(K single-row positions per step)")
     ap.add_argument("--positions", type=int, default=None,
                     help="draft positions per draft-side step (default: the workload's K)")
+    ap.add_argument("--draft-noise", type=float, default=None,
+                    help="override: std of the draft logits' noise around the target logits")
+    ap.add_argument("--padded", action="store_true",
+                    help="also time the same batch padded (every cache to the longest, every "
+                         "block to the largest K), as a padded multi-sample step would run")
+    ap.add_argument("--gumbel-drafts", action="store_true",
+                    help="keep the generator's stand-in drafts (Gumbel-max over the unprocessed "
+                         "draft row) instead of drawing them from p_hat on the device")
+    ap.add_argument("--acc-seeds", type=int, default=64,
+                    help="Philox seeds of the measured acceptance (drafts redrawn per seed)")
+    ap.add_argument("--cpu-child", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.cpu_child:                  # the oracle timed with all cores (no GPU)
+        inp = W.make_inputs(W.workload(args.workload, **overrides(args)))
+        if not args.gumbel_drafts:
+            inp["draft_tokens"], _ = oracle_drafts(inp)
+        print(json.dumps(cpu_baseline(inp, args.cpu_budget, cores=args.cpu_child)), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, rank)
         return
@@ -445,6 +610,10 @@ def main():
     inp["seq_ids"] = inp["seq_ids"] + lo
     from speculative_decoding_verify_09_gb300.buffers import StepBuffers
     sets = [StepBuffers(inp, api) for _ in range(args.sets)]
+    if not args.gumbel_drafts:        # drafts from p_hat, as the draft model draws them
+        for d in sets:
+            gpu_drafts = draw_drafts_on_device(torch, api, d, inp)
+        inp["draft_tokens"] = gpu_drafts
     nbytes = W.step_bytes(inp)
     stream = torch.cuda.current_stream()
 
@@ -549,9 +718,57 @@ def main():
     e2e["mode"] = "two independent batches in flight (copies of one overlap the other's step)"
     e2e_serial["mode"] = "one step at a time, host waits for each"
 
-    cpu = None
+    # measured acceptance (untimed): per Philox seed, redraw the drafts from
+    # p_hat and run the sampler; mean accepted drafts per sequence
+    acc = None
+    if not args.gumbel_drafts and args.acc_seeds > 0:
+        dacc = StepBuffers(inp, api)
+        tot = 0.0
+        for sd in range(args.acc_seeds):
+            draw_drafts_on_device(torch, api, dacc, inp, seed=1000 + sd)
+            dacc.sample.seed = 1000 + sd
+            api.spec_reject_sample(dacc.sample, dacc.ws)
+            tot += float(dacc.num_accepted.float().mean())
+        acc = {"measured_accepted_per_seq": tot / args.acc_seeds, "seeds": args.acc_seeds,
+               "drafts": "drawn from p_hat per seed (Philox stream 1)"}
+
+    padded = None
+    if args.padded:
+        Lmax, Kmax = int(np.max(inp["kv_len"])), int(np.max(np.diff(inp["cu_q"]))) - 1
+        wp = W.workload(args.workload, **dict(over, L_dist="fixed", L_fixed=(Lmax,) * w.B,
+                                              K_lo=Kmax, K_hi=Kmax, K_fixed=(Kmax,) * w.B))
+        inp_p = W.make_inputs(wp)
+        inp_p["seq_ids"] = inp_p["seq_ids"] + lo
+        sets_p = [StepBuffers(inp_p, api) for _ in range(args.sets)]
+        if not args.gumbel_drafts:
+            for d in sets_p:
+                draw_drafts_on_device(torch, api, d, inp_p)
+        for k in range(3):
+            step(sets_p[k % len(sets_p)])
+        ms_p, n_p, _ = timed_replays(torch, sets_p, step, args.steps, stream, dist, shard,
+                                     args.no_graph, False)
+        bytes_p = W.padded_step_bytes(inp)["total"]
+        padded = {"ms_per_step": ms_p / n_p, "steps": n_p, "step_bytes": bytes_p,
+                  "padding_free_ms_per_step": per_step_ms,
+                  "padding_free_step_bytes": step_total,
+                  "time_ratio": (ms_p / n_p) / per_step_ms, "bytes_ratio": bytes_p / step_total,
+                  "how": f"the same shapes with every cache at the longest ({Lmax}) and every "
+                         f"block at the largest K ({Kmax}); the fused step timed on it"}
+        del sets_p
+
+    cpu = cpu_all = oracle_agree = ties = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp)
+        inp_o = dict(inp)
+        drafts_tied = set()
+        if not args.gumbel_drafts:
+            inp_o["draft_tokens"], drafts_tied = oracle_drafts(inp)
+        oracle_agree, ties = oracle_check(inp_o, inp["draft_tokens"], drafts_tied,
+                                          sets[0].num_accepted.cpu().numpy(),
+                                          sets[0].out_tokens.cpu().numpy())
+        if acc is not None:
+            acc["closed_form_accepted_per_seq"] = acceptance_closed_form(inp_o)
+        cpu = cpu_baseline(inp_o)
+        cpu_all = cpu_baseline_all_cores(sys.argv[1:])
 
     if rank == 0:
         line = {
@@ -577,10 +794,17 @@ def main():
                          "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["attention"],
                          "avg_launch_us": attn_us, "kernel_src": sha},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,
             "e2e_serial": e2e_serial,
             "gpu_launches": kernels_per_step(w) * n_steps,
             "clocks": clocks,
+            "drafts": "Gumbel-max stand-in" if args.gumbel_drafts else
+                      "drawn from p_hat on the device (spec_draft_sample, Philox stream 1)",
+            "acceptance": acc,
+            "oracle_check": oracle_agree,
+            "ties": ties,
+            "padded": padded,
         }
         print(json.dumps(line), flush=True)
     if dist:

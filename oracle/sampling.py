@@ -169,7 +169,8 @@ def process_row(logits, temperature, top_p, top_k=0, alt=False):
     k = int(np.argmax(M >= tp)) if np.any(M >= tp) else vals.shape[0] - 1
     tau = vals[k]
     above = M[k] - tp
-    below = tp - (M[k - 1] if k > 0 else 0.0)
+    # the mass above the top class is exactly 0 on every path: no tie there
+    below = tp - M[k - 1] if k > 0 else np.inf
     if alt and min(abs(above), abs(below)) < NUCLEUS_TIE_EPS:
         if abs(above) <= abs(below) and k + 1 < vals.shape[0]:
             tau = vals[k + 1]

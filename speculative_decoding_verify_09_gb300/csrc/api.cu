@@ -199,7 +199,7 @@ Layout layout(const sv_attn_args *a, const sv_sample_args *s) {
     L.parts = off;
     off += round_up(rows * L.splan.stat_chunks * sizeof(sv::ChunkPart));
     L.draw_parts = off;
-    off += round_up(static_cast<size_t>(s->batch) * L.splan.draw_chunks * 8);
+    off += round_up(static_cast<size_t>(s->batch) * L.splan.draw_chunks * 16);
   }
   if (a) {
     // size the partials for the largest grids any device could get
@@ -323,7 +323,7 @@ sv::SamplerLaunch sampler_launch(const sv_sample_args *sample, const Layout &L, 
   SL.ws.seq_cnt1 = at<uint32_t>(ws, L.seq_cnt1);
   SL.ws.seq_cnt2 = at<uint32_t>(ws, L.seq_cnt2);
   SL.ws.parts = at<sv::ChunkPart>(ws, L.parts);
-  SL.ws.draw_parts = at<unsigned long long>(ws, L.draw_parts);
+  SL.ws.draw_parts = at<unsigned __int128>(ws, L.draw_parts);
   return SL;
 }
 

@@ -23,6 +23,8 @@ struct RowStats {
   int32_t amax;       // greedy row (temperature 0): index of the one-hot; else -1
   float c_hi, c_lo;   // log2(e) / T of the row's sequence as a float pair
   double ssum;        // sum over the kept set of exp((l - lmax) / T)
+  float acc_hi, acc_lo;   // the same sum from float-float weights (~1e-13), for residuals
+  float it_hi, it_lo;     // 1 / T of the row's sequence as a float pair
 };
 
 // Partial (max, sum) of one chunk of a row (chunked statistics).
@@ -30,6 +32,7 @@ struct ChunkPart {
   float m;            // chunk max
   float s_hi, s_lo;   // sum of exp((l - m) / T) over the chunk, float-float
   uint32_t bad;       // NaN / +inf seen
+  float a_hi, a_lo;   // the same sum from float-float weights
 };
 
 // Sampler workspace regions (device pointers).
@@ -39,7 +42,7 @@ struct SamplerWs {
   uint32_t *seq_cnt1;       // [B] row arrivals per sequence (zero between calls)
   uint32_t *seq_cnt2;       // [B] draw-chunk arrivals per sequence (zero between calls)
   ChunkPart *parts;         // [(2R - B) * stat_chunks]
-  unsigned long long *draw_parts;   // [B * draw_chunks]
+  unsigned __int128 *draw_parts;    // [B * draw_chunks] fixed-point (2^-116) chunk sums
 };
 
 struct SamplerPlan {

@@ -29,6 +29,7 @@
 // index does not depend on the summation order.  The near-tie windows of the
 // decisions (1e-5) are far wider than these errors.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -90,6 +91,19 @@ __device__ __forceinline__ void unpack(const uint4 raw, uint32_t (&b)[LT<T>::EPV
       b[2 * i] = w[i] & 0xFFFFu;
       b[2 * i + 1] = w[i] >> 16;
     }
+  }
+}
+
+// Bits of element e (0 <= e < EPV) of a loaded vector, without indexing a
+// local array (a dynamic index would move the vector to local memory).
+template <typename T>
+__device__ __forceinline__ uint32_t elem_bits(const uint4 raw, int e) {
+  if constexpr (LT<T>::EPV == 4) {
+    return e < 2 ? (e == 0 ? raw.x : raw.y) : (e == 2 ? raw.z : raw.w);
+  } else {
+    const int q = e >> 1;
+    const uint32_t w = q < 2 ? (q == 0 ? raw.x : raw.y) : (q == 2 ? raw.z : raw.w);
+    return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
   }
 }
 
@@ -211,8 +225,10 @@ struct SampParams {
   int do_append;
   AppendView app;
   float c_hi, c_lo;   // log2(e)/T as two floats
+  float it_hi, it_lo; // 1/T as two floats
   int pdl_secondary;  // launched early behind another grid (see PdlTail)
   uint32_t stream;    // Philox counter word 3: 0 verify, 1 draft-token draws
+  float2 exp2tab[kExp2Tab];   // 2^(j/64), j = -32..32, float-float (exp2_ff)
 };
 
 // A launch that may start before the previous grid on its stream has finished
@@ -226,6 +242,8 @@ struct PdlTail {
 };
 
 struct SampSmem {
+  float2 exp2tab[kExp2Tab];   // 2^(j/64) as float-float (accurate kept-set sums)
+  float tconst[4];            // log2(e)/T and 1/T of the row, float pairs
   FF red[2][8 * kSampNW];     // double-buffered float-float partials
   float redf[32];
   unsigned long long red64[32];
@@ -508,20 +526,33 @@ __device__ __forceinline__ float row_prob(const RowProb &rp, uint32_t bits, int 
   return __fmaf_rn(w, rp.inv_hi, __fmul_rn(w, rp.inv_lo));
 }
 
-// Fixed-point (2^-52) draw weight of vocabulary index x: mode 0 the residual
-// max(0, q_hat - p_hat), mode 1 q_hat.
-template <typename T>
-__device__ __forceinline__ unsigned long long fix_weight(const RowProb &pq, const RowProb &pp,
-                                                         int mode, uint32_t bq, uint32_t bp, int x) {
-  float r = row_prob<T>(pq, bq, x);
-  if (mode == 0) r = fmaxf(__fsub_rn(r, row_prob<T>(pp, bp, x)), 0.0f);
-  return fix52(r);
-}
+// Draw weight of vocabulary index x: mode 0 the residual max(0, q_hat -
+// p_hat) (with relative accuracy, see ResidualFn; exact 0 / 1 differences for
+// greedy one-hot rows), mode 1 q_hat.
+struct DrawWeight {
+  RowProb pq, pp;
+  ResidualFn rf;
+  int mode;
+  bool onehot;
+  template <typename T>
+  __device__ __forceinline__ float w(uint32_t bq, uint32_t bp, int x) const {
+    if (mode != 0) return row_prob<T>(pq, bq, x);
+    if (onehot) return fmaxf(__fsub_rn(row_prob<T>(pq, bq, x), row_prob<T>(pp, bp, x)), 0.0f);
+    const float lq = LT<T>::key(bq) < pq.tau ? -INFINITY : LT<T>::val(bq);
+    const float lp = LT<T>::key(bp) < pp.tau ? -INFINITY : LT<T>::val(bp);
+    return rf(lq, lp);
+  }
+  template <typename T>
+  __device__ __forceinline__ u128 fix(uint32_t bq, uint32_t bp, int x) const {
+    return fix116(w<T>(bq, bp, x));
+  }
+};
 
 // Finish a row's statistics (one thread): ssum and its float-float inverse,
 // the row's log2(e)/T constant and, for a greedy row, its argmax.
 __device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t tau, bool valid,
-                                            double ssum, float c_hi, float c_lo, int amax) {
+                                            double ssum, float c_hi, float c_lo, int amax,
+                                            FF acc, float it_hi, float it_lo) {
   RowStats o;
   o.lmax = lmax;
   o.tau_key = tau;
@@ -533,6 +564,10 @@ __device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t t
   o.c_hi = c_hi;
   o.c_lo = c_lo;
   o.ssum = ssum;
+  o.acc_hi = acc.hi;
+  o.acc_lo = acc.lo;
+  o.it_hi = it_hi;
+  o.it_lo = it_lo;
   *st = o;
 }
 
@@ -637,8 +672,10 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
   constexpr int EPV = LT<T>::EPV;
   constexpr int NW = kStatNT / 32;
   __shared__ float redf[NW];
-  __shared__ FF redff[NW];
+  __shared__ FF redff[NW], redacc[NW];
+  __shared__ float2 tab[kExp2Tab];
   __shared__ int flag[2];
+  exp2_table_fill(tab, P.exp2tab);
   const sv_sample_args &a = P.a;
   const int NCH = P.plan.stat_chunks;
   const int r = blockIdx.x / NCH, c = blockIdx.x - r * NCH;
@@ -696,14 +733,18 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
   for (int k = 1; k < NW; ++k) mx = fmaxf(mx, redf[k]);
   // chunk sum of exp((l - mx)/T), Kahan per thread, float-float across threads
   const WeightFn wf{mx, P.c_hi, P.c_lo};
+  const FF cc{P.c_hi, P.c_lo};
   float sum = 0.0f, comp = 0.0f;
+  FF acc = ff_make(0.0f);
   auto kahan = [&](const uint32_t (&b)[EPV]) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
-      const float y = __fsub_rn(wf(LT<T>::val(b[e])), comp);
+      const float l = LT<T>::val(b[e]);
+      const float y = __fsub_rn(wf(l), comp);
       const float t = __fadd_rn(sum, y);
       comp = __fsub_rn(__fsub_rn(t, sum), y);
       sum = t;
+      if (l != -INFINITY) acc = ff_add(acc, exp2_ff(ff_mul(two_sum(l, -mx), cc), tab));
     }
   };
   if (mx > -INFINITY) {
@@ -722,16 +763,25 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
     }
   }
   FF f = warp_sum_ff(FF{sum, -comp});
-  if (l == 0) redff[w] = f;
+  acc = warp_sum_ff(acc);
+  if (l == 0) {
+    redff[w] = f;
+    redacc[w] = acc;
+  }
   __syncthreads();
   if (tid == 0) {
-    FF t = redff[0];
-    for (int k = 1; k < NW; ++k) t = ff_add(t, redff[k]);
+    FF t = redff[0], ta = redacc[0];
+    for (int k = 1; k < NW; ++k) {
+      t = ff_add(t, redff[k]);
+      ta = ff_add(ta, redacc[k]);
+    }
     ChunkPart cp;
     cp.m = mx;
     cp.s_hi = t.hi;
     cp.s_lo = t.lo;
     cp.bad = bad ? 1u : 0u;
+    cp.a_hi = ta.hi;
+    cp.a_lo = ta.lo;
     P.ws.parts[static_cast<int64_t>(r) * NCH + c] = cp;
     __threadfence();
     const unsigned old = atomicInc(&P.ws.row_cnt[r], static_cast<unsigned>(NCH - 1));
@@ -745,7 +795,7 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
         M = fmaxf(M, __ldcg(&parts[k].m));
         anybad |= __ldcg(&parts[k].bad);
       }
-      FF S = ff_make(0.0f);
+      FF S = ff_make(0.0f), A = ff_make(0.0f);
       if (M > -INFINITY) {
         const WeightFn sc{M, P.c_hi, P.c_lo};
         for (int k = 0; k < NCH; ++k) {
@@ -754,10 +804,13 @@ __global__ void __launch_bounds__(kStatNT) stats_chunk_kernel(const SampParams P
           const float f = sc(qm);                        // exp((m_k - M)/T)
           S = ff_add(S, ff_add(FF{__fmul_rn(__ldcg(&parts[k].s_hi), f), 0.0f},
                                FF{__fmul_rn(__ldcg(&parts[k].s_lo), f), 0.0f}));
+          const FF fa = exp2_ff(ff_mul(two_sum(qm, -M), cc), tab);
+          A = ff_add(A, ff_mul(FF{__ldcg(&parts[k].a_hi), __ldcg(&parts[k].a_lo)}, fa));
         }
       }
       const bool valid = !anybad && M > -INFINITY;
-      write_stats(&P.ws.stats[r], M, 0u, valid, ff_to_double(S), P.c_hi, P.c_lo, -1);
+      write_stats(&P.ws.stats[r], M, 0u, valid, ff_to_double(S), P.c_hi, P.c_lo, -1, A, P.it_hi,
+                  P.it_lo);
     }
   }
   __syncthreads();
@@ -786,6 +839,7 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
   }
   const T *row = static_cast<const T *>(base) + off;
   constexpr int EPV = LT<T>::EPV;
+  exp2_table_fill(sm.exp2tab, P.exp2tab);
   RowPass<T> rp;
   rp.init(row, a.vocab, reinterpret_cast<uint4 *>(smem_raw + kSmemRowOff));  // the one HBM read
   float mx = -INFINITY;
@@ -809,7 +863,8 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
   const bool valid = param_ok && !bad && mx > -INFINITY;
   uint32_t tau = 0;
   double ssum = 0.0;
-  float c_hi = 0.0f, c_lo = 0.0f;
+  FF acc = ff_make(0.0f);
+  float c_hi = 0.0f, c_lo = 0.0f, it_hi = 0.0f, it_lo = 0.0f;
   int amax = -1;
   if (valid && Tr == 0.0f) {
     // greedy: one-hot at the lowest index holding the maximum
@@ -823,9 +878,19 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
     amax = static_cast<int>(-block_max_f<kSampNT>(first, sm.redf));
     ssum = 1.0;
   } else if (valid) {
-    const double c = 1.4426950408889634 / static_cast<double>(Tr);
-    c_hi = static_cast<float>(c);
-    c_lo = static_cast<float>(c - static_cast<double>(c_hi));
+    if (tid == 0) {                   // fp64 once per CTA
+      const double c = 1.4426950408889634 / static_cast<double>(Tr);
+      const double it = 1.0 / static_cast<double>(Tr);
+      sm.tconst[0] = static_cast<float>(c);
+      sm.tconst[1] = static_cast<float>(c - static_cast<double>(sm.tconst[0]));
+      sm.tconst[2] = static_cast<float>(it);
+      sm.tconst[3] = static_cast<float>(it - static_cast<double>(sm.tconst[2]));
+    }
+    __syncthreads();
+    c_hi = sm.tconst[0];
+    c_lo = sm.tconst[1];
+    it_hi = sm.tconst[2];
+    it_lo = sm.tconst[3];
     const WeightFn wf{mx, c_hi, c_lo};
     uint32_t kmin = 0;
     if (tkr > 0 && tkr < a.vocab) kmin = topk_key<T>(rp, tkr, sm);
@@ -848,8 +913,23 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
       tau = kmin;
       ssum = ff_to_double(S[0]);
     }
+    // the kept set's sum again from float-float weights (residual draws)
+    const FF cc{c_hi, c_lo};
+    FF acc1 = ff_make(0.0f);
+    rp.each([&](const uint32_t (&bits)[EPV]) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float l = LT<T>::val(bits[e]);
+        if (LT<T>::key(bits[e]) >= tau && l != -INFINITY)
+          acc1 = ff_add(acc1, exp2_ff(ff_mul(two_sum(l, -mx), cc), sm.exp2tab));
+      }
+    });
+    FF A1[1] = {acc1};
+    __syncthreads();
+    block_sum_ff<1>(A1, sm.red[0]);
+    acc = A1[0];
   }
-  if (tid == 0) write_stats(&P.ws.stats[r], mx, tau, valid, ssum, c_hi, c_lo, amax);
+  if (tid == 0) write_stats(&P.ws.stats[r], mx, tau, valid, ssum, c_hi, c_lo, amax, acc, it_hi, it_lo);
   arrive_sequence<T>(P, i, &sm.bcast[3]);
 }
 
@@ -864,20 +944,22 @@ constexpr int kDrawNT = 256;
 constexpr int kDrawVec = 2;          // contiguous vectors per thread in the walk
 
 struct DrawSmem {
-  unsigned long long red[kDrawNT / 32];
-  unsigned long long bc64[2];
+  u128 red[kDrawNT / 32];
+  u128 bc128[2];
+  FF L;
+  float inv_sq;
   int bc[4];
 };
 
-// Sum of the chunk's fixed-point weights (block-wide, all threads get it).
+// Sum of the chunk's fixed-point draw weights (block-wide, all threads get it).
 template <typename T>
-__device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int v0, int v1,
-                                        const RowProb &pq, const RowProb &pp, int mode,
-                                        DrawSmem &sm) {
+__device__ u128 chunk_sum(const T *trow, const T *drow, int V, int v0, int v1,
+                          const DrawWeight &dw, DrawSmem &sm) {
   constexpr int EPV = LT<T>::EPV;
+  const bool two = dw.mode == 0;
   const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
-  const bool al_d = mode == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
-  unsigned long long s = 0;
+  const bool al_d = two && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  u128 s = 0;
   for (int vb = v0; vb < v1; vb += kDrawVec * kDrawNT) {
     uint4 q[kDrawVec], d[kDrawVec];
 #pragma unroll
@@ -885,7 +967,7 @@ __device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int
       const int v = vb + k * kDrawNT + threadIdx.x;
       if (v < v1) {
         q[k] = load_vec<T>(trow, V, v, al_t);
-        if (mode == 0) d[k] = load_vec<T>(drow, V, v, al_d);
+        if (two) d[k] = load_vec<T>(drow, V, v, al_d);
       }
     }
 #pragma unroll
@@ -894,21 +976,13 @@ __device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int
       if (v < v1) {
         uint32_t bq[EPV], bd[EPV];
         unpack<T>(q[k], bq);
-        if (mode == 0) unpack<T>(d[k], bd);
+        if (two) unpack<T>(d[k], bd);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[e], mode == 0 ? bd[e] : 0u, v * EPV + e);
+        for (int e = 0; e < EPV; ++e) s += dw.fix<T>(bq[e], two ? bd[e] : 0u, v * EPV + e);
       }
     }
   }
-  s = warp_sum_u64(s);
-  const int w = threadIdx.x >> 5;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sm.red[w] = s;
-  __syncthreads();
-  unsigned long long t = 0;
-#pragma unroll
-  for (int k = 0; k < kDrawNT / 32; ++k) t += sm.red[k];
-  return t;
+  return block_sum_u128<kDrawNT>(s, sm.red);
 }
 
 // Index of the first element of vectors [v0, v1) whose running weight sum,
@@ -916,33 +990,33 @@ __device__ unsigned long long chunk_sum(const T *trow, const T *drow, int V, int
 // owns kDrawVec contiguous vectors, so thread order is vocabulary order.
 template <typename T>
 __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
-                          const RowProb &pq, const RowProb &pp, int mode,
-                          unsigned long long tgt, DrawSmem &sm, unsigned long long *scan_red) {
+                          const DrawWeight &dw, u128 tgt, DrawSmem &sm, u128 *scan_red) {
   constexpr int EPV = LT<T>::EPV;
+  const bool two = dw.mode == 0;
   const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
-  const bool al_d = mode == 0 && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  const bool al_d = two && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
   const int tid = threadIdx.x;
   int result = -1;
   if (tid == 0) sm.bc[0] = -1;
-  unsigned long long base = 0;
+  u128 base = 0;
   for (int vb = v0; vb < v1; vb += kDrawVec * kDrawNT) {
     const int va = vb + tid * kDrawVec;
     uint32_t bq[kDrawVec][EPV], bd[kDrawVec][EPV];
-    unsigned long long s = 0;
+    u128 s = 0;
 #pragma unroll
     for (int k = 0; k < kDrawVec; ++k) {
       if (va + k < v1) {
         unpack<T>(load_vec<T>(trow, V, va + k, al_t), bq[k]);
-        if (mode == 0) unpack<T>(load_vec<T>(drow, V, va + k, al_d), bd[k]);
+        if (two) unpack<T>(load_vec<T>(drow, V, va + k, al_d), bd[k]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) s += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u, (va + k) * EPV + e);
+        for (int e = 0; e < EPV; ++e) s += dw.fix<T>(bq[k][e], two ? bd[k][e] : 0u, (va + k) * EPV + e);
       }
     }
-    unsigned long long total;
-    const unsigned long long ex = block_exclusive_scan_u64<kDrawNT>(s, scan_red, &total);
-    const unsigned long long lo = base + ex;
+    u128 total;
+    const u128 ex = block_exclusive_scan_u128<kDrawNT>(s, scan_red, &total);
+    const u128 lo = base + ex;
     if (s > 0 && lo <= tgt && tgt < lo + s) {
-      unsigned long long c = lo;
+      u128 c = lo;
       int x = (va + kDrawVec) * EPV - 1;
       bool found = false;
 #pragma unroll
@@ -950,7 +1024,7 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           if (!found && va + k < v1) {
-            c += fix_weight<T>(pq, pp, mode, bq[k][e], mode == 0 ? bd[k][e] : 0u, (va + k) * EPV + e);
+            c += dw.fix<T>(bq[k][e], two ? bd[k][e] : 0u, (va + k) * EPV + e);
             if (c > tgt) { x = (va + k) * EPV + e; found = true; }
           }
         }
@@ -967,7 +1041,7 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 template <typename T>
 __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   __shared__ DrawSmem sm;
-  __shared__ unsigned long long scan_red[kDrawNT / 32];
+  __shared__ u128 scan_red[kDrawNT / 32];
   const sv_sample_args &a = P.a;
   const int NCH = P.plan.draw_chunks;
   const int i = blockIdx.x / NCH, c = blockIdx.x - i * NCH;
@@ -1025,12 +1099,33 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const T *trow = static_cast<const T *>(a.target_logits) + static_cast<int64_t>(r0 + n) * V;
   const T *drow = mode == 0 ? static_cast<const T *>(a.draft_logits) + static_cast<int64_t>(p0 + n) * V
                             : trow;
-  const RowProb pq = rowprob_of(&P.ws.stats[r0 + n]);
-  const RowProb pp = mode == 0 ? rowprob_of(&P.ws.stats[R + p0 + n]) : pq;
+  const RowStats *sq = &P.ws.stats[r0 + n];
+  const RowStats *sp = &P.ws.stats[R + p0 + n];
+  DrawWeight dw;
+  dw.pq = rowprob_of(sq);
+  dw.pp = mode == 0 ? rowprob_of(sp) : dw.pq;
+  dw.mode = mode;
+  dw.onehot = dw.pq.amax >= 0 || dw.pp.amax >= 0;
+  dw.rf.init(__ldcg(&sq->lmax), mode == 0 ? __ldcg(&sp->lmax) : 0.0f, __ldcg(&sq->c_hi),
+             __ldcg(&sq->c_lo), FF{__ldcg(&sq->it_hi), __ldcg(&sq->it_lo)},
+             __ldcg(&sq->it_hi) == 1.0f && __ldcg(&sq->it_lo) == 0.0f, sizeof(T) == 4);
+  if (mode == 0 && !dw.onehot) {
+    if (tid == 0) {                   // fp64 once per CTA, not per thread
+      const FF aq{__ldcg(&sq->acc_hi), __ldcg(&sq->acc_lo)};
+      const FF ap{__ldcg(&sp->acc_hi), __ldcg(&sp->acc_lo)};
+      sm.L = ln_ratio_ff(ap, aq);
+      sm.inv_sq = static_cast<float>(1.0 / ff_to_double(aq));
+    }
+    __syncthreads();
+    dw.rf.L = sm.L;
+    dw.rf.inv_sq = sm.inv_sq;
+  }
+  DrawWeight dq = dw;                 // q_hat of row n (empty-residual fallback)
+  dq.mode = 1;
   const int NV = (V + EPV - 1) / EPV;
   const int per = (NV + NCH - 1) / NCH;
   const int v0 = min(NV, c * per), v1 = min(NV, v0 + per);
-  const unsigned long long cs = chunk_sum<T>(trow, drow, V, v0, v1, pq, pp, mode, sm);
+  const u128 cs = chunk_sum<T>(trow, drow, V, v0, v1, dw, sm);
   if (tid == 0) {
     P.ws.draw_parts[static_cast<int64_t>(i) * NCH + c] = cs;
     __threadfence();
@@ -1050,19 +1145,19 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   int use_mode = mode;
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (tid == 0) {
-      unsigned long long Z = 0;
+      u128 Z = 0;
       if (attempt == 0) {
-        for (int k = 0; k < NCH; ++k) Z += __ldcg(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
+        for (int k = 0; k < NCH; ++k) Z += ldcg_u128(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
       }
-      sm.bc64[0] = Z;
+      sm.bc128[0] = Z;
     }
     __syncthreads();
-    unsigned long long Z = sm.bc64[0];
+    u128 Z = sm.bc128[0];
     if (attempt == 1) {            // fallback: q_hat of row n, chunk sums computed here
       Z = 0;
       for (int k = 0; k < NCH; ++k) {
         const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
-        Z += chunk_sum<T>(trow, trow, V, a0, a1, pq, pq, 1, sm);
+        Z += chunk_sum<T>(trow, trow, V, a0, a1, dq, sm);
       }
     }
     if (Z == 0) {
@@ -1074,25 +1169,25 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
       if (tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: cannot happen for a valid row
       return;
     }
-    const unsigned long long tgt = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);   // floor(k*Z/2^24)
+    const u128 tgt = scale_u24(ku, Z);          // floor(k * Z / 2^24)
     // locate the chunk (chunk sums recomputed in the fallback)
-    unsigned long long cum = 0;
+    u128 cum = 0;
     int cstar = NCH - 1;
     for (int k = 0; k < NCH; ++k) {
-      unsigned long long zk;
+      u128 zk;
       if (use_mode == mode) {
-        zk = __ldcg(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
+        zk = ldcg_u128(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
       } else {
         const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
-        zk = chunk_sum<T>(trow, trow, V, a0, a1, pq, pq, 1, sm);
+        zk = chunk_sum<T>(trow, trow, V, a0, a1, dq, sm);
       }
       if (tgt < cum + zk) { cstar = k; break; }
       cum += zk;
     }
     const int a0 = min(NV, cstar * per), a1 = min(NV, a0 + per);
     const int x = use_mode == mode
-                      ? chunk_walk<T>(trow, drow, V, a0, a1, pq, pp, mode, tgt - cum, sm, scan_red)
-                      : chunk_walk<T>(trow, trow, V, a0, a1, pq, pq, 1, tgt - cum, sm, scan_red);
+                      ? chunk_walk<T>(trow, drow, V, a0, a1, dw, tgt - cum, sm, scan_red)
+                      : chunk_walk<T>(trow, trow, V, a0, a1, dq, tgt - cum, sm, scan_red);
     if (tid == 0) a.out_tokens[r0 + n] = x;
     return;
   }
@@ -1139,9 +1234,16 @@ struct ClusterSmem {
   int dtok[kMaxRows];
   float redm[kMaxRows][kClNW], reds[kMaxRows][kClNW];
   uint32_t redb[kMaxRows][kClNW];
-  unsigned long long tot[2];                         // slice totals of the two run sums
-  unsigned long long scan_red[kClNW];
-  unsigned long long dec_local;                      // target inside this slice (owner only)
+  u128 tot[2];                                       // slice totals of the sums A and B
+  u128 scan_red[kClNW];
+  u128 dec_pa, dec_pb;                               // prefix of the owner slice
+  FF dec_L;                                          // exact ln(S_p / S_q) (recut pass)
+  i128 dec_tg;                                       // the target, in units of A + beta B
+  long long dec_beta;                                // beta * 2^56
+  FF ssum[2];                                        // slice float-float sums (C1)
+  FF redff[2][kClNW];
+  FF Lr;                                             // ln(S_p / S_q) of rows n
+  int walker;                                        // thread whose run holds the target
   uint32_t draw_u24[kMaxQRows];                      // draw uniform if n = index
   int dec_use, dec_owner;
   int n;
@@ -1436,106 +1538,228 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   }
   const int mode = n < K ? 0 : 1;
   const int qt = n, qd = K + 1 + n;                 // target row n, draft row n
-  const float mq_ = sm.st_m[qt], iq = sm.st_inv[qt];
-  const float mp_ = mode == 0 ? sm.st_m[qd] : 0.0f, ip = mode == 0 ? sm.st_inv[qd] : 0.0f;
-  auto qhat = [&](uint32_t b) { return __fmul_rn(ex2c(LT<T>::val(b) - mq_), iq); };
-  auto phat = [&](uint32_t b) { return __fmul_rn(ex2c(LT<T>::val(b) - mp_), ip); };
+  const float mq_ = sm.st_m[qt];
   const int vpt = (per + kClNT - 1) / kClNT;        // vectors per run
   const int ra = min(nv, tid * vpt), rb = min(nv, ra + vpt);
   const T *rq = row_ptr(qt), *rd = row_ptr(qd);
   const bool alq = (reinterpret_cast<uintptr_t>(rq) & 15) == 0;
   const bool ald = (reinterpret_cast<uintptr_t>(rd) & 15) == 0;
-  unsigned long long s0 = 0, s1 = 0;
-  for (int v = ra; v < rb; ++v) {
-    uint32_t bq[EPV], bd[EPV];
-    unpack<T>(load_vec<T>(rq, V, v0 + v, alq), bq);
-    if (mode == 0) unpack<T>(load_vec<T>(rd, V, v0 + v, ald), bd);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      const float qh = qhat(bq[e]);
-      s1 += fix52(qh);
-      if (mode == 0) s0 += fix52(fmaxf(__fsub_rn(qh, phat(bd[e])), 0.0f));
+  ResidualFn rf;
+  rf.init(mq_, mode == 0 ? sm.st_m[qd] : 0.0f, P.c_hi, P.c_lo, FF{P.it_hi, P.it_lo},
+          P.it_hi == 1.0f && P.it_lo == 0.0f, sizeof(T) == 4);
+  rf.inv_sq = sm.st_inv[qt];
+  const float ip = mode == 0 ? sm.st_inv[qd] : 0.0f;
+  // ---- C (one pass): the draw weights of row n as two exact fixed-point sums
+  // A and B, combined as A + beta * B once beta is known.
+  //  * bonus draw, or the empty-residual fallback (use 1): A = q_hat, beta = 0;
+  //  * after a rejection (use 0): with L0 = ln(S_p / S_q) from the fp32 sums,
+  //    A = q_hat max(0, -expm1(t - L0)) and B = q_hat exp(t - L0) [t < L0]
+  //    (q_hat and 0 where p_hat = 0 or q_hat = 0, see ResidualFn), and
+  //      G = sum_x q_hat_x expm1(t_x - L0) + sum_{x: q_hat_x = 0} p_hat_x
+  //        = (S_p / S_q) exp(-L0) - 1,
+  //    a small number (L0 is close) known to a small fraction of the residual
+  //    mass itself (summed in float-float).  The exact L satisfies
+  //    exp(L - L0) = 1 + G, so where t < L0 the residual at L is
+  //    q_hat (1 - exp(t - L0) / (1 + G)) = A + beta * B, beta = G / (1 + G);
+  //    only tokens with t between L0 and L (a band of width |L - L0| ~ 1e-6)
+  //    are off, by at most q_hat |L - L0|.
+  // A + beta * B is evaluated in 128-bit integers from the prefix sums at
+  // every decision point, the same function of the same integers everywhere,
+  // so the slice, thread and token searches agree.
+  const float L0 = mode == 0 ? logf(__fdividef(rf.inv_sq, ip)) : 0.0f;
+  rf.L = FF{L0, 0.0f};
+  const float mp_ = rf.mp;
+  // use 0: the one-pass sums above (and the distances dneg / dpos of the
+  // nearest t - L0 below / at-or-above 0, which tell whether the exact L cuts
+  // the tokens where L0 did); use 2: the residual at the exact L directly
+  // (beta = 0), when it does not; use 1: q_hat.
+  float dneg = INFINITY, dpos = INFINITY;
+  auto weights = [&](int use, uint32_t bq, uint32_t bd, u128 &wa, u128 &wb, float &gterm) {
+    const float lq = LT<T>::val(bq);
+    wa = 0;
+    wb = 0;
+    gterm = 0.0f;
+    if (use == 1) {
+      wa = fix116(rf.qhat(lq));
+      return;
     }
-  }
-  if (mode != 0) s0 = s1;
-  unsigned long long z0, z1;
-  const unsigned long long ex0 = block_exclusive_scan_u64<kClNT>(s0, sm.scan_red, &z0);
-  __syncthreads();
-  const unsigned long long ex1 = block_exclusive_scan_u64<kClNT>(s1, sm.scan_red, &z1);
-  if (tid == 0) {
-    sm.tot[0] = z0;
-    sm.tot[1] = z1;
-  }
-  cluster_sync_all();                              // (2) slice totals visible
-
-  // ---- phase D: locate the target among the slices; the owner walks its run
-  if (w == 0) {
-    unsigned long long t0 = 0, t1 = 0;
-    if (l < C) {
-      t0 = *dsmem(&sm.tot[0], l);
-      t1 = *dsmem(&sm.tot[1], l);
+    const float lp = LT<T>::val(bd);
+    if (use == 2) {
+      wa = fix116(rf(lq, lp));
+      return;
     }
-    unsigned long long c0 = t0, c1 = t1;           // inclusive prefix over slices
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y0 = __shfl_up_sync(0xffffffffu, c0, o);
-      const unsigned long long y1 = __shfl_up_sync(0xffffffffu, c1, o);
-      if (l >= o) {
-        c0 += y0;
-        c1 += y1;
+    if (lq == -INFINITY) {
+      if (lp != -INFINITY) gterm = __fmul_rn(ex2c(lp - mp_), ip);
+      return;
+    }
+    const float qh = rf.qhat(lq);
+    if (lp == -INFINITY) {
+      wa = fix116(qh);
+      gterm = -qh;
+      return;
+    }
+    const float d = rf.arg(lq, lp, rf.L);
+    const float em = expm1_fast(d);
+    gterm = __fmul_rn(qh, em);
+    if (d < 0.0f) {
+      wa = fix116(-gterm);
+      wb = fix116(__fmaf_rn(qh, em, qh));
+      dneg = fminf(dneg, -d);
+    } else {
+      dpos = fminf(dpos, d);
+    }
+  };
+  FF rf_L_exact = FF{0.0f, 0.0f};
+  int use = mode;
+  for (int round = 0; round < 3; ++round) {
+    u128 sa = 0, sb = 0;
+    FF g = ff_make(0.0f);
+    for (int v = ra; v < rb; ++v) {
+      const uint4 xq = load_vec<T>(rq, V, v0 + v, alq);
+      const uint4 xd = use != 1 ? load_vec<T>(rd, V, v0 + v, ald) : xq;
+#pragma unroll 1
+      for (int e = 0; e < EPV; ++e) {
+        u128 wa, wb;
+        float gt;
+        weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), wa, wb, gt);
+        sa += wa;
+        sb += wb;
+        g = ff_add(g, ff_make(gt));
       }
     }
-    const unsigned long long Z0 = __shfl_sync(0xffffffffu, c0, 31);
-    const unsigned long long Z1 = __shfl_sync(0xffffffffu, c1, 31);
-    const unsigned long long pre0 = __shfl_sync(0xffffffffu, c0 - t0, static_cast<int>(k));
-    const unsigned long long pre1 = __shfl_sync(0xffffffffu, c1 - t1, static_cast<int>(k));
-    if (l == 0) {
-      int use = mode;
-      if (use == 0 && Z0 == 0) {                   // rejected, empty residual: draw from q_hat
-        use = 1;
-        if (k == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+    u128 ta, tb;
+    const u128 exa = block_exclusive_scan_u128<kClNT>(sa, sm.scan_red, &ta);
+    __syncthreads();
+    const u128 exb = use == 0 ? block_exclusive_scan_u128<kClNT>(sb, sm.scan_red, &tb)
+                              : static_cast<u128>(0);
+    if (use == 0) {
+      g = warp_sum_ff(g);
+      dneg = warp_min(dneg);
+      dpos = warp_min(dpos);
+      if (l == 0) {
+        sm.redff[0][w] = g;
+        sm.redff[1][w] = FF{dneg, dpos};
       }
-      const unsigned long long Z = use == 0 ? Z0 : Z1;
-      const unsigned long long pre = use == 0 ? pre0 : pre1;
-      const unsigned long long mine = use == 0 ? sm.tot[0] : sm.tot[1];
-      int owner = 0;
-      unsigned long long local = 0;
-      if (Z == 0) {
-        if (k == 0) a.out_tokens[r0 + n] = -1;     // empty q_hat: cannot happen for a valid row
-      } else {
-        const unsigned long long ku = sm.draw_u24[n];
-        const unsigned long long tg = (__umul64hi(ku, Z) << 40) | ((ku * Z) >> 24);   // floor(k*Z/2^24)
-        owner = pre <= tg && tg < pre + mine;
-        local = tg - pre;
-      }
-      sm.dec_use = use;
-      sm.dec_owner = owner;
-      sm.dec_local = local;
+      __syncthreads();
     }
-  }
-  __syncthreads();
-  if (sm.dec_owner) {
-    const int use = sm.dec_use;
-    const unsigned long long local = sm.dec_local;
-    const unsigned long long ex = use == 0 ? ex0 : ex1, mine = use == 0 ? s0 : s1;
-    if (ex <= local && local < ex + mine) {
-      unsigned long long c = ex;
-      int x = -1;
-      for (int v = ra; v < rb && x < 0; ++v) {
-        uint32_t bq[EPV], bd[EPV];
-        unpack<T>(load_vec<T>(rq, V, v0 + v, alq), bq);
-        if (use == 0) unpack<T>(load_vec<T>(rd, V, v0 + v, ald), bd);
+    if (tid == 0) {
+      sm.tot[0] = ta;
+      sm.tot[1] = use == 0 ? tb : static_cast<u128>(0);
+      FF x = ff_make(0.0f), dd = FF{INFINITY, INFINITY};
+      if (use == 0) {
+        x = sm.redff[0][0];
+        dd = sm.redff[1][0];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          if (x < 0) {
-            const float qh = qhat(bq[e]);
-            c += use == 0 ? fix52(fmaxf(__fsub_rn(qh, phat(bd[e])), 0.0f)) : fix52(qh);
-            if (c > local) x = (v0 + v) * EPV + e;
-          }
+        for (int q = 1; q < kClNW; ++q) {
+          x = ff_add(x, sm.redff[0][q]);
+          dd = FF{fminf(dd.hi, sm.redff[1][q].hi), fminf(dd.lo, sm.redff[1][q].lo)};
         }
       }
-      a.out_tokens[r0 + n] = x;
+      sm.ssum[0] = x;
+      sm.ssum[1] = dd;
     }
+    cluster_sync_all();                            // (2) slice totals and G visible
+    // ---- D: every CTA finds the slice holding the target (warp 0)
+    if (w == 0) {
+      const u128 a0 = l < C ? *dsmem(&sm.tot[0], l) : static_cast<u128>(0);
+      const u128 b0 = l < C ? *dsmem(&sm.tot[1], l) : static_cast<u128>(0);
+      FF gl = l < C ? *dsmem(&sm.ssum[0], l) : ff_make(0.0f);
+      const FF dl = l < C ? *dsmem(&sm.ssum[1], l) : FF{INFINITY, INFINITY};
+      FF G = shfl_ff(gl, 0);
+#pragma unroll 1
+      for (int q = 1; q < C; ++q) G = ff_add(G, shfl_ff(gl, q));   // the same order everywhere
+      // exp(-L) = exp(-L0) / (1 + G): the residual at L is exactly A + beta B
+      // with beta = 1 - exp(L0 - L) = G / (1 + G) = G - G^2 + ..., unless L
+      // and L0 cut the tokens differently (some t between them), or beta is
+      // not small: then an exact pass at L.  No fp64 on this path (it runs
+      // at a small fraction of the fp32 rate on this GPU).
+      const float Gs = __fadd_rn(G.hi, G.lo);
+      const float dL = use == 0 ? log1pf(Gs) : 0.0f;                         // L - L0
+      const float nneg = warp_min(dl.hi), npos = warp_min(dl.lo);
+      const float margin = __fadd_rn(__fmul_rn(2.0f, fabsf(dL)), 1e-7f);
+      const bool big = use == 0 && !(fabsf(G.hi) < 0x1p-14f);
+      const bool recut = big || (use == 0 && (dL >= 0.0f ? npos <= margin : nneg <= margin));
+      // beta * 2^56 as an integer: G.hi 2^56 is exact; the rest (G.lo - G^2
+      // + G^3, below 2^-28 here) rounds to an integer
+      const long long beta = use == 0 && !big
+          ? __float2ll_rn(__fmul_rn(G.hi, 0x1p56f)) +
+            __float2ll_rn(__fmul_rn(__fadd_rn(G.lo, __fmul_rn(__fmul_rn(G.hi, G.hi),
+                                                             __fsub_rn(G.hi, 1.0f))),
+                                    0x1p56f))
+          : 0ll;
+      if (recut && l == 0) {
+        rf_L_exact = two_sum(L0, dL);
+      }
+      const u128 ca = warp_inclusive_scan_u128(a0);   // inclusive prefixes over slices
+      const u128 cb = warp_inclusive_scan_u128(b0);
+      const i128 Z = comb(shfl_u128(ca, 31), shfl_u128(cb, 31), beta);
+      const i128 tg = Z > 0 ? static_cast<i128>(scale_u24(sm.draw_u24[n], static_cast<u128>(Z)))
+                            : static_cast<i128>(0);
+      const unsigned hit = __ballot_sync(0xffffffffu, l < C && comb(ca, cb, beta) > tg);
+      const int owner = hit ? __ffs(hit) - 1 : C - 1;
+      const u128 pa = shfl_u128(ca - a0, owner), pb = shfl_u128(cb - b0, owner);
+      if (l == 0) {
+        sm.dec_use = recut ? -2 : Z > 0 ? use : -1;
+        sm.dec_L = rf_L_exact;
+        sm.dec_owner = owner == static_cast<int>(k);
+        sm.dec_pa = pa;
+        sm.dec_pb = pb;
+        sm.dec_beta = beta;
+        sm.dec_tg = tg;
+        sm.walker = kClNT;
+      }
+    }
+    __syncthreads();
+    if (sm.dec_use == -2) {                        // exact pass at L (the same in every CTA)
+      rf.L = sm.dec_L;
+      use = 2;
+      cluster_sync_all();                          // every CTA has read the totals
+      continue;
+    }
+    if (sm.dec_use < 0) {                          // Z <= 0 (the same in every CTA)
+      if (use != 1) {                              // rejected, empty residual: draw from q_hat
+        if (k == 0 && tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+        use = 1;
+        cluster_sync_all();                        // every CTA has read the totals
+        continue;
+      }
+      if (k == 0 && tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: not for a valid row
+      break;
+    }
+    if (sm.dec_owner) {                            // uniform within the CTA
+      const long long beta = sm.dec_beta;
+      const i128 tg = sm.dec_tg;
+      const u128 pa = sm.dec_pa, pb = sm.dec_pb;
+      // the first thread whose run ends past the target
+      if (comb(pa + exa + sa, pb + exb + sb, beta) > tg) atomicMin(&sm.walker, tid);
+      __syncthreads();
+      const int wt = min(sm.walker, kClNT - 1);
+      if (w == (wt >> 5)) {
+        // The walker's warp walks its run together: lane e recomputes element
+        // e of the run (the same weight bits as the run sums), inclusive
+        // scans over the lanes give the running sums, the first lane past the
+        // target holds the token.
+        static_assert(kClVPT * 8 <= 32, "a run has at most 32 elements");
+        const int wra = min(nv, wt * vpt), wrb = min(nv, wra + vpt);
+        const int nel = (wrb - wra) * EPV;
+        const u128 wxa = shfl_u128(exa, wt & 31), wxb = shfl_u128(exb, wt & 31);
+        u128 fa = 0, fb = 0;
+        if (l < nel) {
+          const int v = wra + l / EPV, e = l % EPV;
+          const uint4 xq = load_vec<T>(rq, V, v0 + v, alq);
+          const uint4 xd = use != 1 ? load_vec<T>(rd, V, v0 + v, ald) : xq;
+          float gt;
+          weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), fa, fb, gt);
+        }
+        fa = warp_inclusive_scan_u128(fa);
+        fb = warp_inclusive_scan_u128(fb);
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, l < nel && comb(pa + wxa + fa, pb + wxb + fb, beta) > tg);
+        const int last = max(nel - 1, 0);
+        if (l == 0) a.out_tokens[r0 + n] = (v0 + wra) * EPV + (hit ? __ffs(hit) - 1 : last);
+      }
+    }
+    break;
   }
   cluster_sync_all();                              // (3) no CTA leaves while its totals are read
 }
@@ -1633,8 +1857,27 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// 2^(j/64) for j = -32..32 as float-float pairs, from double precision
+// (built once, thread-safe static initialization).
+struct Exp2Table {
+  float2 v[kExp2Tab];
+  Exp2Table() {
+    for (int t = 0; t < kExp2Tab; ++t) {
+      const double x = std::exp2(static_cast<double>(t - 32) / 64.0);
+      const float hi = static_cast<float>(x);
+      v[t] = make_float2(hi, static_cast<float>(x - static_cast<double>(hi)));
+    }
+  }
+};
+static const float2 *exp2_table_host() {
+  static const Exp2Table tab;
+  return tab.v;
+}
+
 cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s) {
   SampParams P;
+  const float2 *tab = exp2_table_host();
+  for (int t = 0; t < kExp2Tab; ++t) P.exp2tab[t] = tab[t];
   P.a = L.a;
   P.ws = L.ws;
   P.plan = L.plan;
@@ -1643,6 +1886,9 @@ cudaError_t launch_sampler(const SamplerLaunch &L, cudaStream_t s) {
   const double c = 1.4426950408889634 / static_cast<double>(L.a.temperature);
   P.c_hi = static_cast<float>(c);
   P.c_lo = static_cast<float>(c - static_cast<double>(P.c_hi));
+  const double it = 1.0 / static_cast<double>(L.a.temperature);
+  P.it_hi = static_cast<float>(it);
+  P.it_lo = static_cast<float>(it - static_cast<double>(P.it_hi));
   P.pdl_secondary = L.pdl_secondary ? 1 : 0;
   P.stream = L.philox_stream;
   if (2 * L.a.num_rows - L.a.batch <= 0) return cudaSuccess;

@@ -43,14 +43,16 @@ def oracle_sampler(inp, seed=None):
                                 inp.get("top_ks"))
 
 
-def check(api, inp, seed=None, expect_status=0):
+def check(api, inp, seed=None, expect_status=0, tie_bound=True):
     d = run_sampler(api, inp, seed)
     ref = oracle_sampler(inp, seed)
     n, ties = compare_sampling(ref, d.num_accepted.cpu().numpy(), d.out_tokens.cpu().numpy(),
                                inp["cu_q"], drafts=inp["draft_tokens"], V=inp["V"])
     assert d.status_bits() == (ref["status"] | expect_status), (d.status_bits(), ref["status"])
-    # the windows are narrow: ties stay rare on these draws
-    assert ref["tie_count"] <= max(3, n // 8), tie_report(ref)
+    # the windows are narrow: ties stay rare on these draws (not on logits
+    # built to tie, where tie_bound is off)
+    if tie_bound:
+        assert ref["tie_count"] <= max(3, n // 8), tie_report(ref)
     print(tie_report(ref))
     return d, ref, ties
 
@@ -166,7 +168,7 @@ def test_tiny_top_p_and_tie_heavy_logits(api):
             q[np.concatenate([np.arange(inp["cu_q"][i], inp["cu_q"][i + 1] - 1)
                               for i in range(inp["B"])])] +
             rng.integers(-2, 3, size=inp["draft_logits"].shape).astype(np.float32) * 0.5)
-        check(api, inp)
+        check(api, inp, tie_bound=False)
 
 
 def test_bad_tokens_nonfinite_and_masked_rows(api):
