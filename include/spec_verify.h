@@ -131,7 +131,11 @@ typedef struct sv_attn_args {
    * layout; the step's own rows come in the cache's format), read as
    * code * k_scale and code * v_scale; q and out stay bf16.  Built for dtype
    * SV_BF16, head_dim 128, no shared prefix and (Hq/Hkv)*max_q_rows <= 16;
-   * other combinations return SV_ERR_UNSUPPORTED. */
+   * other combinations return SV_ERR_UNSUPPORTED.  The tensor-core operands
+   * are f16, so q is rounded to f16: q must lie within the f16 range
+   * (|q| <= 65504).  A larger q element becomes infinite and makes the
+   * outputs of its own (row, head) non-finite (other rows and heads are
+   * unaffected); no status bit reports it. */
   int32_t kv_dtype;         /* 0 (K/V in dtype) or SV_E4M3 */
   float k_scale;            /* E4M3 K scale; 0 -> 1 */
   float v_scale;            /* E4M3 V scale; 0 -> 1 */

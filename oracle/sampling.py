@@ -39,8 +39,11 @@ Readings where the pages are silent (each one is listed in the design notes):
     chosen); if a rejection leaves Z == 0 the draw falls back to q_hat and the
     EMPTY_RESIDUAL status bit is set;
   * a draft token outside [0, V) is a rejection with the BAD_TOKEN bit;
-  * a row holding NaN or +inf, or only -inf, makes its sequence fail: no token,
-    no append, NONFINITE bit.
+  * a row holding NaN or +inf, or only -inf, makes its sequence fail (no token,
+    no append, NONFINITE bit) when the left-to-right loop reaches it: target
+    and draft row j up to the first rejection, or the bonus row; rows after
+    the first rejection are never used (the loop stops there), so they cannot
+    fail the sequence.
 """
 import numpy as np
 
@@ -280,6 +283,17 @@ def verify_sequence(q_rows, p_rows, drafts, u_acc, u_smp, audit=None):
     return n, x, status
 
 
+def _first_rejection(qp, pp, drafts, u_acc, upto):
+    """Index of the first rejected draft among pairs 0..upto-1 (all valid), or
+    None when every one of them is accepted."""
+    V = qp[0].probs.shape[0]
+    for j in range(upto):
+        d = int(drafts[j])
+        if d < 0 or d >= V or not accept(u_acc[j], pp[j].probs[d], qp[j].probs[d]):
+            return j
+    return None
+
+
 # --------------------------------------------------------------------------
 # the batch
 # --------------------------------------------------------------------------
@@ -348,15 +362,26 @@ def reject_sample(target_logits, draft_logits, draft_tokens, cu_q, kv_len,
               for j in range(K + 1)]
         pp = [process_row(to_f64(draft_logits[p0 + j]), T_i, tp_i, tk_i)
               for j in range(K)]
-        if not all(r.valid for r in qp + pp):
-            seq_status[i] = DEV_NONFINITE
-            num_acc[i] = -1
-            continue
+        # Only the row pairs the left-to-right loop reaches are used: pair j
+        # (target row j, draft row j) up to the first rejection, or the bonus
+        # row K.  The sequence fails if a reached row is invalid.
+        bad_at = next((j for j in range(K + 1)
+                       if not qp[j].valid or (j < K and not pp[j].valid)), None)
+        Kr = K
+        if bad_at is not None:
+            rej = _first_rejection(qp, pp, draft_tokens[p0:p0 + K], u_acc, bad_at)
+            if rej is None:                  # the loop reaches the invalid pair
+                seq_status[i] = DEV_NONFINITE
+                num_acc[i] = -1
+                continue
+            Kr = rej + 1                     # decisions 0..rej; rejected at rej
         audit = []
-        n, x, st = verify_sequence(np.stack([r.probs for r in qp]),
-                                   np.stack([r.probs for r in pp]) if K else
-                                   np.zeros((0, qp[0].probs.shape[0])),
-                                   draft_tokens[p0:p0 + K], u_acc, u_smp, audit)
+        V = qp[0].probs.shape[0]
+        n, x, st = verify_sequence(np.stack([r.probs for r in qp[:Kr + 1]]),
+                                   np.stack([r.probs for r in pp[:Kr]]) if Kr else
+                                   np.zeros((0, V)),
+                                   draft_tokens[p0:p0 + Kr], u_acc[:Kr + 1], u_smp[:Kr + 1],
+                                   audit)
         seq_status[i] = st
         num_acc[i] = n
         out_tokens[r0:r0 + n] = draft_tokens[p0:p0 + n]

@@ -585,15 +585,16 @@ __device__ void accept_sequence(const SampParams &P, int i) {
   const int r0 = cuq(a, i), K = cuq(a, i + 1) - r0 - 1, p0 = r0 - i;
   const int L = a.kv_len[i];
   const RowStats *st = P.ws.stats;
+  // pair j (target row j, draft row j; the bonus row alone at j = K) is valid
   int ok = 1;
   if (lane <= K) ok = __ldcg(&st[r0 + lane].valid) != 0;
   if (lane < K) ok = ok && (__ldcg(&st[R + p0 + lane].valid) != 0);
-  ok = __all_sync(0xffffffffu, ok) && L >= 0;
-  if (!ok) {
+  const unsigned badm = __ballot_sync(0xffffffffu, lane <= K && !ok);
+  if (L < 0) {
     if (lane <= K) a.out_tokens[r0 + lane] = -1;
     if (lane == 0) {
       a.num_accepted[i] = -1;
-      set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
+      set_status(a.dev_status, SV_DEV_BAD_LENGTH);
     }
     return;
   }
@@ -603,7 +604,7 @@ __device__ void accept_sequence(const SampParams &P, int i) {
   const uint32_t sid_hi = static_cast<uint32_t>(static_cast<unsigned long long>(sid) >> 32);
   bool rej = false, bad = false;
   int d = 0;
-  if (lane < K) {
+  if (lane < K && ok) {
     d = a.draft_tokens[p0 + lane];
     if (d < 0 || d >= V) {
       rej = bad = true;
@@ -621,11 +622,17 @@ __device__ void accept_sequence(const SampParams &P, int i) {
   }
   const unsigned rm = __ballot_sync(0xffffffffu, rej);
   const unsigned bm = __ballot_sync(0xffffffffu, bad);
-  const int n = rm ? (__ffs(rm) - 1) : K;
-  if (lane <= K) a.out_tokens[r0 + lane] = lane < n ? d : -1;
+  // the loop stops at the first rejection or the first invalid pair; only
+  // rows it reaches are used, so an invalid pair fails the sequence only if
+  // no rejection comes before it
+  const int first_rej = rm ? (__ffs(rm) - 1) : K;
+  const int first_bad = badm ? (__ffs(badm) - 1) : K + 1;
+  const int n = first_bad <= first_rej ? -1 : first_rej;
+  if (lane <= K) a.out_tokens[r0 + lane] = (n >= 0 && lane < n) ? d : -1;
   if (lane == 0) {
     a.num_accepted[i] = n;
-    if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
+    if (n < 0) set_status(a.dev_status, SV_DEV_NONFINITE);
+    else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
   }
 }
 
@@ -1458,13 +1465,14 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   __syncthreads();
   // accept tests, lane j for draft j+1 (same decisions in every CTA)
   if (w == 0) {
-    int okall = 1;
-    for (int q = l; q < nrows; q += 32) okall &= sm.st_bad[q] == 0;
-    okall = __all_sync(0xffffffffu, okall) && L >= 0;
+    // pair l (target row l, draft row l; the bonus row alone at l = K) valid
+    const bool pair_ok = l <= K && sm.st_bad[l] == 0 && (l == K || sm.st_bad[K + 1 + l] == 0);
+    const unsigned badm = __ballot_sync(0xffffffffu, l <= K && !pair_ok);
+    const bool okall = L >= 0;
     const long long sid = a.seq_ids ? a.seq_ids[i] : static_cast<long long>(i);
     bool rej = false, bad = false;
     int d = 0;
-    if (okall && l < K) {
+    if (okall && l < K && pair_ok) {
       d = sm.dtok[l];
       if (d < 0 || d >= V) {
         rej = bad = true;
@@ -1479,13 +1487,18 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     }
     const unsigned rm = __ballot_sync(0xffffffffu, rej);
     const unsigned bm = __ballot_sync(0xffffffffu, bad);
-    const int n = !okall ? -1 : (rm ? (__ffs(rm) - 1) : K);
+    // the loop stops at the first rejection or the first invalid pair (only
+    // rows it reaches are used)
+    const int first_rej = rm ? (__ffs(rm) - 1) : K;
+    const int first_bad = badm ? (__ffs(badm) - 1) : K + 1;
+    const int n = !okall || first_bad <= first_rej ? -1 : first_rej;
     if (l == 0) sm.n = n;
     if (k == 0) {
       if (l <= K) a.out_tokens[r0 + l] = (n >= 0 && l < n) ? d : -1;
       if (l == 0) {
         a.num_accepted[i] = n;
-        if (!okall) set_status(a.dev_status, L < 0 ? SV_DEV_BAD_LENGTH : SV_DEV_NONFINITE);
+        if (!okall) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+        else if (n < 0) set_status(a.dev_status, SV_DEV_NONFINITE);
         else if (n < K && ((bm >> n) & 1u)) set_status(a.dev_status, SV_DEV_BAD_TOKEN);
       }
     }

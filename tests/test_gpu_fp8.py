@@ -70,6 +70,33 @@ def test_e4m3_small_all_outputs(api, Hq, Hkv, K_hi):
                                 K_hi=K_hi, gen_seed=70 + K_hi))
 
 
+def test_e4m3_q_range(api):
+    """q is rounded to f16 for the tensor cores: inside the f16 range (here
+    |q| up to ~6e4) the outputs match the oracle; one element beyond it makes
+    only its own (row, head) output non-finite, as the header states."""
+    inp = e4m3_inputs("bass_b8", B=3, Hq=4, Hkv=4, L_lo=10, L_hi=300, K_lo=1, K_hi=4,
+                      gen_seed=83)
+    q = W.bf16_bits_to_f32(inp["q"])
+    q *= np.float32(6e4 / np.max(np.abs(q)))
+    inp["q"] = W.f32_to_bf16_bits(q)
+    inp.update(k_scale=6.25e-6, v_scale=0.0625)   # scores and outputs stay O(1)
+    full_check(api, inp)
+    r, h = 2, 1
+    q2 = q.copy()
+    q2[r, h, 7] = 7.0e4                        # beyond the f16 range
+    inp["q"] = W.f32_to_bf16_bits(q2)
+    d = run_attn(api, inp)
+    got = d.out.float().cpu().numpy()
+    ref = oracle_all(inp)
+    bad = ~np.isfinite(got)
+    assert bad[r, h].all()
+    bad[r, h] = False
+    assert not bad.any()
+    mask = np.ones(got.shape[:2], dtype=bool)
+    mask[r, h] = False
+    assert float(np.max(np.abs(got[mask] - ref[mask]))) < TOL
+
+
 def test_e4m3_scales_enter_as_defined(api):
     """k_scale scales the scores and v_scale the output: other scales on the
     same codes still match the oracle's definition."""

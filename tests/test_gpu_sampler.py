@@ -177,8 +177,9 @@ def test_bad_tokens_nonfinite_and_masked_rows(api):
     inp["draft_tokens"][cu[1] - 1 + 1] = 512          # seq 1, draft 2: out of range
     inp["draft_tokens"][cu[2] - 2] = -3               # seq 2, draft 1: negative
     nan_bits = np.uint16(0x7FC0)
-    inp["target_logits"][cu[3] + 2, 100] = nan_bits   # seq 3 fails
+    inp["target_logits"][cu[3], 100] = nan_bits       # seq 3 fails (pair 0 is always reached)
     inp["draft_logits"][cu[4] - 4, 5] = np.uint16(0x7F80)   # +inf: seq 4 fails
+    inp["target_logits"][cu[1] + 3, 7] = nan_bits     # seq 1: fails only if pair 3 is reached
     inp["target_logits"][cu[5]:cu[6], :400] = np.uint16(0xFF80)   # -inf: masked tokens
     d, ref, _ = check(api, inp, expect_status=0)
     assert ref["status"] & oracle.DEV_BAD_TOKEN and ref["status"] & oracle.DEV_NONFINITE

@@ -423,6 +423,35 @@ def test_nonfinite_row_fails_only_its_sequence():
     assert r["num_accepted"][1] == 1        # p == q: accepted
 
 
+def test_rows_after_the_first_rejection_cannot_fail():
+    """Draft 1 is certain to be rejected (p puts all mass on it, q none), so
+    the loop stops at pair 0: a NaN in pair 1 or in the bonus row is never
+    read and the sequence succeeds; the same NaN in pair 0 fails it."""
+    V = 8
+    cu = np.array([0, 3], dtype=np.int32)
+    tgt = np.zeros((3, V), dtype=np.float32)
+    drf = np.zeros((2, V), dtype=np.float32)
+    tgt[0, 5] = -np.inf                     # q(5) = 0
+    drf[0, :] = -np.inf
+    drf[0, 5] = 0.0                         # p one-hot at 5
+    drafts = np.array([5, 1], dtype=np.int32)
+    for r_bad in ("t1", "d1", "t2"):
+        t, d = tgt.copy(), drf.copy()
+        if r_bad == "t1":
+            t[1, 0] = np.nan
+        elif r_bad == "d1":
+            d[1, 0] = np.inf
+        else:
+            t[2, :] = -np.inf
+        r = S.reject_sample(t, d, drafts, cu, np.array([4], dtype=np.int32), 1.0, 1.0, 9)
+        assert r["num_accepted"][0] == 0 and r["seq_status"][0] == 0, r_bad
+        assert r["out_tokens"][0] not in (-1, 5) and list(r["out_tokens"][1:]) == [-1, -1]
+    t = tgt.copy()
+    t[0, 2] = np.nan
+    r = S.reject_sample(t, drf, drafts, cu, np.array([4], dtype=np.int32), 1.0, 1.0, 9)
+    assert r["num_accepted"][0] == -1 and r["seq_status"][0] == S.DEV_NONFINITE
+
+
 # ---------------------------------------------------------------- processing
 def test_temperature_only_is_library_softmax():
     from scipy.special import softmax
