@@ -85,7 +85,8 @@ enum {
                                   inconsistent with the host bounds or the
                                   pool: that sequence is skipped */
   SV_DEV_TIMEOUT = 32u,        /* an internal wait of the attention pipeline
-                                  gave up (not expected; outputs of the
+                                  gave up (not expected at the built-in bound,
+                                  see sv_set_wait_limit; outputs of the
                                   affected CTA are left unwritten) */
   SV_DEV_BAD_PARAM = 64u       /* a per-sequence temperature < 0 or NaN, top_p
                                   <= 0 or NaN, or top_k < 0: that sequence
@@ -305,6 +306,20 @@ SV_API size_t sv_draft_workspace_bytes(const sv_draft_args *draft);
  * SV_ERR_* and launch nothing). */
 SV_API sv_status spec_draft_sample(const sv_draft_args *draft, void *ws, size_t ws_bytes,
                                    void *stream);
+
+/* Bound on the polls of one internal wait of the attention pipeline (an
+ * mbarrier of the copy ring, of a Q slot, of the consumer group or of the
+ * merge hand-off), for every attention launch that starts after the call in
+ * this process; 0 restores the built-in bound (2^22 polls).  A wait that runs
+ * out sets SV_DEV_TIMEOUT in *dev_status; its CTA stops, drains the copies
+ * it started (that drain always keeps the built-in bound) and leaves, so the
+ * outputs it owned stay unwritten and the workspace's merge counters may be
+ * left nonzero: zero the workspace again (sv_workspace_init, or
+ * sv_static_scratch_reset for spec_verify_attn_static) before its next use.
+ * A small bound makes waits run out on purpose; this exists to exercise that
+ * path (the papers have no counterpart).  Not synchronized with launches in
+ * flight on other host threads. */
+SV_API sv_status sv_set_wait_limit(uint32_t polls);
 
 /* Thread-local description of the last non-OK status returned on this
  * thread ("" if none). */

@@ -76,6 +76,8 @@ def _load():
     lib.spec_verify_attn_static.restype = ctypes.c_int
     lib.sv_static_scratch_reset.argtypes = [_p]
     lib.sv_static_scratch_reset.restype = ctypes.c_int
+    lib.sv_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.sv_set_wait_limit.restype = ctypes.c_int
     lib.spec_reject_sample.argtypes = [P(SampleArgs), _p, ctypes.c_size_t, _p]
     lib.spec_reject_sample.restype = ctypes.c_int
     lib.sv_draft_workspace_bytes.argtypes = [P(DraftArgs)]

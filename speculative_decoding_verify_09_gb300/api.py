@@ -145,6 +145,10 @@ class Workspace:
         self.ptr = (base + 255) // 256 * 256
         _check(lib.sv_workspace_init(ctypes.c_void_p(self.ptr), self.nbytes, _stream(stream)))
 
+    def zero(self, stream=None):
+        """Zero the workspace again (after a call that reported SV_DEV_TIMEOUT)."""
+        _check(lib.sv_workspace_init(ctypes.c_void_p(self.ptr), self.nbytes, _stream(stream)))
+
     @classmethod
     def for_args(cls, attn=None, sample=None, device=None, stream=None):
         return cls(workspace_bytes(attn, sample), device, stream)
@@ -166,6 +170,12 @@ def sv_static_scratch_reset(stream=None):
     """Zero the static scratch's merge counters on `stream` (after a static call
     reported SV_DEV_TIMEOUT); allocates nothing."""
     _check(lib.sv_static_scratch_reset(_stream(stream)))
+
+
+def sv_set_wait_limit(polls):
+    """Bound on the polls of one attention pipeline wait (0: the built-in
+    bound); a small bound makes waits run out on purpose (SV_DEV_TIMEOUT)."""
+    _check(lib.sv_set_wait_limit(int(polls)))
 
 
 def spec_reject_sample(sample, ws, stream=None):

@@ -1,6 +1,7 @@
 // C ABI of the verify step: argument checks, workspace layout, launches.
 // See include/spec_verify.h for the contract of every entry point.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -339,6 +340,16 @@ static __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATC
 
 namespace {
 
+std::atomic<uint32_t> g_wait_limit{0};
+
+}  // namespace
+
+namespace sv {
+uint32_t attention_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+}  // namespace sv
+
+namespace {
+
 // Front zone of g_static_scratch that holds only merge counters (B * Hkv words).
 constexpr size_t kStaticCounterBytes = 64 * 1024;
 
@@ -602,6 +613,11 @@ SV_API sv_status spec_verify_step(const sv_attn_args *attn, const sv_sample_args
   if ((st = run_attention(attn, L, ws, opts_step(L.splan), s)) != SV_OK) return st;
   cudaError_t e = sv::launch_sampler(SL, s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return SV_OK;
+}
+
+SV_API sv_status sv_set_wait_limit(uint32_t polls) {
+  g_wait_limit.store(polls, std::memory_order_relaxed);
   return SV_OK;
 }
 

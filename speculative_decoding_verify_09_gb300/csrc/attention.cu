@@ -97,6 +97,7 @@ struct AttnParams {
   uint32_t *dev_status;
   int64_t tiles_bound;            // host bound on the global tile count
   int pdl_primary;                // let the next launch start at once
+  uint32_t spin_limit;            // polls of one mbarrier wait before it gives up
   // shared-prefix (bifurcated) arrangement
   int mode;                       // 0 plain; 1 decode partials only; 2 prefix partials
   int G, spb;                     // groups; sequences per prefix row-block
@@ -221,9 +222,10 @@ __device__ __forceinline__ void fold_piece(float &mm, float &den, float4 &acc, f
   mm = mn;
 }
 
-// Wait for the phase of parity `parity` to complete; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it)
+// Wait for the phase of parity `parity` to complete; false after `limit`
+// polls (the launch's wait limit: kSpinLimit unless the host set a smaller one).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_test(bar, parity)) return true;
   return false;
 }
@@ -498,7 +500,7 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
     if (*abort_flag) { ok = false; break; }
     if (k == 0 || ld.lt == 0) {              // a segment starts: its header and Q rows
       const int slot = nq & 1;
-      if (!mbar_wait(rg.qempty + 8 * slot, ((nq >> 1) & 1) ^ 1)) { ok = false; break; }
+      if (!mbar_wait(rg.qempty + 8 * slot, ((nq >> 1) & 1) ^ 1, P.spin_limit)) { ok = false; break; }
       const uint32_t qs = rg.q + slot * C::kQSlotB;
       if (lane == 0) {
         *reinterpret_cast<SeqInfo *>(smem + (qs - rg.base)) = s;
@@ -513,7 +515,7 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
       }
       ++nq;
     }
-    if (!mbar_wait(rg.empty + 8 * st, ph ^ 1)) { ok = false; break; }
+    if (!mbar_wait(rg.empty + 8 * st, ph ^ 1, P.spin_limit)) { ok = false; break; }
     if constexpr (KV8) {
       // E4M3 rows of D bytes: lane owns 16-byte chunk lane % 8 of rows lane / 8
       // + 4 * p; chunk c of row r lands at chunk c ^ (r % 8) (bank spread for
@@ -602,16 +604,19 @@ __device__ __forceinline__ void attn_produce(const AttnParams &P, const Sched &S
     *abort_flag = 1;
   }
   {
-    // Before leaving, every copy this warp started must have landed: wait for
-    // the last fill of each stage and Q slot (all earlier fills completed
-    // before the slot could be refilled).
+    // Before leaving, every copy this warp started must have landed, whatever
+    // the launch's wait limit: each lane's own cp.async copies (waited for
+    // unconditionally), then the last fill of each stage and Q slot under the
+    // full kSpinLimit (all earlier fills completed before the slot could be
+    // refilled; the Q rows are bulk copies that complete on their mbarrier).
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     for (int s2 = 0; s2 < NS && s2 < issued; ++s2) {
       const int last = s2 + (issued - 1 - s2) / NS * NS;
-      mbar_wait(rg.full + 8 * s2, (last / NS) & 1);
+      mbar_wait(rg.full + 8 * s2, (last / NS) & 1, kSpinLimit);
     }
     for (int s2 = 0; s2 < 2 && s2 < nq; ++s2) {
       const int last = s2 + (nq - 1 - s2) / 2 * 2;
-      mbar_wait(rg.qfull + 8 * s2, (last >> 1) & 1);
+      mbar_wait(rg.qfull + 8 * s2, (last >> 1) & 1, kSpinLimit);
     }
   }
 }
@@ -629,7 +634,7 @@ __device__ __forceinline__ void attn_merge_jobs(const AttnParams &P, const Ring 
   const int lane = threadIdx.x & 31, g = P.g;
   for (int nj = 0;; ++nj) {
     const int js = nj % kJobs;
-    if (!mbar_wait(rg.jfull + 8 * js, (nj / kJobs) & 1)) {
+    if (!mbar_wait(rg.jfull + 8 * js, (nj / kJobs) & 1, P.spin_limit)) {
       if (lane == 0) {
         set_status(P.dev_status, SV_DEV_TIMEOUT);
         *abort_flag = 1;
@@ -774,7 +779,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   // consumer-group barrier (bounded)
   auto csync = [&]() {
     mbar_arrive(rg.ebar);
-    if (!mbar_wait(rg.ebar, ephase)) ok = false;
+    if (!mbar_wait(rg.ebar, ephase, P.spin_limit)) ok = false;
     ephase ^= 1;
   };
 
@@ -803,7 +808,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   uint32_t qf[kHoldQ ? KS : 1][2];
   auto begin_segment = [&]() -> bool {
     const int slot = nq & 1;
-    if (!mbar_wait(rg.qfull + 8 * slot, (nq >> 1) & 1)) return false;
+    if (!mbar_wait(rg.qfull + 8 * slot, (nq >> 1) & 1, P.spin_limit)) return false;
     qslot = rg.q + slot * C::kQSlotB;
     cs = *reinterpret_cast<const SeqInfo *>(smem + (qslot - rg.base));
     active = row_w0 < cs.M;
@@ -825,7 +830,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   // its partial writes; seg = -1 ends the merger).
   auto post_job = [&](const MergeJob &jb) {
     const int js = njob % kJobs;
-    if (!mbar_wait(rg.jempty + 8 * js, ((njob / kJobs) & 1) ^ 1)) ok = false;
+    if (!mbar_wait(rg.jempty + 8 * js, ((njob / kJobs) & 1) ^ 1, P.spin_limit)) ok = false;
     if (tid == 0) jobs[js] = jb;
     mbar_arrive(rg.jfull + 8 * js);
     ++njob;
@@ -936,7 +941,7 @@ __device__ __forceinline__ void attn_bf16_body(const AttnParams &P, unsigned cha
   ok = begin_segment();
 
   for (int k = 0; k < ntiles && ok; ++k) {
-    if (!mbar_wait(rg.full + 8 * st, ph)) { ok = false; break; }
+    if (!mbar_wait(rg.full + 8 * st, ph, P.spin_limit)) { ok = false; break; }
     if (active) {
       const uint32_t kbase = rg.base + st * C::kStageB;
       const uint32_t vbase = kbase + C::kTileB;
@@ -1565,6 +1570,8 @@ cudaError_t launch_attention(const sv_attn_args &a, const AttnPlan &p, const Att
   P.dev_status = a.dev_status;
   P.tiles_bound = p.tiles_bound;
   P.pdl_primary = 0;
+  P.spin_limit = attention_wait_limit();
+  if (P.spin_limit == 0 || P.spin_limit > kSpinLimit) P.spin_limit = kSpinLimit;
   P.mode = 0;
   P.G = a.num_groups;
   P.spb = p.spb;

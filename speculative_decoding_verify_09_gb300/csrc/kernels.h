@@ -103,6 +103,10 @@ struct AttnWs {
   float *pre_o, *pre_ml;      // prefix partials
 };
 
+// Polls of one attention pipeline wait before it gives up with SV_DEV_TIMEOUT
+// (0: the built-in bound); set by sv_set_wait_limit, read at each launch.
+uint32_t attention_wait_limit();
+
 // num_sms = 0: device-independent plan (grids at their upper bound).
 AttnPlan plan_attention(const sv_attn_args &a, int num_sms);
 int attention_max_batch();
