@@ -235,6 +235,31 @@ __device__ __forceinline__ FF exp2_ff(FF y, const float2 *tab) {
   return FF{__fmul_rn(e.hi, p2), __fmul_rn(e.lo, p2)};
 }
 
+// ---------------------------------------------------------------- 64-bit fixed point
+// Draw weights as exact integers in units of 2^-63: a float r in [0, 2) is
+// exact down to 2^-40 and truncated below (the error of a sum of V weights is
+// below V 2^-63, far below any draw's resolution); sums of weights that add
+// up to at most 2 fit in 64 bits.
+__device__ __forceinline__ unsigned long long fix63(float r) {
+  const uint32_t b = __float_as_uint(r);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;  // r = m * 2^(e - 150)
+  const int sh = e - 87;
+  if (sh >= 0) return m << sh;
+  return -sh < 24 ? (m >> (-sh)) : 0ull;
+}
+
+__device__ __forceinline__ unsigned long long warp_inclusive_scan_u64(unsigned long long v) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (l >= o) v += t;
+  }
+  return v;
+}
+
 // ---------------------------------------------------------------- 128-bit fixed point
 // Draw weights as exact integers in units of 2^-116: a float r in [0, 2) is
 // exact down to 2^-93 and truncated below; sums of up to 2^11 times the
@@ -277,6 +302,11 @@ __device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
 typedef __int128 i128;
 __device__ __forceinline__ i128 comb(u128 a, u128 b, long long beta56) {
   return static_cast<i128>(a) + ((static_cast<i128>(b >> 40) * beta56) >> 16);
+}
+// The same for 2^-63 sums (b < 2^64, |beta56| < 2^42: the product fits).
+__device__ __forceinline__ i128 comb63(unsigned long long a, unsigned long long b,
+                                       long long beta56) {
+  return static_cast<i128>(a) + ((static_cast<i128>(b) * beta56) >> 56);
 }
 
 __device__ __forceinline__ u128 shfl_up_u128(u128 v, int o) {

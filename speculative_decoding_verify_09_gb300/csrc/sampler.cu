@@ -1241,9 +1241,9 @@ struct ClusterSmem {
   int dtok[kMaxRows];
   float redm[kMaxRows][kClNW], reds[kMaxRows][kClNW];
   uint32_t redb[kMaxRows][kClNW];
-  u128 tot[2];                                       // slice totals of the sums A and B
-  u128 scan_red[kClNW];
-  u128 dec_pa, dec_pb;                               // prefix of the owner slice
+  unsigned long long tot[2];                         // slice totals of the sums A and B
+  unsigned long long scan64[kClNW];
+  unsigned long long dec_pa, dec_pb;                 // prefix of the owner slice
   FF dec_L;                                          // exact ln(S_p / S_q) (recut pass)
   i128 dec_tg;                                       // the target, in units of A + beta B
   long long dec_beta;                                // beta * 2^56
@@ -1576,9 +1576,10 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   //    q_hat (1 - exp(t - L0) / (1 + G)) = A + beta * B, beta = G / (1 + G);
   //    only tokens with t between L0 and L (a band of width |L - L0| ~ 1e-6)
   //    are off, by at most q_hat |L - L0|.
-  // A + beta * B is evaluated in 128-bit integers from the prefix sums at
-  // every decision point, the same function of the same integers everywhere,
-  // so the slice, thread and token searches agree.
+  // A and B are 2^-63 fixed-point sums; A + beta * B is evaluated in 128-bit
+  // integers from the prefix sums at every decision point, the same function
+  // of the same integers everywhere, so the slice, thread and token searches
+  // agree.
   const float L0 = mode == 0 ? logf(__fdividef(rf.inv_sq, ip)) : 0.0f;
   rf.L = FF{L0, 0.0f};
   const float mp_ = rf.mp;
@@ -1587,18 +1588,19 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   // the tokens where L0 did); use 2: the residual at the exact L directly
   // (beta = 0), when it does not; use 1: q_hat.
   float dneg = INFINITY, dpos = INFINITY;
-  auto weights = [&](int use, uint32_t bq, uint32_t bd, u128 &wa, u128 &wb, float &gterm) {
+  auto weights = [&](int use, uint32_t bq, uint32_t bd, unsigned long long &wa,
+                     unsigned long long &wb, float &gterm) {
     const float lq = LT<T>::val(bq);
     wa = 0;
     wb = 0;
     gterm = 0.0f;
     if (use == 1) {
-      wa = fix116(rf.qhat(lq));
+      wa = fix63(rf.qhat(lq));
       return;
     }
     const float lp = LT<T>::val(bd);
     if (use == 2) {
-      wa = fix116(rf(lq, lp));
+      wa = fix63(rf(lq, lp));
       return;
     }
     if (lq == -INFINITY) {
@@ -1607,7 +1609,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     }
     const float qh = rf.qhat(lq);
     if (lp == -INFINITY) {
-      wa = fix116(qh);
+      wa = fix63(qh);
       gterm = -qh;
       return;
     }
@@ -1615,8 +1617,8 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     const float em = expm1_fast(d);
     gterm = __fmul_rn(qh, em);
     if (d < 0.0f) {
-      wa = fix116(-gterm);
-      wb = fix116(__fmaf_rn(qh, em, qh));
+      wa = fix63(-gterm);
+      wb = fix63(__fmaf_rn(qh, em, qh));
       dneg = fminf(dneg, -d);
     } else {
       dpos = fminf(dpos, d);
@@ -1625,28 +1627,31 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   FF rf_L_exact = FF{0.0f, 0.0f};
   int use = mode;
   for (int round = 0; round < 3; ++round) {
-    u128 sa = 0, sb = 0;
-    FF g = ff_make(0.0f);
+    unsigned long long sa = 0, sb = 0;
+    float gs = 0.0f, gc = 0.0f;                    // Kahan sum of G's terms
     for (int v = ra; v < rb; ++v) {
       const uint4 xq = load_vec<T>(rq, V, v0 + v, alq);
       const uint4 xd = use != 1 ? load_vec<T>(rd, V, v0 + v, ald) : xq;
 #pragma unroll 1
       for (int e = 0; e < EPV; ++e) {
-        u128 wa, wb;
+        unsigned long long wa, wb;
         float gt;
         weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), wa, wb, gt);
         sa += wa;
         sb += wb;
-        g = ff_add(g, ff_make(gt));
+        const float y = __fsub_rn(gt, gc);
+        const float t2 = __fadd_rn(gs, y);
+        gc = __fsub_rn(__fsub_rn(t2, gs), y);
+        gs = t2;
       }
     }
-    u128 ta, tb;
-    const u128 exa = block_exclusive_scan_u128<kClNT>(sa, sm.scan_red, &ta);
+    unsigned long long ta, tb = 0;
+    const unsigned long long exa = block_exclusive_scan_u64<kClNT>(sa, sm.scan64, &ta);
     __syncthreads();
-    const u128 exb = use == 0 ? block_exclusive_scan_u128<kClNT>(sb, sm.scan_red, &tb)
-                              : static_cast<u128>(0);
+    const unsigned long long exb =
+        use == 0 ? block_exclusive_scan_u64<kClNT>(sb, sm.scan64, &tb) : 0ull;
     if (use == 0) {
-      g = warp_sum_ff(g);
+      const FF g = warp_sum_ff(FF{gs, -gc});
       dneg = warp_min(dneg);
       dpos = warp_min(dpos);
       if (l == 0) {
@@ -1657,7 +1662,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     }
     if (tid == 0) {
       sm.tot[0] = ta;
-      sm.tot[1] = use == 0 ? tb : static_cast<u128>(0);
+      sm.tot[1] = use == 0 ? tb : 0ull;
       FF x = ff_make(0.0f), dd = FF{INFINITY, INFINITY};
       if (use == 0) {
         x = sm.redff[0][0];
@@ -1674,8 +1679,8 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     cluster_sync_all();                            // (2) slice totals and G visible
     // ---- D: every CTA finds the slice holding the target (warp 0)
     if (w == 0) {
-      const u128 a0 = l < C ? *dsmem(&sm.tot[0], l) : static_cast<u128>(0);
-      const u128 b0 = l < C ? *dsmem(&sm.tot[1], l) : static_cast<u128>(0);
+      const unsigned long long a0 = l < C ? *dsmem(&sm.tot[0], l) : 0ull;
+      const unsigned long long b0 = l < C ? *dsmem(&sm.tot[1], l) : 0ull;
       FF gl = l < C ? *dsmem(&sm.ssum[0], l) : ff_make(0.0f);
       const FF dl = l < C ? *dsmem(&sm.ssum[1], l) : FF{INFINITY, INFINITY};
       FF G = shfl_ff(gl, 0);
@@ -1703,14 +1708,15 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
       if (recut && l == 0) {
         rf_L_exact = two_sum(L0, dL);
       }
-      const u128 ca = warp_inclusive_scan_u128(a0);   // inclusive prefixes over slices
-      const u128 cb = warp_inclusive_scan_u128(b0);
-      const i128 Z = comb(shfl_u128(ca, 31), shfl_u128(cb, 31), beta);
+      const unsigned long long ca = warp_inclusive_scan_u64(a0);   // inclusive prefixes over slices
+      const unsigned long long cb = warp_inclusive_scan_u64(b0);
+      const i128 Z = comb63(__shfl_sync(0xffffffffu, ca, 31), __shfl_sync(0xffffffffu, cb, 31), beta);
       const i128 tg = Z > 0 ? static_cast<i128>(scale_u24(sm.draw_u24[n], static_cast<u128>(Z)))
                             : static_cast<i128>(0);
-      const unsigned hit = __ballot_sync(0xffffffffu, l < C && comb(ca, cb, beta) > tg);
+      const unsigned hit = __ballot_sync(0xffffffffu, l < C && comb63(ca, cb, beta) > tg);
       const int owner = hit ? __ffs(hit) - 1 : C - 1;
-      const u128 pa = shfl_u128(ca - a0, owner), pb = shfl_u128(cb - b0, owner);
+      const unsigned long long pa = __shfl_sync(0xffffffffu, ca - a0, owner);
+      const unsigned long long pb = __shfl_sync(0xffffffffu, cb - b0, owner);
       if (l == 0) {
         sm.dec_use = recut ? -2 : Z > 0 ? use : -1;
         sm.dec_L = rf_L_exact;
@@ -1742,9 +1748,9 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     if (sm.dec_owner) {                            // uniform within the CTA
       const long long beta = sm.dec_beta;
       const i128 tg = sm.dec_tg;
-      const u128 pa = sm.dec_pa, pb = sm.dec_pb;
+      const unsigned long long pa = sm.dec_pa, pb = sm.dec_pb;
       // the first thread whose run ends past the target
-      if (comb(pa + exa + sa, pb + exb + sb, beta) > tg) atomicMin(&sm.walker, tid);
+      if (comb63(pa + exa + sa, pb + exb + sb, beta) > tg) atomicMin(&sm.walker, tid);
       __syncthreads();
       const int wt = min(sm.walker, kClNT - 1);
       if (w == (wt >> 5)) {
@@ -1755,8 +1761,9 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
         static_assert(kClVPT * 8 <= 32, "a run has at most 32 elements");
         const int wra = min(nv, wt * vpt), wrb = min(nv, wra + vpt);
         const int nel = (wrb - wra) * EPV;
-        const u128 wxa = shfl_u128(exa, wt & 31), wxb = shfl_u128(exb, wt & 31);
-        u128 fa = 0, fb = 0;
+        const unsigned long long wxa = __shfl_sync(0xffffffffu, exa, wt & 31);
+        const unsigned long long wxb = __shfl_sync(0xffffffffu, exb, wt & 31);
+        unsigned long long fa = 0, fb = 0;
         if (l < nel) {
           const int v = wra + l / EPV, e = l % EPV;
           const uint4 xq = load_vec<T>(rq, V, v0 + v, alq);
@@ -1764,10 +1771,10 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
           float gt;
           weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), fa, fb, gt);
         }
-        fa = warp_inclusive_scan_u128(fa);
-        fb = warp_inclusive_scan_u128(fb);
+        fa = warp_inclusive_scan_u64(fa);
+        fb = warp_inclusive_scan_u64(fb);
         const unsigned hit =
-            __ballot_sync(0xffffffffu, l < nel && comb(pa + wxa + fa, pb + wxb + fb, beta) > tg);
+            __ballot_sync(0xffffffffu, l < nel && comb63(pa + wxa + fa, pb + wxb + fb, beta) > tg);
         const int last = max(nel - 1, 0);
         if (l == 0) a.out_tokens[r0 + n] = (v0 + wra) * EPV + (hit ? __ffs(hit) - 1 : last);
       }
