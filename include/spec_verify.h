@@ -54,7 +54,7 @@ extern "C" {
 #endif
 
 #define SV_API __attribute__((visibility("default")))
-#define SV_ABI_VERSION 4
+#define SV_ABI_VERSION 5
 
 typedef enum sv_status {
   SV_OK = 0,
@@ -320,6 +320,24 @@ SV_API sv_status spec_draft_sample(const sv_draft_args *draft, void *ws, size_t 
  * path (the papers have no counterpart).  Not synchronized with launches in
  * flight on other host threads. */
 SV_API sv_status sv_set_wait_limit(uint32_t polls);
+
+/* One whole draft position (added in ABI 5): the draft model's single-row
+ * attention (spec_verify_attn with one block row per sequence: cu_q = 0..B,
+ * max_q_rows 1, num_rows B), the append of the position's own K/V row, and
+ * the draft-token draw of spec_draft_sample, as one call.  The speculative-
+ * sampling paper's algorithm draws the K drafts one position at a time; the
+ * draw reads only the draft logits (inputs here), so it and the append start
+ * beside the attention (programmatic dependent launch) instead of after it.
+ * attn and draft must describe the same batch (same B, kv_len pointer and
+ * dtype).  Writes attn->out, draft->draft_tokens, the pool row kv_start[i] +
+ * kv_len[i] and new_kv_len[i] = kv_len[i] + 1 (kv_len[i] with
+ * SV_DEV_CAPACITY when kv_len[i] + 1 > kv_cap[i]; new_kv_len must not alias
+ * kv_len).  Same results as the three separate calls.  Workspace:
+ * sv_draft_step_workspace_bytes, zeroed once like the others. */
+SV_API size_t sv_draft_step_workspace_bytes(const sv_attn_args *attn, const sv_draft_args *draft);
+SV_API sv_status spec_draft_step(const sv_attn_args *attn, const sv_draft_args *draft,
+                                 const int32_t *kv_cap, int32_t *new_kv_len, void *ws,
+                                 size_t ws_bytes, void *stream);
 
 /* Thread-local description of the last non-OK status returned on this
  * thread ("" if none). */

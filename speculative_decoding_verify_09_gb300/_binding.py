@@ -84,6 +84,10 @@ def _load():
     lib.sv_draft_workspace_bytes.restype = ctypes.c_size_t
     lib.spec_draft_sample.argtypes = [P(DraftArgs), _p, ctypes.c_size_t, _p]
     lib.spec_draft_sample.restype = ctypes.c_int
+    lib.sv_draft_step_workspace_bytes.argtypes = [P(AttnArgs), P(DraftArgs)]
+    lib.sv_draft_step_workspace_bytes.restype = ctypes.c_size_t
+    lib.spec_draft_step.argtypes = [P(AttnArgs), P(DraftArgs), _p, _p, _p, ctypes.c_size_t, _p]
+    lib.spec_draft_step.restype = ctypes.c_int
     lib.kv_append_ragged.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_int64] + [_p] * 5 + \
         [ctypes.c_int64] + [_p] * 7
     lib.kv_append_ragged.restype = ctypes.c_int

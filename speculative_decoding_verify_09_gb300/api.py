@@ -120,6 +120,21 @@ def draft_args(draft_logits, kv_len, draft_tokens, *, temperature, top_p, seed, 
     return d
 
 
+def spec_draft_step(attn, draft, kv_cap, new_kv_len, ws, stream=None):
+    """One draft position: single-row attention, append of the position's row
+    and the draft-token draw, the last two beside the attention."""
+    _check(lib.spec_draft_step(ctypes.byref(attn), ctypes.byref(draft), _ptr(kv_cap),
+                               _ptr(new_kv_len), ctypes.c_void_p(ws.ptr), ws.nbytes,
+                               _stream(stream)))
+
+
+def draft_step_workspace_bytes(attn, draft):
+    n = lib.sv_draft_step_workspace_bytes(ctypes.byref(attn), ctypes.byref(draft))
+    if n == 0:
+        _check(1)
+    return n
+
+
 def draft_workspace_bytes(draft):
     n = lib.sv_draft_workspace_bytes(ctypes.byref(draft))
     if n == 0:

@@ -276,6 +276,7 @@ class DraftBuffers:
                 **self.per_seq))
         self.ws_attn = api.Workspace.for_args(self.attn[0])
         self.ws_draft = api.Workspace(api.draft_workspace_bytes(self.draft[0]))
+        self.ws_step = api.Workspace(api.draft_step_workspace_bytes(self.attn[0], self.draft[0]))
         self.cur = 0
 
     @property
@@ -313,11 +314,22 @@ class DraftBuffers:
         api.spec_draft_sample(self.draft[c], self.ws_draft, stream)
         self.cur = c + 1
 
-    def run_all(self, stream=None):
-        """Every position from the starting lengths (one draft-side step)."""
+    def run_fused(self, stream=None):
+        """The next draft position as one call (spec_draft_step): the draw and
+        the append start beside the attention."""
+        c = self.cur
+        if c >= self.positions:
+            raise IndexError(f"all {self.positions} draft positions have run; rewind first")
+        self.api.spec_draft_step(self.attn[c], self.draft[c], self.kv_cap, self.kv_lens[c + 1],
+                                 self.ws_step, stream)
+        self.cur = c + 1
+
+    def run_all(self, stream=None, fused=False):
+        """Every position from the starting lengths (one draft-side step), as
+        three calls per position or (fused) one."""
         self.rewind()
         for _ in range(self.positions):
-            self.run(stream)
+            self.run_fused(stream) if fused else self.run(stream)
 
     def status_bits(self):
         return int(self.status.item()) & 0xFFFFFFFF

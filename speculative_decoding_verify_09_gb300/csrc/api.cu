@@ -538,6 +538,64 @@ SV_API sv_status spec_draft_sample(const sv_draft_args *draft, void *ws, size_t 
   return SV_OK;
 }
 
+SV_API size_t sv_draft_step_workspace_bytes(const sv_attn_args *attn, const sv_draft_args *draft) {
+  if (!attn || check_attn(attn) != SV_OK || check_draft(draft) != SV_OK) return 0;
+  const sv_sample_args s = draft_as_sample(draft);
+  const size_t t = layout(attn, &s).total + round_up(static_cast<size_t>(draft->batch) * 4);
+  return t > 0 ? t : kAlign;
+}
+
+SV_API sv_status spec_draft_step(const sv_attn_args *attn, const sv_draft_args *draft,
+                                 const int32_t *kv_cap, int32_t *new_kv_len, void *ws,
+                                 size_t ws_bytes, void *stream) {
+  sv_status st = check_attn(attn);
+  if (st != SV_OK) return st;
+  if ((st = check_draft(draft)) != SV_OK) return st;
+  if (attn->batch != draft->batch || attn->num_rows != attn->batch || attn->max_q_rows != 1 ||
+      attn->kv_len != draft->kv_len || attn->dtype != draft->dtype)
+    return fail(SV_ERR_INVALID,
+                "draft step: the attention must have one block row per sequence (cu_q = 0..B, "
+                "max_q_rows 1) and share kv_len and dtype with the draw");
+  if (attn->batch > 0) {
+    if (!kv_cap || !new_kv_len) return fail(SV_ERR_INVALID, "draft step: null kv_cap / new_kv_len");
+    if (new_kv_len == attn->kv_len)
+      return fail(SV_ERR_INVALID, "draft step: new_kv_len aliases kv_len");
+    if (!attn->k_cache || !attn->v_cache) return fail(SV_ERR_INVALID, "draft step: null cache");
+  }
+  const sv_sample_args sa = draft_as_sample(draft);
+  const Layout L = layout(attn, &sa);
+  const size_t acc = L.total;     // [B] scratch for the (always 0) accepted counts
+  if ((st = check_ws(ws, ws_bytes, acc + round_up(static_cast<size_t>(draft->batch) * 4))) != SV_OK)
+    return st;
+  if (attn->batch == 0) return SV_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The position's attention launches first; the draw (Philox stream 1) and the
+  // append of the position's own K/V row start beside it as its programmatic
+  // dependent launch: neither reads the attention's output, and the append
+  // writes only the pool row at kv_len[i], which the attention does not read.
+  sv::SamplerLaunch SL = sampler_launch(&sa, L, ws);
+  SL.a.num_accepted = at<int32_t>(ws, acc);
+  SL.do_append = true;
+  SL.pdl_secondary = true;
+  SL.philox_stream = 1;
+  const int esz = attn->kv_dtype == SV_E4M3 ? 1 : attn->dtype == SV_F32 ? 4 : 2;
+  SL.app.k_new = attn->k_new;
+  SL.app.v_new = attn->v_new;
+  SL.app.k_cache = const_cast<void *>(attn->k_cache);
+  SL.app.v_cache = const_cast<void *>(attn->v_cache);
+  SL.app.pool_rows = attn->pool_rows;
+  SL.app.kv_start = attn->kv_start;
+  SL.app.kv_cap = kv_cap;
+  SL.app.new_kv_len = new_kv_len;
+  SL.app.row_bytes = attn->num_kv_heads * attn->head_dim * esz;
+  if (SL.app.row_bytes % 16)
+    return fail(SV_ERR_UNSUPPORTED, "draft step: K/V row bytes not a multiple of 16");
+  if ((st = run_attention(attn, L, ws, opts_step(L.splan), s)) != SV_OK) return st;
+  cudaError_t e = sv::launch_sampler(SL, s);
+  if (e != cudaSuccess) return cuda_fail(e, "draft sampler launch");
+  return SV_OK;
+}
+
 SV_API sv_status kv_append_ragged(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t dtype, int32_t max_q_rows, int64_t num_rows,
                                   const int32_t *cu_q, const void *k_new, const void *v_new,

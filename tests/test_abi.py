@@ -44,7 +44,7 @@ def test_exports_exactly_the_declared_symbols(binding):
 
 
 def test_struct_mirrors_and_version(binding):
-    assert binding.lib.sv_abi_version() == 4
+    assert binding.lib.sv_abi_version() == 5
     assert binding.lib.sv_struct_size(0) == ctypes.sizeof(binding.AttnArgs)
     assert binding.lib.sv_struct_size(1) == ctypes.sizeof(binding.SampleArgs)
     assert binding.lib.sv_struct_size(2) == ctypes.sizeof(binding.DraftArgs)

@@ -132,10 +132,12 @@ def test_draft_draws_use_their_own_stream(api):
     ("ragged_gqa_b32", dict(B=12, L_hi=3000)),
     ("bass_b8", {}),
 ])
-def test_draft_positions_match_oracle(api, name, kw):
-    """Four consecutive draft positions through the C ABI against the oracle's
-    draft_step iterated: attention outputs, drawn tokens, appended rows and
-    lengths after every position."""
+@pytest.mark.parametrize("fused", [False, True])
+def test_draft_positions_match_oracle(api, name, kw, fused):
+    """Four consecutive draft positions through the C ABI (three calls per
+    position, or the fused spec_draft_step) against the oracle's draft_step
+    iterated: attention outputs, drawn tokens, appended rows and lengths after
+    every position."""
     w = W.workload(name, **kw)
     base, steps = W.make_draft_inputs(w, positions=4)
     d = DraftBuffers(base, api, positions=4, steps=steps)
@@ -143,7 +145,7 @@ def test_draft_positions_match_oracle(api, name, kw):
     tol = 1e-4 if w.dtype == "f32" else 2e-2
     for t, st in enumerate(steps):
         inp.update(st)
-        d.run()
+        d.run_fused() if fused else d.run()
         torch.cuda.synchronize()
         ref = oracle.draft_step(inp)
         err = float(np.max(np.abs(d.out[t].float().cpu().numpy() - ref["out"])))
@@ -157,14 +159,36 @@ def test_draft_positions_match_oracle(api, name, kw):
         inp.update(k_cache=ref["k_cache"], v_cache=ref["v_cache"], kv_len=ref["new_kv_len"])
 
 
-def test_draft_position_capacity_overflow(api):
+@pytest.mark.parametrize("fused", [False, True])
+def test_draft_position_capacity_overflow(api, fused):
     base, _ = W.make_draft_inputs(W.workload("bass_b8", B=4, L_lo=64, L_hi=128))
     base = dict(base, kv_cap=base["kv_len"].copy())
     d = DraftBuffers(base, api)
-    d.run()
+    d.run_fused() if fused else d.run()
     torch.cuda.synchronize()
     assert list(d.kv_len.cpu().numpy()) == list(base["kv_len"])
     assert d.status_bits() & oracle.DEV_CAPACITY
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("bass_b8", {}),
+    ("ragged_gqa_b32", dict(B=16, L_hi=4000)),          # nucleus: the row-path sampler
+])
+def test_fused_draft_step_equals_three_calls(api, name, kw):
+    """spec_draft_step gives the bits of the three separate calls (same
+    kernels, same split of the attention, same Philox counters)."""
+    base, steps = W.make_draft_inputs(W.workload(name, **kw), positions=3)
+    a = DraftBuffers(base, api, positions=3, steps=steps)
+    b = DraftBuffers(base, api, positions=3, steps=steps)
+    a.run_all()
+    b.run_all(fused=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.tokens, b.tokens)
+    assert torch.equal(a.outputs["new_len"], b.outputs["new_len"])
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.k_cache.view(torch.int16), b.k_cache.view(torch.int16))
+    assert torch.equal(a.v_cache.view(torch.int16), b.v_cache.view(torch.int16))
+    assert a.status_bits() == b.status_bits() == 0
 
 
 def test_draft_step_rewinds_to_identical_results(api):
