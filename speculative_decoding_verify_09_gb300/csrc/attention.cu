@@ -1224,6 +1224,17 @@ __global__ void __launch_bounds__(AttnCfg<D, RS, NB, KV8>::kThreads)
   attn_bf16_body<D, RS, NB, KV8>(P, smem);
 }
 
+// The same kernel under a 128-register cap (launch bounds of two 256-thread
+// CTAs per SM; it is launched with fewer threads): used for the 16-row
+// configuration, whose uncapped two CTAs per SM would take every register of
+// the SM and leave none for the sampler CTAs the fused step runs beside them.
+template <int D, int RS, int NB, bool KV8>
+__global__ void __launch_bounds__(256, 2) attn_bf16_kernel_cap128(const AttnParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (P.pdl_primary) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  attn_bf16_body<D, RS, NB, KV8>(P, smem);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-prefix merge: out(i, h, j) combines the decode partials of (i, hk)
 // (cache + block keys, causal) with the prefix partials of the row-block that
@@ -1453,7 +1464,13 @@ cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int
   }
   P.sm = smem_map_for<D, RS, NB, KV8>(P, stages_for<D, RS, NB, KV8>(P, opt.smem_cap));
   const int bytes = std::max(P.sm.total, opt.smem_min);
-  auto kern = attn_bf16_kernel<D, RS, NB, KV8>;
+  static_assert(C::kThreads <= 256 || !(RS == 1 && NB == 2), "the capped kernel's bounds");
+  auto kern = [] {
+    if constexpr (D == 128 && RS == 1 && NB == 2 && !KV8)
+      return attn_bf16_kernel_cap128<D, RS, NB, KV8>;
+    else
+      return attn_bf16_kernel<D, RS, NB, KV8>;
+  }();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   if (e != cudaSuccess) return e;
   // all of the SM's unified L1 as shared memory (the loads bypass L1): an SM
