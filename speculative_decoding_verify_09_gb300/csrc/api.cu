@@ -200,7 +200,8 @@ Layout layout(const sv_attn_args *a, const sv_sample_args *s) {
     L.parts = off;
     off += round_up(rows * L.splan.stat_chunks * sizeof(sv::ChunkPart));
     L.draw_parts = off;
-    off += round_up(static_cast<size_t>(s->batch) * L.splan.draw_chunks * 16);
+    off += round_up(static_cast<size_t>(s->batch) * L.splan.draw_chunks *
+                    (1 + static_cast<size_t>(L.splan.draw_threads)) * 16);
   }
   if (a) {
     // size the partials for the largest grids any device could get
@@ -325,6 +326,7 @@ sv::SamplerLaunch sampler_launch(const sv_sample_args *sample, const Layout &L, 
   SL.ws.seq_cnt2 = at<uint32_t>(ws, L.seq_cnt2);
   SL.ws.parts = at<sv::ChunkPart>(ws, L.parts);
   SL.ws.draw_parts = at<unsigned __int128>(ws, L.draw_parts);
+  SL.ws.draw_thr = SL.ws.draw_parts + static_cast<size_t>(SL.a.batch) * L.splan.draw_chunks;
   return SL;
 }
 

@@ -250,6 +250,19 @@ __device__ __forceinline__ unsigned long long fix63(float r) {
   return -sh < 24 ? (m >> (-sh)) : 0ull;
 }
 
+// floor(r * 2^44) for a float r in [0, 1] (integer operations only): the unit
+// of the per-key masses of the histogram statistics, whose sums over at most
+// 2^18 elements stay below 2^62.
+__device__ __forceinline__ unsigned long long fix44(float r) {
+  const uint32_t b = __float_as_uint(r);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;  // r = m * 2^(e - 150)
+  const int sh = e - 106;
+  if (sh >= 0) return m << sh;
+  return -sh < 24 ? (m >> (-sh)) : 0ull;
+}
+
 __device__ __forceinline__ unsigned long long warp_inclusive_scan_u64(unsigned long long v) {
   const int l = threadIdx.x & 31;
 #pragma unroll
@@ -549,10 +562,35 @@ struct ResidualFn {
   }
 };
 
-// ln(S_p / S_q) of two float-float sums, as a float-float (fp64 logs, once
-// per draw).
-__device__ __forceinline__ FF ln_ratio_ff(FF sp, FF sq) {
-  return ff_from_double(log(ff_to_double(sp)) - log(ff_to_double(sq)));
+// 1 / s of a positive float-float as a float-float (relative error near
+// 2^-46): the rounded reciprocal and one correction step.
+__device__ __forceinline__ FF ff_recip(FF s) {
+  const float h = __frcp_rn(s.hi);
+  float e = __fmaf_rn(-s.hi, h, 1.0f);
+  e = __fmaf_rn(-s.lo, h, e);
+  return quick_two_sum(h, __fmul_rn(e, h));
+}
+
+// ln(s) of a float-float s >= 1 as a float-float (absolute error near
+// 2^-44): L0 = logf(s), then ln s = L0 + ln(1 + u) with u = s e^(-L0) - 1
+// (|u| ~ 1e-6, e^(-L0) by exp2_ff), ln(1 + u) = u - u^2/2 (the u^3 term is
+// below 2^-59).  No fp64: it runs at a small fraction of the fp32 rate here.
+__device__ __forceinline__ FF ln_ff(FF s, const float2 *tab) {
+  const float L0 = fmaxf(logf(s.hi), 0.0f);
+  constexpr float kLog2eHi = 1.44269502162933349609375f, kLog2eLo = 1.925963033500011079e-08f;
+  const FF p = two_prod(L0, kLog2eHi);
+  const FF y = quick_two_sum(p.hi, __fmaf_rn(L0, kLog2eLo, p.lo));
+  const FF e = exp2_ff(ff_neg(y), tab);
+  const FF se = ff_mul(s, e);
+  const FF u = quick_two_sum(__fsub_rn(se.hi, 1.0f), se.lo);      // se.hi - 1 is exact
+  const FF lu = ff_add(u, ff_make(__fmul_rn(-0.5f, __fmul_rn(u.hi, u.hi))));
+  return ff_add(FF{L0, 0.0f}, lu);
+}
+
+// ln(S_p / S_q) of two float-float sums >= 1 (row sums relative to the row
+// maximum, whose own weight is 1), as a float-float.
+__device__ __forceinline__ FF ln_ratio_ff(FF sp, FF sq, const float2 *tab) {
+  return ff_add(ln_ff(sp, tab), ff_neg(ln_ff(sq, tab)));
 }
 
 }  // namespace sv

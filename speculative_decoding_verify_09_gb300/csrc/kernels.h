@@ -22,8 +22,8 @@ struct RowStats {
   float inv_lo;
   int32_t amax;       // greedy row (temperature 0): index of the one-hot; else -1
   float c_hi, c_lo;   // log2(e) / T of the row's sequence as a float pair
-  double ssum;        // sum over the kept set of exp((l - lmax) / T)
-  float acc_hi, acc_lo;   // the same sum from float-float weights (~1e-13), for residuals
+  float acc_hi, acc_lo;   // sum over the kept set of exp((l - lmax) / T) from float-float
+                          // weights (~1e-13), for residual draws
   float it_hi, it_lo;     // 1 / T of the row's sequence as a float pair
 };
 
@@ -43,13 +43,18 @@ struct SamplerWs {
   uint32_t *seq_cnt2;       // [B] draw-chunk arrivals per sequence (zero between calls)
   ChunkPart *parts;         // [(2R - B) * stat_chunks]
   unsigned __int128 *draw_parts;    // [B * draw_chunks] fixed-point (2^-116) chunk sums
+  unsigned __int128 *draw_thr;      // [B * draw_chunks * draw_threads] the chunks' per-thread
+                                    // run sums (runs in vocabulary order)
 };
 
 struct SamplerPlan {
   int stat_chunks;          // CTAs per row in the statistics phase (1: nucleus path)
-  int draw_chunks;          // CTAs per sequence in the draw phase
+  int draw_chunks;          // CTAs per sequence in the draw phase (<= 128; <= 512 vectors each)
+  int draw_threads;         // threads per draw CTA (one run of the chunk each)
   bool cluster;             // one CTA cluster per sequence (no nucleus, rows fit in smem)
   int cluster_nvt;          // 16-byte vectors per thread and row in the cluster kernel (1, 2)
+  int win_stats;            // bf16 rows off the cluster path: the window-histogram
+                            // statistics kernel (0: the f32 kernels)
 };
 
 struct AppendView {   // what the fused step's append needs (all device pointers)

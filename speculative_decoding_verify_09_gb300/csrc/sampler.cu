@@ -241,6 +241,25 @@ struct PdlTail {
   }
 };
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Generic address of `p` in the shared memory of cluster CTA `rank`.
+template <typename X>
+__device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
+  uint64_t r;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<X *>(r);
+}
+
 struct SampSmem {
   float2 exp2tab[kExp2Tab];   // 2^(j/64) as float-float (accurate kept-set sums)
   float tconst[4];            // log2(e)/T and 1/T of the row, float pairs
@@ -563,7 +582,6 @@ __device__ __forceinline__ void write_stats(RowStats *st, float lmax, uint32_t t
   o.amax = valid ? amax : -1;
   o.c_hi = c_hi;
   o.c_lo = c_lo;
-  o.ssum = ssum;
   o.acc_hi = acc.hi;
   o.acc_lo = acc.lo;
   o.it_hi = it_hi;
@@ -941,6 +959,475 @@ __global__ void __launch_bounds__(kSampNT) stats_row_kernel(const SampParams P) 
 }
 
 // --------------------------------------------------------------------------
+// Phase 1c (bf16 rows off the cluster path): one CTA per row, statistics from
+// a histogram of the keys in a window just below the row's maximum.  Equal
+// bf16 logits have equal weights, so within the window every cut and sum
+// follows exactly from the count of each key: work per distinct value, not
+// per element.
+//   Pass 1 streams the row for its largest and smallest key (NaN / +inf lie
+// above 0xFF7F, NaN below 0x7F).  Pass 2 (from L2) counts the keys of the
+// window [kb - 2047, kb], kb the largest key, and sums exp((l - max)/T) of
+// the elements below it (their float sum completes the row's sum S).  Then,
+// on the window's 64 chunks of 32 keys: per-chunk counts and 2^-44 masses,
+// their prefixes, the top-k key, the nucleus cut, and the kept set's sum
+// from float-float weights.  Should a cut lie below the window (a flat row,
+// a large top-k), the next window starts at the largest key below this one
+// and the row is counted again; keys above a window are already in the
+// prefixes.  Shared memory: about 10 KB, so the CTAs run beside the
+// attention's in the fused step.
+// --------------------------------------------------------------------------
+constexpr int kWinNT = 256;
+constexpr int kWinNW = kWinNT / 32;
+constexpr int kWinKeys = 2048;                         // keys per window
+constexpr int kWinCh = kWinKeys / 32;                  // chunks of 32 keys
+constexpr int kWinStages = 8;                          // row vectors per thread in flight
+constexpr uint32_t kKeyNegInf = 0x007Fu;               // -inf; keys below it: NaN
+
+struct WinSmem {
+  uint4 ring[kWinStages][kWinNT];                      // the row stream's slots
+  unsigned long long cmass[kWinCh], cpm[kWinCh];       // per chunk: 2^-44 mass, its prefix
+  uint32_t win[kWinKeys];                              // count of key kb - d at d
+  uint32_t ccnt[kWinCh], cpc[kWinCh];                  // per chunk: count, its prefix
+  float2 exp2tab[kExp2Tab];
+  FF redff[2][kWinNW];
+  uint32_t redu[2][kWinNW];
+  unsigned long long tot[2];                           // the window's count and mass
+  float tconst[4];
+  uint32_t cut_key[2];                                 // top-k key, nucleus cut
+  unsigned long long cut_m[2];                         // mass at and above each
+  int flag[2];
+};
+
+// The bf16 value of an order-preserving key, as a float.
+__device__ __forceinline__ float key_value(uint32_t k) {
+  const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+  return __uint_as_float(b << 16);
+}
+
+// Order-preserving keys of the two bf16 values of a word (packed halves).
+__device__ __forceinline__ uint32_t keys2_of(uint32_t wd) {
+  const uint32_t sg = (wd >> 15) & 0x00010001u;
+  return wd ^ (0x80008000u | (sg * 0x7FFFu));
+}
+
+// f(v, vector) for every 16-byte vector of the row this thread owns (v =
+// k * kWinNT + tid, in increasing order).  An aligned row streams through a
+// ring of kWinStages 16-byte slots per thread in shared memory, filled by
+// cp.async kWinStages vectors ahead (deep prefetch without registers; each
+// thread reads only its own slots, so no barrier); a slot is refilled after
+// its vector has been used.  An unaligned row, and a row's ragged last
+// vector, use plain loads.  Elements past V read as -inf.
+template <typename F>
+__device__ __forceinline__ void win_stream(const uint16_t *row, int V, int NV, bool aligned,
+                                           uint4 (*ring)[kWinNT], F &&f) {
+  const int tid = threadIdx.x;
+  if (!aligned) {
+#pragma unroll 1
+    for (int v = tid; v < NV; v += kWinNT) f(v, load_vec<uint16_t>(row, V, v, false));
+    return;
+  }
+  auto issue = [&](int v, int slot) {
+    if (v < NV) {
+      uint4 *dst = &ring[slot][tid];
+      if (v * 8 + 8 <= V) cp_async16(smem_u32(dst), row + v * 8, 16);
+      else *dst = load_vec<uint16_t>(row, V, v, true);
+    }
+    cp_async_commit();                           // one group per step (maybe empty)
+  };
+#pragma unroll
+  for (int k = 0; k < kWinStages; ++k) issue(k * kWinNT + tid, k);
+  int slot = 0;
+#pragma unroll 1
+  for (int v = tid; v < NV; v += kWinNT) {
+    cp_async_wait<kWinStages - 1>();             // this thread's oldest group has landed
+    const uint4 cur = ring[slot][tid];
+    f(v, cur);
+    issue(v + kWinStages * kWinNT, slot);
+    slot = slot + 1 == kWinStages ? 0 : slot + 1;
+  }
+  cp_async_wait<0>();
+}
+
+// Keys of the two bf16 values of a word with -0 taken as +0 (as key_of_bf16).
+__device__ __forceinline__ uint32_t keys2_merged(uint32_t wd) {
+  return keys2_of(wd & ~__vcmpeq2(wd, 0x80008000u));
+}
+
+// Block-wide float-float sum of one value per thread (fixed order; all get it).
+__device__ __forceinline__ FF win_sum_ff(FF v, FF *red) {
+  v = warp_sum_ff(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  FF t = red[0];
+#pragma unroll
+  for (int k = 1; k < kWinNW; ++k) t = ff_add(t, red[k]);
+  return t;
+}
+
+// A 2^-44 fixed-point sum as a float-float (both parts exact conversions).
+__device__ __forceinline__ FF ff_from_fix44(unsigned long long x) {
+  const float hi = __ull2float_rn(x);
+  const long long rem = static_cast<long long>(x - __float2ull_rn(hi));
+  return FF{__fmul_rn(hi, 0x1p-44f), __fmul_rn(__ll2float_rn(rem), 0x1p-44f)};
+}
+
+// floor(s * p) for a 2^-44 sum s < 2^62 and a float p in (0, 1), exactly.
+__device__ __forceinline__ unsigned long long mul_fix_p(unsigned long long s, float p) {
+  const uint32_t b = __float_as_uint(p);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  const unsigned long long m = e ? ((b & 0x7FFFFFu) | 0x800000u) : (b & 0x7FFFFFu);
+  const int sh = e ? 150 - e : 149;                     // p = m * 2^-sh
+  const u128 prod = static_cast<u128>(s) * m;
+  return sh < 128 ? static_cast<unsigned long long>(prod >> sh) : 0ull;
+}
+
+// Row statistics from the row's finished sums (one thread).
+__device__ __forceinline__ void write_stats_ff(RowStats *st, float lmax, uint32_t tau, bool valid,
+                                               FF ssum, float c_hi, float c_lo, int amax, FF acc,
+                                               float it_hi, float it_lo) {
+  RowStats o;
+  o.lmax = lmax;
+  o.tau_key = tau;
+  o.valid = valid ? 1u : 0u;
+  const FF inv = valid ? ff_recip(ssum) : FF{0.0f, 0.0f};
+  o.inv_hi = inv.hi;
+  o.inv_lo = inv.lo;
+  o.amax = valid ? amax : -1;
+  o.c_hi = c_hi;
+  o.c_lo = c_lo;
+  o.acc_hi = acc.hi;
+  o.acc_lo = acc.lo;
+  o.it_hi = it_hi;
+  o.it_lo = it_lo;
+  *st = o;
+}
+
+// log2(e)/T and 1/T as float-float pairs (no fp64): quotient, exact
+// remainder by fma, corrected quotient.
+__device__ __forceinline__ void temp_consts(float T, float *out) {
+  constexpr float kLog2eHi = 1.44269502162933349609375f, kLog2eLo = 1.925963033500011079e-08f;
+  const float q = __fdiv_rn(kLog2eHi, T);
+  const float rq = __fadd_rn(__fmaf_rn(-q, T, kLog2eHi), kLog2eLo);
+  const FF c = quick_two_sum(q, __fdiv_rn(rq, T));
+  const float t = __frcp_rn(T);
+  const FF it = quick_two_sum(t, __fdiv_rn(__fmaf_rn(-t, T, 1.0f), T));
+  out[0] = c.hi;
+  out[1] = c.lo;
+  out[2] = it.hi;
+  out[3] = it.lo;
+}
+
+// A 2^-44 fixed-point value of a non-negative float-float below 2^18.
+__device__ __forceinline__ unsigned long long fix44_ff(FF x) {
+  return __float2ull_rn(__fmul_rn(x.hi, 0x1p44f)) +
+         static_cast<unsigned long long>(__float2ll_rn(__fmul_rn(x.lo, 0x1p44f)));
+}
+
+__global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P) {
+  const PdlTail tail{P.pdl_secondary};
+  __shared__ WinSmem sm;
+  const sv_sample_args &a = P.a;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const void *base;
+  int64_t off;
+  const int i = row_seq(a, r, base, off);
+  if (!seq_rows_ok(a, i)) {
+    if (tid == 0) set_status(a.dev_status, SV_DEV_BAD_LENGTH);
+    return;
+  }
+  const uint16_t *row = static_cast<const uint16_t *>(base) + off;
+  const int V = a.vocab, NV = (V + 7) / 8;
+  const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+  exp2_table_fill(sm.exp2tab, P.exp2tab);
+  const float Tr = a.temperatures ? a.temperatures[i] : a.temperature;
+  const float tpr = a.top_ps ? a.top_ps[i] : a.top_p;
+  const int tkr = a.top_ks ? a.top_ks[i] : a.top_k;
+  const bool param_ok = Tr >= 0.0f && tpr > 0.0f && tkr >= 0;     // NaN fails the compares
+  if (tid == 0) {
+    if (!param_ok) set_status(a.dev_status, SV_DEV_BAD_PARAM);
+    if (a.temperatures && param_ok && Tr > 0.0f) temp_consts(Tr, sm.tconst);
+  }
+  // ---- pass 1: the largest and smallest key (elements past V read as -inf:
+  // neither NaN nor a maximum unless every logit is -inf)
+  uint32_t kmax2 = 0u, kmin2 = 0xFFFFFFFFu;
+  win_stream(row, V, NV, aligned, sm.ring, [&](int, const uint4 &x) {
+    const uint32_t k0 = keys2_of(x.x), k1 = keys2_of(x.y), k2 = keys2_of(x.z), k3 = keys2_of(x.w);
+    kmax2 = __vmaxu2(kmax2, __vmaxu2(__vmaxu2(k0, k1), __vmaxu2(k2, k3)));
+    kmin2 = __vminu2(kmin2, __vminu2(__vminu2(k0, k1), __vminu2(k2, k3)));
+  });
+  uint32_t tmax = max(kmax2 & 0xFFFFu, kmax2 >> 16), tmin = min(kmin2 & 0xFFFFu, kmin2 >> 16);
+  tmax = __reduce_max_sync(0xffffffffu, tmax);
+  tmin = __reduce_min_sync(0xffffffffu, tmin);
+  if (l == 0) {
+    sm.redu[0][w] = tmax;
+    sm.redu[1][w] = tmin;
+  }
+  __syncthreads();
+  uint32_t maxkey = 0u, minkey = 0xFFFFu;
+#pragma unroll
+  for (int k = 0; k < kWinNW; ++k) {
+    maxkey = max(maxkey, sm.redu[0][k]);
+    minkey = min(minkey, sm.redu[1][k]);
+  }
+  if (maxkey == 0x7FFFu) maxkey = 0x8000u;      // -0 and +0: one key (as key_of_bf16)
+  const bool bad = maxkey >= 0xFF80u || minkey < kKeyNegInf;
+  bool valid = param_ok && !bad && maxkey > kKeyNegInf;          // some finite logit
+  const float M = valid ? key_value(maxkey) : -INFINITY;
+  RowStats *out = &P.ws.stats[r];
+  if (!valid) {
+    if (tid == 0)
+      write_stats_ff(out, M, 0u, false, FF{0.0f, 0.0f}, 0.0f, 0.0f, -1, FF{0.0f, 0.0f}, 0.0f, 0.0f);
+  } else if (Tr == 0.0f) {
+    // ---- greedy: one-hot at the lowest index holding the maximum (values
+    // compared, so -0 and +0 are equal); a thread's vectors come in order
+    int first = INT_MAX;
+    win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+      uint32_t b[8];
+      unpack<uint16_t>(x, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (first == INT_MAX && LT<uint16_t>::val(b[e]) == M) first = v * 8 + e;
+    });
+    first = __reduce_min_sync(0xffffffffu, first);
+    __syncthreads();
+    if (l == 0) sm.redu[0][w] = static_cast<uint32_t>(first);
+    __syncthreads();
+    if (tid == 0) {
+      int f = INT_MAX;
+      for (int k = 0; k < kWinNW; ++k) f = min(f, static_cast<int>(sm.redu[0][k]));
+      write_stats_ff(out, M, 0u, true, FF{1.0f, 0.0f}, 0.0f, 0.0f, f, FF{1.0f, 0.0f}, 0.0f, 0.0f);
+    }
+  } else {
+    const bool own_t = a.temperatures != nullptr;
+    const float c_hi = own_t ? sm.tconst[0] : P.c_hi, c_lo = own_t ? sm.tconst[1] : P.c_lo;
+    const float it_hi = own_t ? sm.tconst[2] : P.it_hi, it_lo = own_t ? sm.tconst[3] : P.it_lo;
+    const WeightFn wf{M, c_hi, c_lo};
+    const FF cc{c_hi, c_lo};
+    const bool topk = tkr > 0 && tkr < V, nucleus = tpr < 1.0f;
+    const bool keep_all = !topk && !nucleus;
+    const unsigned long long K = topk ? static_cast<unsigned long long>(tkr) : 0ull;
+    auto wfix = [&](uint32_t k) -> unsigned long long {          // 2^-44 weight of a key
+      return k > kKeyNegInf ? fix44(wf(key_value(k))) : 0ull;
+    };
+    auto wff = [&](uint32_t k) -> FF {                           // float-float weight
+      return exp2_ff(ff_mul(two_sum(key_value(k), -M), cc), sm.exp2tab);
+    };
+    uint32_t kb = maxkey;                      // the window: keys [klo, kb]
+    unsigned long long pre_c = 0, pre_m = 0;   // count / mass of the keys above the window
+    unsigned long long sk = 0, S_fix = 0, ssum = 0;
+    FF acc_pre = ff_make(0.0f), acc_tail = ff_make(0.0f), acc = ff_make(0.0f);
+    bool have_k = !topk, have_p = !nucleus, done = false;
+    uint32_t kmin = 0u, tau = 0u;
+    for (int it = 0; it < 64 && !done; ++it) {   // 32 windows cover every key
+      const uint32_t klo = kb >= kWinKeys - 1 ? kb - (kWinKeys - 1) : 0u;
+      for (int d = tid; d < kWinKeys; d += kWinNT) sm.win[d] = 0u;
+      __syncthreads();
+      // ---- pass 2: count the window's keys; the first pass also sums every
+      // element's fp32 weight (the row's sum S, Kahan-compensated per vector)
+      float s = 0.0f, sc = 0.0f;
+      const float mc_hi = c_hi, mc_lo = c_lo;
+      auto count_vec = [&](const uint4 &x, int nel, bool sum) {
+        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+        float vs = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t kk = keys2_merged(wd[q]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const bool live = 2 * q + h < nel;
+            const uint32_t d = kb - (h ? (kk >> 16) : (kk & 0xFFFFu));   // keys above kb wrap
+            if (live && d < static_cast<uint32_t>(kWinKeys)) atomicAdd(&sm.win[d], 1u);
+            if (sum) {
+              const float lv = __uint_as_float(h ? (wd[q] & 0xFFFF0000u) : (wd[q] << 16));
+              const float dl = __fsub_rn(lv, M);                        // -inf -> weight 0
+              const float wv = fast_exp2(__fmaf_rn(dl, mc_hi, __fmul_rn(dl, mc_lo)));
+              vs = __fadd_rn(vs, live ? wv : 0.0f);
+            }
+          }
+        }
+        if (sum) {
+          const float y = __fsub_rn(vs, sc);
+          const float t = __fadd_rn(s, y);
+          sc = __fsub_rn(__fsub_rn(t, s), y);
+          s = t;
+        }
+      };
+      if (it == 0) {
+        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) { count_vec(x, V - v * 8, true); });
+      } else {
+        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) { count_vec(x, V - v * 8, false); });
+      }
+      FF at = ff_make(0.0f);                   // keep-all rows: float-float tail weights
+      if (it == 0 && keep_all) {
+        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+          const int nel = min(8, V - v * 8);
+#pragma unroll 1
+          for (int e = 0; e < nel; ++e) {
+            const uint32_t k = key_of_bf16(elem_bits<uint16_t>(x, e));
+            if (k < klo && k > kKeyNegInf) at = ff_add(at, wff(k));
+          }
+        });
+      }
+      FF rowsum = ff_make(0.0f);
+      if (it == 0) {
+        rowsum = win_sum_ff(FF{s, -sc}, sm.redff[0]);
+        if (keep_all) acc_tail = win_sum_ff(at, sm.redff[1]);
+      }
+      __syncthreads();
+      // ---- per chunk: count and mass (lane l: key kb - (32 ch + l))
+      for (int ch = w; ch < kWinCh; ch += kWinNW) {
+        const int d = 32 * ch + l;
+        const uint32_t c = sm.win[d];
+        const unsigned long long m = c ? static_cast<unsigned long long>(c) * wfix(kb - d) : 0ull;
+        const uint32_t cs = __reduce_add_sync(0xffffffffu, c);
+        const unsigned long long ms = warp_sum_u64(m);
+        if (l == 0) {
+          sm.ccnt[ch] = cs;
+          sm.cmass[ch] = ms;
+        }
+      }
+      __syncthreads();
+      if (w == 0) {                            // prefixes over the chunks, in key order
+        const unsigned long long c0 = sm.ccnt[2 * l], c1 = sm.ccnt[2 * l + 1];
+        const unsigned long long m0 = sm.cmass[2 * l], m1 = sm.cmass[2 * l + 1];
+        const unsigned long long ic = warp_inclusive_scan_u64(c0 + c1);
+        const unsigned long long im = warp_inclusive_scan_u64(m0 + m1);
+        sm.cpc[2 * l] = static_cast<uint32_t>(ic - c0 - c1);
+        sm.cpc[2 * l + 1] = static_cast<uint32_t>(ic - c1);
+        sm.cpm[2 * l] = im - m0 - m1;
+        sm.cpm[2 * l + 1] = im - m1;
+        if (l == 31) {
+          sm.tot[0] = ic;
+          sm.tot[1] = im;
+        }
+      }
+      __syncthreads();
+      const unsigned long long wc = sm.tot[0], wm = sm.tot[1];
+      if (it == 0) {
+        S_fix = fix44_ff(rowsum);              // the sum over every element
+        if (!topk) sk = S_fix;
+      }
+      // Warp 0: the chunk whose prefix range holds `tg` (counts or masses),
+      // then its lanes' inclusive scan: the key where the running value first
+      // reaches tg, and the mass at and above it, into slot q.
+      auto crossing = [&](bool by_count, unsigned long long tg, int q) {
+        const unsigned long long pre = by_count ? pre_c : pre_m;
+        auto lo = [&](int ch) { return pre + (by_count ? sm.cpc[ch] : sm.cpm[ch]); };
+        auto val = [&](int ch) { return by_count ? static_cast<unsigned long long>(sm.ccnt[ch]) : sm.cmass[ch]; };
+        const bool o0 = lo(2 * l) < tg && tg <= lo(2 * l) + val(2 * l);
+        const bool o1 = lo(2 * l + 1) < tg && tg <= lo(2 * l + 1) + val(2 * l + 1);
+        const unsigned bal = __ballot_sync(0xffffffffu, o0 || o1);
+        const int src = bal ? __ffs(bal) - 1 : 0;
+        const int ch = 2 * src + (__shfl_sync(0xffffffffu, o0 ? 1 : 0, src) ? 0 : 1);
+        const int d = 32 * ch + l;
+        const uint32_t c = sm.win[d];
+        const unsigned long long m = c ? static_cast<unsigned long long>(c) * wfix(kb - d) : 0ull;
+        const unsigned long long icn = warp_inclusive_scan_u64(c), imn = warp_inclusive_scan_u64(m);
+        const unsigned hit = __ballot_sync(0xffffffffu, lo(ch) + (by_count ? icn : imn) >= tg);
+        if (hit && l == __ffs(hit) - 1) {
+          sm.cut_key[q] = kb - static_cast<uint32_t>(d);
+          sm.cut_m[q] = pre_m + sm.cpm[ch] + imn;
+        }
+      };
+      // ---- top-k: the largest key with at least k elements at or above it
+      bool restart = false;
+      if (!have_k && pre_c + wc >= K) {
+        if (w == 0) crossing(true, K, 0);
+        __syncthreads();
+        kmin = sm.cut_key[0];
+        sk = sm.cut_m[0];
+        have_k = true;
+        // a nucleus target (top_p times the top-k mass) met above this window:
+        // count the windows again from the top
+        restart = nucleus && max(mul_fix_p(sk, tpr), 1ull) <= pre_m;
+      }
+      if (restart) {
+        kb = maxkey;
+        pre_c = 0;
+        pre_m = 0;
+        acc_pre = ff_make(0.0f);
+        __syncthreads();
+        continue;
+      }
+      // ---- nucleus: the largest key whose mass at or above it reaches top_p * S
+      if (have_k && !have_p) {
+        const unsigned long long tg = max(mul_fix_p(sk, tpr), 1ull);
+        if (pre_m + wm >= tg) {
+          if (w == 0) crossing(false, tg, 1);
+          __syncthreads();
+          tau = sm.cut_key[1];
+          ssum = sm.cut_m[1];
+          have_p = true;
+        }
+      }
+      // ---- the float-float sum of this window's keys at or above the cut
+      // (all of them when the cuts lie further down)
+      done = have_k && have_p;
+      const uint32_t cut = done ? (nucleus ? tau : kmin) : klo;
+      FF aw = ff_make(0.0f);
+      for (int ch = w; ch < kWinCh; ch += kWinNW) {
+        if (kb < cut + 32u * static_cast<uint32_t>(ch)) break;    // chunks fall in key order
+        if (sm.ccnt[ch] == 0u) continue;
+        const int d = 32 * ch + l;
+        const uint32_t c = sm.win[d];
+        if (c != 0u && kb - static_cast<uint32_t>(d) >= cut && kb - static_cast<uint32_t>(d) > kKeyNegInf)
+          aw = ff_add(aw, ff_mul(FF{static_cast<float>(c), 0.0f}, wff(kb - d)));
+      }
+      aw = win_sum_ff(aw, sm.redff[0]);
+      acc_pre = ff_add(acc_pre, aw);
+      if (done) {
+        tau = cut;
+        if (!nucleus) ssum = topk ? sk : S_fix;
+        acc = ff_add(acc_pre, acc_tail);       // acc_tail: keep-all rows only
+      } else {
+        pre_c += wc;
+        pre_m += wm;
+        // the next window starts at the largest key below this one
+        uint32_t nxt = 0u;                     // 1 + that key (0: none)
+        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+          const int nel = V - v * 8;
+          const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t kk = keys2_merged(wd[q]);
+            const uint32_t k0 = kk & 0xFFFFu, k1 = kk >> 16;
+            if (2 * q < nel && k0 < klo) nxt = max(nxt, k0 + 1u);
+            if (2 * q + 1 < nel && k1 < klo) nxt = max(nxt, k1 + 1u);
+          }
+        });
+        nxt = __reduce_max_sync(0xffffffffu, nxt);
+        __syncthreads();
+        if (l == 0) sm.redu[0][w] = nxt;
+        __syncthreads();
+        uint32_t n1 = 0u;
+#pragma unroll
+        for (int k = 0; k < kWinNW; ++k) n1 = max(n1, sm.redu[0][k]);
+        if (n1 == 0u) {
+          // no key left below: a nucleus target above the exact total mass
+          // (top_p within the sum's rounding of 1) keeps every key
+          if (have_k && !have_p && !topk) {
+            tau = 0u;
+            ssum = pre_m;
+            acc = acc_pre;
+            done = true;
+          }
+          break;
+        }
+        kb = n1 - 1u;
+      }
+      __syncthreads();
+    }
+    if (!done) valid = false;
+    if (tid == 0)
+      write_stats_ff(out, M, tau, valid, ff_from_fix44(ssum), c_hi, c_lo, -1, acc, it_hi, it_lo);
+  }
+  arrive_sequence<uint16_t>(P, i, &sm.flag[0]);
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// --------------------------------------------------------------------------
 // Phase 2: draw and append.  CTA (sequence i, chunk c): fixed-point sum of the
 // draw weights of its chunk of row n_i (residual of target/draft row n_i, or
 // the bonus target row); the last chunk to finish scans the chunk sums, finds
@@ -951,6 +1438,7 @@ constexpr int kDrawNT = 256;
 constexpr int kDrawVec = 2;          // contiguous vectors per thread in the walk
 
 struct DrawSmem {
+  float2 exp2tab[kExp2Tab];
   u128 red[kDrawNT / 32];
   u128 bc128[2];
   FF L;
@@ -992,6 +1480,66 @@ __device__ u128 chunk_sum(const T *trow, const T *drow, int V, int v0, int v1,
   return block_sum_u128<kDrawNT>(s, sm.red);
 }
 
+// Fixed-point sum of the draw weights of one run: vectors [va, va + kDrawVec)
+// clipped to v1 (one thread).
+template <typename T>
+__device__ __forceinline__ u128 run_sum(const T *trow, const T *drow, int V, int va, int v1,
+                                        const DrawWeight &dw) {
+  constexpr int EPV = LT<T>::EPV;
+  const bool two = dw.mode == 0;
+  const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
+  const bool al_d = two && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  uint4 q[kDrawVec], d[kDrawVec];
+#pragma unroll
+  for (int k = 0; k < kDrawVec; ++k) {
+    if (va + k < v1) {
+      q[k] = load_vec<T>(trow, V, va + k, al_t);
+      if (two) d[k] = load_vec<T>(drow, V, va + k, al_d);
+    }
+  }
+  u128 s = 0;
+#pragma unroll
+  for (int k = 0; k < kDrawVec; ++k) {
+    if (va + k < v1) {
+      uint32_t bq[EPV], bd[EPV];
+      unpack<T>(q[k], bq);
+      if (two) unpack<T>(d[k], bd);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) s += dw.fix<T>(bq[e], two ? bd[e] : 0u, (va + k) * EPV + e);
+    }
+  }
+  return s;
+}
+
+// The warp of the thread whose run [vf, vf + kDrawVec) holds the target walks
+// that run together: lane e recomputes element e of the run (the same weight
+// bits as the run sums), an inclusive scan over the lanes gives the running
+// sums from `lof` (the run's start), the first lane past `tgt` holds the
+// token.  Call with the whole warp; returns the token index on every lane.
+template <typename T>
+__device__ __forceinline__ int run_walk(const T *trow, const T *drow, int V, int vf, int v1,
+                                        const DrawWeight &dw, u128 lof, u128 tgt) {
+  constexpr int EPV = LT<T>::EPV;
+  constexpr int RUN = kDrawVec * EPV;
+  static_assert(RUN <= 32, "a run has at most 32 elements");
+  const bool two = dw.mode == 0;
+  const bool al_t = (reinterpret_cast<uintptr_t>(trow) & 15) == 0;
+  const bool al_d = two && (reinterpret_cast<uintptr_t>(drow) & 15) == 0;
+  const int lane = threadIdx.x & 31;
+  const bool in = lane < RUN && vf + lane / EPV < v1;
+  u128 wgt = 0;
+  if (in) {
+    const int v = vf + lane / EPV, e = lane % EPV;
+    const uint32_t eq = elem_bits<T>(load_vec<T>(trow, V, v, al_t), e);
+    const uint32_t ed = two ? elem_bits<T>(load_vec<T>(drow, V, v, al_d), e) : 0u;
+    wgt = dw.fix<T>(eq, ed, v * EPV + e);
+  }
+  const u128 cum = warp_inclusive_scan_u128(wgt);
+  const unsigned hit = __ballot_sync(0xffffffffu, in && lof + cum > tgt);
+  const unsigned inm = __ballot_sync(0xffffffffu, in);
+  return vf * EPV + (hit ? __ffs(hit) - 1 : 31 - __clz(inm));
+}
+
 // Index of the first element of vectors [v0, v1) whose running weight sum,
 // starting at 0, exceeds `tgt` (requires the chunk total > tgt).  Thread t
 // owns kDrawVec contiguous vectors, so thread order is vocabulary order.
@@ -1022,20 +1570,12 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
     u128 total;
     const u128 ex = block_exclusive_scan_u128<kDrawNT>(s, scan_red, &total);
     const u128 lo = base + ex;
-    if (s > 0 && lo <= tgt && tgt < lo + s) {
-      u128 c = lo;
-      int x = (va + kDrawVec) * EPV - 1;
-      bool found = false;
-#pragma unroll
-      for (int k = 0; k < kDrawVec; ++k)
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          if (!found && va + k < v1) {
-            c += dw.fix<T>(bq[k][e], two ? bd[k][e] : 0u, (va + k) * EPV + e);
-            if (c > tgt) { x = (va + k) * EPV + e; found = true; }
-          }
-        }
-      sm.bc[0] = x;
+    const unsigned fm = __ballot_sync(0xffffffffu, s > 0 && lo <= tgt && tgt < lo + s);
+    if (fm) {
+      const int src = __ffs(fm) - 1;
+      const int x = run_walk<T>(trow, drow, V, __shfl_sync(0xffffffffu, va, src), v1, dw,
+                                shfl_u128(lo, src), tgt);
+      if ((tid & 31) == 0) sm.bc[0] = x;
     }
     __syncthreads();
     result = sm.bc[0];
@@ -1046,9 +1586,13 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
+__global__ void __launch_bounds__(kDrawNT, 3) draw_kernel(const SampParams P) {
   __shared__ DrawSmem sm;
   __shared__ u128 scan_red[kDrawNT / 32];
+  // launched early behind the histogram statistics: nothing is read before
+  // that grid has finished (a no-op after a plain launch)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  exp2_table_fill(sm.exp2tab, P.exp2tab);
   const sv_sample_args &a = P.a;
   const int NCH = P.plan.draw_chunks;
   const int i = blockIdx.x / NCH, c = blockIdx.x - i * NCH;
@@ -1117,11 +1661,12 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
              __ldcg(&sq->c_lo), FF{__ldcg(&sq->it_hi), __ldcg(&sq->it_lo)},
              __ldcg(&sq->it_hi) == 1.0f && __ldcg(&sq->it_lo) == 0.0f, sizeof(T) == 4);
   if (mode == 0 && !dw.onehot) {
-    if (tid == 0) {                   // fp64 once per CTA, not per thread
+    __syncthreads();                  // the exp2 table
+    if (tid == 0) {                   // float-float, once per CTA
       const FF aq{__ldcg(&sq->acc_hi), __ldcg(&sq->acc_lo)};
       const FF ap{__ldcg(&sp->acc_hi), __ldcg(&sp->acc_lo)};
-      sm.L = ln_ratio_ff(ap, aq);
-      sm.inv_sq = static_cast<float>(1.0 / ff_to_double(aq));
+      sm.L = ln_ratio_ff(ap, aq, sm.exp2tab);
+      sm.inv_sq = __frcp_rn(aq.hi);   // a common factor of all weights: any rounding
     }
     __syncthreads();
     dw.rf.L = sm.L;
@@ -1132,7 +1677,12 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const int NV = (V + EPV - 1) / EPV;
   const int per = (NV + NCH - 1) / NCH;
   const int v0 = min(NV, c * per), v1 = min(NV, v0 + per);
-  const u128 cs = chunk_sum<T>(trow, drow, V, v0, v1, dw, sm);
+  // thread t's run: vectors [v0 + t kDrawVec, +kDrawVec) (a chunk has at most
+  // kDrawVec * kDrawNT vectors); the run sums are kept for the last CTA
+  const u128 st = run_sum<T>(trow, drow, V, v0 + tid * kDrawVec, v1, dw);
+  P.ws.draw_thr[(static_cast<int64_t>(i) * NCH + c) * kDrawNT + tid] = st;
+  __threadfence();
+  const u128 cs = block_sum_u128<kDrawNT>(st, sm.red);
   if (tid == 0) {
     P.ws.draw_parts[static_cast<int64_t>(i) * NCH + c] = cs;
     __threadfence();
@@ -1151,50 +1701,87 @@ __global__ void __launch_bounds__(kDrawNT) draw_kernel(const SampParams P) {
   const unsigned long long ku = u24(wv.y);
   int use_mode = mode;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    if (tid == 0) {
-      u128 Z = 0;
-      if (attempt == 0) {
-        for (int k = 0; k < NCH; ++k) Z += ldcg_u128(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
+    u128 Z = 0, tgt = 0, cum = 0;
+    int cstar = NCH - 1;
+    if (attempt == 0) {
+      // warp 0: the chunk sums in order (four per lane, draw_chunks <= 128),
+      // the total, the target floor(k Z / 2^24) and the chunk holding it
+      static_assert(kDrawNT >= 32, "one warp at least");
+      if (tid < 32) {
+        const u128 *parts = P.ws.draw_parts + static_cast<int64_t>(i) * NCH;
+        u128 z[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          z[q] = 4 * tid + q < NCH ? ldcg_u128(parts + 4 * tid + q) : static_cast<u128>(0);
+        const u128 own = z[0] + z[1] + z[2] + z[3];
+        const u128 inc = warp_inclusive_scan_u128(own);
+        const u128 Zw = shfl_u128(inc, 31);
+        const u128 tg = scale_u24(ku, Zw);
+        const u128 ex = inc - own;
+        if (tid == 0) {
+          sm.bc128[0] = Zw;
+          sm.bc128[1] = 0;
+          sm.bc[2] = NCH - 1;
+        }
+        __syncwarp();
+        if (Zw > 0 && ex <= tg && tg < inc) {     // one lane
+          u128 b = ex;
+          int q = 0;
+          while (q < 3 && tg >= b + z[q]) b += z[q++];
+          sm.bc[2] = 4 * tid + q;
+          sm.bc128[1] = b;
+        }
       }
-      sm.bc128[0] = Z;
-    }
-    __syncthreads();
-    u128 Z = sm.bc128[0];
-    if (attempt == 1) {            // fallback: q_hat of row n, chunk sums computed here
-      Z = 0;
+      __syncthreads();
+      Z = sm.bc128[0];
+      cum = sm.bc128[1];
+      cstar = sm.bc[2];
+      tgt = scale_u24(ku, Z);
+    } else {                       // fallback: q_hat of row n, chunk sums computed here
       for (int k = 0; k < NCH; ++k) {
         const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
         Z += chunk_sum<T>(trow, trow, V, a0, a1, dq, sm);
+      }
+      tgt = scale_u24(ku, Z);
+      for (int k = 0; k < NCH; ++k) {
+        const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
+        const u128 zk = chunk_sum<T>(trow, trow, V, a0, a1, dq, sm);
+        if (tgt < cum + zk) { cstar = k; break; }
+        cum += zk;
       }
     }
     if (Z == 0) {
       if (attempt == 0 && mode == 0) {
         if (tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
         use_mode = 1;
+        __syncthreads();           // sm.bc128 is rewritten by the fallback
         continue;
       }
       if (tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: cannot happen for a valid row
       return;
     }
-    const u128 tgt = scale_u24(ku, Z);          // floor(k * Z / 2^24)
-    // locate the chunk (chunk sums recomputed in the fallback)
-    u128 cum = 0;
-    int cstar = NCH - 1;
-    for (int k = 0; k < NCH; ++k) {
-      u128 zk;
-      if (use_mode == mode) {
-        zk = ldcg_u128(&P.ws.draw_parts[static_cast<int64_t>(i) * NCH + k]);
-      } else {
-        const int a0 = min(NV, k * per), a1 = min(NV, a0 + per);
-        zk = chunk_sum<T>(trow, trow, V, a0, a1, dq, sm);
-      }
-      if (tgt < cum + zk) { cstar = k; break; }
-      cum += zk;
-    }
     const int a0 = min(NV, cstar * per), a1 = min(NV, a0 + per);
-    const int x = use_mode == mode
-                      ? chunk_walk<T>(trow, drow, V, a0, a1, dw, tgt - cum, sm, scan_red)
-                      : chunk_walk<T>(trow, trow, V, a0, a1, dq, tgt - cum, sm, scan_red);
+    int x;
+    if (use_mode == mode) {
+      // the stored run sums of chunk cstar, scanned in vocabulary order; the
+      // warp of the run holding the target walks it
+      const u128 tr = tgt - cum;
+      const u128 sr = ldcg_u128(P.ws.draw_thr + (static_cast<int64_t>(i) * NCH + cstar) * kDrawNT + tid);
+      if (tid == 0) sm.bc[0] = -1;
+      u128 total;
+      const u128 ex = block_exclusive_scan_u128<kDrawNT>(sr, scan_red, &total);
+      const unsigned fm = __ballot_sync(0xffffffffu, sr > 0 && ex <= tr && tr < ex + sr);
+      if (fm) {
+        const int src = __ffs(fm) - 1;
+        const int xf = run_walk<T>(trow, drow, V, a0 + ((tid & ~31) + src) * kDrawVec, a1, dw,
+                                   shfl_u128(ex, src), tr);
+        if ((tid & 31) == 0) sm.bc[0] = xf;
+      }
+      __syncthreads();
+      x = sm.bc[0];
+    } else {
+      x = chunk_walk<T>(trow, trow, V, a0, a1, dq, tgt - cum, sm, scan_red);
+    }
     if (tid == 0) a.out_tokens[r0 + n] = x;
     return;
   }
@@ -1255,25 +1842,6 @@ struct ClusterSmem {
   int dec_use, dec_owner;
   int n;
 };
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-// Generic address of `p` in the shared memory of cluster CTA `rank`.
-template <typename X>
-__device__ __forceinline__ X *dsmem(X *p, uint32_t rank) {
-  uint64_t r;
-  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
-  return reinterpret_cast<X *>(r);
-}
 
 // 2^(d * log2(e)/T) for d = l - max <= 0 (0 for d = -inf).
 struct Ex2c {
@@ -1794,11 +2362,15 @@ SamplerPlan plan_sampler(const sv_sample_args &a) {
   const bool extended = a.temperature == 0.0f || a.top_k > 0 || a.temperatures || a.top_ps ||
                         a.top_ks;
   p.stat_chunks = a.top_p < 1.0f || extended ? 1 : std::max(1, std::min(32, (nv + 1023) / 1024));
-  p.draw_chunks = std::max(1, std::min(64, (nv + 511) / 512));
+  p.draw_chunks = std::max(1, std::min(128, (nv + 511) / 512));   // <= 512 vectors each
+  p.draw_threads = kDrawNT;
   // one cluster per sequence when there is no nucleus and the rows' slices fit
   const int per = (nv + kClusterN - 1) / kClusterN;
   p.cluster_nvt = per > kClNT ? 2 : 1;
   p.cluster = a.top_p >= 1.0f && !extended && per <= kClVPT * kClNT;
+  // bf16 rows off the cluster path: the window-histogram statistics kernel
+  p.win_stats = a.dtype == SV_BF16 ? 1 : 0;
+  if (p.win_stats) p.stat_chunks = 1;
   return p;
 }
 
@@ -1863,7 +2435,10 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
     if (e == cudaSuccess) return e;
     (void)cudaGetLastError();          // no room for a cluster: two-kernel path
   }
-  if (P.plan.stat_chunks > 1) {
+  const bool win = P.plan.win_stats != 0;
+  if (win) {
+    e = launch_first(stats_win_kernel, rows, kWinNT, 0, P, s);
+  } else if (P.plan.stat_chunks > 1) {
     e = launch_first(stats_chunk_kernel<T>, rows * P.plan.stat_chunks, kStatNT, 0, P, s);
   } else {
     const size_t smem = kSmemRowOff + kRowSmemBytes;
@@ -1873,8 +2448,19 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
     e = launch_first(stats_row_kernel<T>, rows, kSampNT, smem, P, s);
   }
   if (e != cudaSuccess) return e;
-  draw_kernel<T><<<P.a.batch * P.plan.draw_chunks, kDrawNT, 0, s>>>(P);
-  return cudaGetLastError();
+  // behind the window statistics kernel the draw starts early (it waits for
+  // the statistics grid before reading anything)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.a.batch * P.plan.draw_chunks);
+  cfg.blockDim = dim3(kDrawNT);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = win ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, draw_kernel<T>, P);
 }
 
 // 2^(j/64) for j = -32..32 as float-float pairs, from double precision
