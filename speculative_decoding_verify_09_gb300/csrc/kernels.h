@@ -49,7 +49,7 @@ struct SamplerWs {
 
 struct SamplerPlan {
   int stat_chunks;          // CTAs per row in the statistics phase (1: nucleus path)
-  int draw_chunks;          // CTAs per sequence in the draw phase (<= 128; <= 512 vectors each)
+  int draw_chunks;          // CTAs per sequence in the draw phase (<= 128; one run per thread)
   int draw_threads;         // threads per draw CTA (one run of the chunk each)
   bool cluster;             // one CTA cluster per sequence (no nucleus, rows fit in smem)
   int cluster_nvt;          // 16-byte vectors per thread and row in the cluster kernel (1, 2)

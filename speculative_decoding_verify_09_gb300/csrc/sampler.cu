@@ -980,11 +980,9 @@ constexpr int kWinNT = 256;
 constexpr int kWinNW = kWinNT / 32;
 constexpr int kWinKeys = 2048;                         // keys per window
 constexpr int kWinCh = kWinKeys / 32;                  // chunks of 32 keys
-constexpr int kWinStages = 8;                          // row vectors per thread in flight
 constexpr uint32_t kKeyNegInf = 0x007Fu;               // -inf; keys below it: NaN
 
-struct WinSmem {
-  uint4 ring[kWinStages][kWinNT];                      // the row stream's slots
+struct WinSmem {                                       // (the row stream's ring follows)
   unsigned long long cmass[kWinCh], cpm[kWinCh];       // per chunk: 2^-44 mass, its prefix
   uint32_t win[kWinKeys];                              // count of key kb - d at d
   uint32_t ccnt[kWinCh], cpc[kWinCh];                  // per chunk: count, its prefix
@@ -1012,14 +1010,15 @@ __device__ __forceinline__ uint32_t keys2_of(uint32_t wd) {
 
 // f(v, vector) for every 16-byte vector of the row this thread owns (v =
 // k * kWinNT + tid, in increasing order).  An aligned row streams through a
-// ring of kWinStages 16-byte slots per thread in shared memory, filled by
-// cp.async kWinStages vectors ahead (deep prefetch without registers; each
-// thread reads only its own slots, so no barrier); a slot is refilled after
-// its vector has been used.  An unaligned row, and a row's ragged last
-// vector, use plain loads.  Elements past V read as -inf.
-template <typename F>
+// ring of STAGES 16-byte slots per thread in shared memory (slot s of thread
+// t at ring[s * kWinNT + t]), filled by cp.async STAGES vectors ahead: deep
+// prefetch without registers; each thread reads only its own slots, so no
+// barrier; a slot is refilled after its vector has been used.  An unaligned
+// row, and a row's ragged last vector, use plain loads.  Elements past V read
+// as -inf.
+template <int STAGES, typename F>
 __device__ __forceinline__ void win_stream(const uint16_t *row, int V, int NV, bool aligned,
-                                           uint4 (*ring)[kWinNT], F &&f) {
+                                           uint4 *ring, F &&f) {
   const int tid = threadIdx.x;
   if (!aligned) {
 #pragma unroll 1
@@ -1028,24 +1027,31 @@ __device__ __forceinline__ void win_stream(const uint16_t *row, int V, int NV, b
   }
   auto issue = [&](int v, int slot) {
     if (v < NV) {
-      uint4 *dst = &ring[slot][tid];
+      uint4 *dst = ring + slot * kWinNT + tid;
       if (v * 8 + 8 <= V) cp_async16(smem_u32(dst), row + v * 8, 16);
       else *dst = load_vec<uint16_t>(row, V, v, true);
     }
     cp_async_commit();                           // one group per step (maybe empty)
   };
 #pragma unroll
-  for (int k = 0; k < kWinStages; ++k) issue(k * kWinNT + tid, k);
+  for (int k = 0; k < STAGES; ++k) issue(k * kWinNT + tid, k);
   int slot = 0;
 #pragma unroll 1
   for (int v = tid; v < NV; v += kWinNT) {
-    cp_async_wait<kWinStages - 1>();             // this thread's oldest group has landed
-    const uint4 cur = ring[slot][tid];
+    cp_async_wait<STAGES - 1>();                 // this thread's oldest group has landed
+    const uint4 cur = ring[slot * kWinNT + tid];
     f(v, cur);
-    issue(v + kWinStages * kWinNT, slot);
-    slot = slot + 1 == kWinStages ? 0 : slot + 1;
+    issue(v + STAGES * kWinNT, slot);
+    slot = slot + 1 == STAGES ? 0 : slot + 1;
   }
   cp_async_wait<0>();
+}
+
+// Per-half maximum of two bf16 pairs; a NaN half wins (NaN propagates).
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // Keys of the two bf16 values of a word with -0 taken as +0 (as key_of_bf16).
@@ -1124,9 +1130,14 @@ __device__ __forceinline__ unsigned long long fix44_ff(FF x) {
          static_cast<unsigned long long>(__float2ll_rn(__fmul_rn(x.lo, 0x1p44f)));
 }
 
-__global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P) {
+constexpr size_t kWinSmemOff = (sizeof(WinSmem) + 127) / 128 * 128;   // the ring's offset
+
+template <int STAGES>
+__global__ void __launch_bounds__(kWinNT, 2) stats_win_kernel(const SampParams P) {
   const PdlTail tail{P.pdl_secondary};
-  __shared__ WinSmem sm;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  WinSmem &sm = *reinterpret_cast<WinSmem *>(smem_raw);
+  uint4 *ring = reinterpret_cast<uint4 *>(smem_raw + kWinSmemOff);
   const sv_sample_args &a = P.a;
   const int r = blockIdx.x;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
@@ -1149,30 +1160,22 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
     if (!param_ok) set_status(a.dev_status, SV_DEV_BAD_PARAM);
     if (a.temperatures && param_ok && Tr > 0.0f) temp_consts(Tr, sm.tconst);
   }
-  // ---- pass 1: the largest and smallest key (elements past V read as -inf:
-  // neither NaN nor a maximum unless every logit is -inf)
-  uint32_t kmax2 = 0u, kmin2 = 0xFFFFFFFFu;
-  win_stream(row, V, NV, aligned, sm.ring, [&](int, const uint4 &x) {
-    const uint32_t k0 = keys2_of(x.x), k1 = keys2_of(x.y), k2 = keys2_of(x.z), k3 = keys2_of(x.w);
-    kmax2 = __vmaxu2(kmax2, __vmaxu2(__vmaxu2(k0, k1), __vmaxu2(k2, k3)));
-    kmin2 = __vminu2(kmin2, __vminu2(__vminu2(k0, k1), __vminu2(k2, k3)));
+  // ---- pass 1: the largest value, NaN propagating (elements past V read as
+  // -inf: no maximum unless every logit is -inf)
+  uint32_t mx2 = 0xFF80FF80u;
+  win_stream<STAGES>(row, V, NV, aligned, ring, [&](int, const uint4 &x) {
+    mx2 = bmax2_nan(mx2, bmax2_nan(bmax2_nan(x.x, x.y), bmax2_nan(x.z, x.w)));
   });
-  uint32_t tmax = max(kmax2 & 0xFFFFu, kmax2 >> 16), tmin = min(kmin2 & 0xFFFFu, kmin2 >> 16);
+  const uint32_t mb = bmax2_nan(mx2, mx2 >> 16) & 0xFFFFu;
+  // a NaN maximum takes the largest key, so the reduction keeps it
+  uint32_t tmax = (mb & 0x7FFFu) > 0x7F80u ? 0xFFFFu : key_of_bf16(mb);
   tmax = __reduce_max_sync(0xffffffffu, tmax);
-  tmin = __reduce_min_sync(0xffffffffu, tmin);
-  if (l == 0) {
-    sm.redu[0][w] = tmax;
-    sm.redu[1][w] = tmin;
-  }
+  if (l == 0) sm.redu[0][w] = tmax;
   __syncthreads();
-  uint32_t maxkey = 0u, minkey = 0xFFFFu;
+  uint32_t maxkey = 0u;
 #pragma unroll
-  for (int k = 0; k < kWinNW; ++k) {
-    maxkey = max(maxkey, sm.redu[0][k]);
-    minkey = min(minkey, sm.redu[1][k]);
-  }
-  if (maxkey == 0x7FFFu) maxkey = 0x8000u;      // -0 and +0: one key (as key_of_bf16)
-  const bool bad = maxkey >= 0xFF80u || minkey < kKeyNegInf;
+  for (int k = 0; k < kWinNW; ++k) maxkey = max(maxkey, sm.redu[0][k]);
+  const bool bad = maxkey >= 0xFF80u;              // +inf or NaN
   bool valid = param_ok && !bad && maxkey > kKeyNegInf;          // some finite logit
   const float M = valid ? key_value(maxkey) : -INFINITY;
   RowStats *out = &P.ws.stats[r];
@@ -1183,7 +1186,7 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
     // ---- greedy: one-hot at the lowest index holding the maximum (values
     // compared, so -0 and +0 are equal); a thread's vectors come in order
     int first = INT_MAX;
-    win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+    win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
       uint32_t b[8];
       unpack<uint16_t>(x, b);
 #pragma unroll
@@ -1221,7 +1224,12 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
     bool have_k = !topk, have_p = !nucleus, done = false;
     uint32_t kmin = 0u, tau = 0u;
     for (int it = 0; it < 64 && !done; ++it) {   // 32 windows cover every key
-      const uint32_t klo = kb >= kWinKeys - 1 ? kb - (kWinKeys - 1) : 0u;
+      // The first pass takes keys raw (-0 one below +0, merged into it after
+      // the pass); its window ends one key higher when its last slot would
+      // hold +0, so the two zeros are never split.  Later passes use merged keys.
+      const uint32_t wlim =
+          it == 0 && kb - 0x8000u == static_cast<uint32_t>(kWinKeys - 1) ? kWinKeys - 1 : kWinKeys;
+      const uint32_t klo = kb >= wlim - 1 ? kb - (wlim - 1) : 0u;   // the window: keys [klo, kb]
       for (int d = tid; d < kWinKeys; d += kWinNT) sm.win[d] = 0u;
       __syncthreads();
       // ---- pass 2: count the window's keys; the first pass also sums every
@@ -1238,7 +1246,7 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
           for (int h = 0; h < 2; ++h) {
             const bool live = 2 * q + h < nel;
             const uint32_t d = kb - (h ? (kk >> 16) : (kk & 0xFFFFu));   // keys above kb wrap
-            if (live && d < static_cast<uint32_t>(kWinKeys)) atomicAdd(&sm.win[d], 1u);
+            if (live && d < wlim) atomicAdd(&sm.win[d], 1u);
             if (sum) {
               const float lv = __uint_as_float(h ? (wd[q] & 0xFFFF0000u) : (wd[q] << 16));
               const float dl = __fsub_rn(lv, M);                        // -inf -> weight 0
@@ -1255,13 +1263,45 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
         }
       };
       if (it == 0) {
-        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) { count_vec(x, V - v * 8, true); });
+        // (no key exceeds kb in the first pass)
+        const float2 nm2 = make_float2(-M, -M), ch2 = make_float2(mc_hi, mc_hi), cl2 = make_float2(mc_lo, mc_lo);
+        win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
+          if (v * 8 + 8 > V) {                 // the ragged last vector
+            count_vec(x, V - v * 8, true);
+            return;
+          }
+          const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+          float2 vs2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t kk = keys2_of(wd[q]);
+            const uint32_t d0 = kb - (kk & 0xFFFFu), d1 = kb - (kk >> 16);
+            if (d0 < wlim) atomicAdd(&sm.win[d0], 1u);
+            if (d1 < wlim) atomicAdd(&sm.win[d1], 1u);
+            const float2 lv = make_float2(__uint_as_float(wd[q] << 16), __uint_as_float(wd[q] & 0xFFFF0000u));
+            const float2 dl = __fadd2_rn(lv, nm2);                     // -inf -> weight 0
+            const float2 ag = __ffma2_rn(dl, ch2, __fmul2_rn(dl, cl2));
+            vs2 = __fadd2_rn(vs2, make_float2(fast_exp2(ag.x), fast_exp2(ag.y)));
+          }
+          const float y = __fsub_rn(__fadd_rn(vs2.x, vs2.y), sc);
+          const float t = __fadd_rn(s, y);
+          sc = __fsub_rn(__fsub_rn(t, s), y);
+          s = t;
+        });
+        __syncthreads();
+        if (tid == 0 && kb >= 0x8000u) {       // -0 (key 0x7FFF) into +0
+          const uint32_t dz = kb - 0x8000u;
+          if (dz + 1u < wlim) {
+            sm.win[dz] += sm.win[dz + 1u];
+            sm.win[dz + 1u] = 0u;
+          }
+        }
       } else {
-        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) { count_vec(x, V - v * 8, false); });
+        win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) { count_vec(x, V - v * 8, false); });
       }
       FF at = ff_make(0.0f);                   // keep-all rows: float-float tail weights
       if (it == 0 && keep_all) {
-        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+        win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
           const int nel = min(8, V - v * 8);
 #pragma unroll 1
           for (int e = 0; e < nel; ++e) {
@@ -1386,7 +1426,7 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
         pre_m += wm;
         // the next window starts at the largest key below this one
         uint32_t nxt = 0u;                     // 1 + that key (0: none)
-        win_stream(row, V, NV, aligned, sm.ring, [&](int v, const uint4 &x) {
+        win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
           const int nel = V - v * 8;
           const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -1435,7 +1475,7 @@ __global__ void __launch_bounds__(kWinNT, 4) stats_win_kernel(const SampParams P
 // slice of block rows 0..n_i to the KV pool (fused step).
 // --------------------------------------------------------------------------
 constexpr int kDrawNT = 256;
-constexpr int kDrawVec = 2;          // contiguous vectors per thread in the walk
+constexpr int kDrawVec = 2;          // contiguous vectors per thread (one run)
 
 struct DrawSmem {
   float2 exp2tab[kExp2Tab];
@@ -2362,7 +2402,8 @@ SamplerPlan plan_sampler(const sv_sample_args &a) {
   const bool extended = a.temperature == 0.0f || a.top_k > 0 || a.temperatures || a.top_ps ||
                         a.top_ks;
   p.stat_chunks = a.top_p < 1.0f || extended ? 1 : std::max(1, std::min(32, (nv + 1023) / 1024));
-  p.draw_chunks = std::max(1, std::min(128, (nv + 511) / 512));   // <= 512 vectors each
+  // one run of kDrawVec vectors per thread: chunks of at most kDrawVec * kDrawNT vectors
+  p.draw_chunks = std::max(1, std::min(128, (nv + kDrawVec * kDrawNT - 1) / (kDrawVec * kDrawNT)));
   p.draw_threads = kDrawNT;
   // one cluster per sequence when there is no nucleus and the rows' slices fit
   const int per = (nv + kClusterN - 1) / kClusterN;
@@ -2437,7 +2478,14 @@ static cudaError_t launch_t(const SampParams &P, cudaStream_t s) {
   }
   const bool win = P.plan.win_stats != 0;
   if (win) {
-    e = launch_first(stats_win_kernel, rows, kWinNT, 0, P, s);
+    // ring depth 16: a 32k row is read whole at once (16 vectors per thread)
+    constexpr int kStages = 16;
+    auto kern = stats_win_kernel<kStages>;
+    const int stages = kStages;
+    const int smem = static_cast<int>(kWinSmemOff) + stages * kWinNT * 16;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = launch_first(kern, rows, kWinNT, static_cast<size_t>(smem), P, s);
   } else if (P.plan.stat_chunks > 1) {
     e = launch_first(stats_chunk_kernel<T>, rows * P.plan.stat_chunks, kStatNT, 0, P, s);
   } else {

@@ -241,6 +241,30 @@ def test_top_k_tie_heavy_and_fp32(api):
     check(api, inp)
 
 
+@pytest.mark.parametrize("max_bits", [0x0000, 0x07FF, 0x0100])
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (0, 0.5), (3, 1.0), (100, 0.7)])
+def test_signed_zeros_and_window_edges(api, max_bits, top_k, top_p):
+    """Rows of +0, -0 and a few negative logits, one of them raised to the
+    row maximum.  The two zeros are one value for the oracle's comparisons,
+    so one tie class.  The maxima: 0 itself; the bf16 pattern 0x07FF, whose
+    order-preserving key is 2047 above +0's (+0 would be the last key of a
+    2048-key window below the maximum); and 0x0100, 256 keys above.  Cuts
+    among the zeros and the negatives lie below such a window."""
+    rng = np.random.default_rng(max_bits + 7 * top_k)
+    inp = sampler_inputs("ragged_gqa_b32", B=6, V=3000, gen_seed=49, top_p=top_p)
+    inp["top_k"] = top_k
+    vals = np.array([0x0000, 0x8000, 0xBF80, 0xC000, 0xBF00], dtype=np.uint16)   # +0 -0 -1 -2 -0.5
+
+    def rows(n):
+        r = vals[rng.integers(0, len(vals), size=(n, inp["V"]))]
+        r[np.arange(n), rng.integers(0, inp["V"], size=n)] = np.uint16(max_bits)
+        return r
+
+    inp["target_logits"] = rows(inp["target_logits"].shape[0])
+    inp["draft_logits"] = rows(inp["draft_logits"].shape[0])
+    check(api, inp, tie_bound=False)
+
+
 def test_top_k_large_vocab(api):
     inp = sampler_inputs("vocab128k_b64", B=6, top_k=50, gen_seed=46)
     check(api, inp)
