@@ -63,9 +63,10 @@ DEV_BAD_PARAM = 64
 # sequence).  TIE_EPS is the stated window of the accept compare and of the
 # residual / bonus CDF at the drawn token.
 TIE_EPS = 1e-5
-# Nucleus cut window: the cut compares a mass with top_p; an fp32 path with
-# fp64 cross-thread sums gets that mass to ~5e-7, so boundaries within 2e-6 of
-# top_p are treated as ties (the 1e-5 windows above are for u comparisons).
+# Nucleus cut window: the cut compares a mass with top_p; an fp32 path (fp32
+# weights, exact sums of them) gets that mass to ~5e-7, so boundaries within
+# 2e-6 of top_p are treated as ties (the 1e-5 windows above are for u
+# comparisons).
 NUCLEUS_TIE_EPS = 2e-6
 TIE_ACCEPT = 1
 TIE_DRAW = 2

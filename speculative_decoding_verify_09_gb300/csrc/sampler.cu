@@ -7,27 +7,30 @@
 // from the last target row.  Same section: temperature / nucleus modify the
 // probabilities before the scheme.  Batch without padding: EMS-SD abstract.
 //
-// Three paths, chosen on the host (plan_sampler):
-//  * Cluster path (top_p >= 1, slice of a row <= 512 vectors per CTA): one
-//    thread-block cluster of 8 CTAs per sequence, every phase exchanged through
-//    distributed shared memory; a few KB of shared memory per CTA, so in the
-//    fused step it runs beside the attention's CTAs (see the cluster kernel).
-//  * Chunked statistics (top_p >= 1, longer rows, or no room for a cluster):
-//    CTA (row, chunk) -> the last chunk of a row merges, the last row of a
-//    sequence runs the accept tests; then the draw kernel.
-//  * Nucleus path (top_p < 1): one CTA per row streams it once from HBM into
-//    shared memory (or from L2 when longer than 64 KB) and finds max, sum and
-//    the tie-inclusive nucleus cut on chip; the last row of a sequence runs the
-//    accept tests; then the draw kernel (per-sequence chunks of row n_i) draws
-//    and, in the fused step, appends the accepted K/V rows.
+// Paths, chosen on the host (plan_sampler):
+//  * Cluster path (bf16 or fp32, no nucleus, no top-k, T > 0, a row slice of
+//    at most 512 vectors per CTA): one thread-block cluster of 8 CTAs per
+//    sequence, every phase exchanged through distributed shared memory; a few
+//    KB of shared memory per CTA, so in the fused step it runs beside the
+//    attention's CTAs (see the cluster kernel).
+//  * Window statistics (other bf16 rows: nucleus, top-k, greedy, per-sequence
+//    parameters, long rows): one CTA per row counts the keys of a window below
+//    the row maximum and takes every cut per distinct value (see the window
+//    kernel); the last row of a sequence runs the accept tests.
+//  * fp32 rows otherwise: chunked statistics (no nucleus: CTA (row, chunk),
+//    the last chunk of a row merges) or one CTA per row with a nucleus search
+//    over weight-exponent bins.
+//  After the statistics, the draw kernel (per-sequence chunks of row n_i)
+//  draws and, in the fused step, appends the accepted K/V rows.
 //
 // Precision: per-element weights 2^((l - lmax) log2(e)/T) in fp32 by the SFU's
-// approximate exp2 (the two statistics paths: float-float sums; the cluster
-// path: fp32 (max, sum) merges, relative error below ~2e-6);
-// the accept test compares u * p_hat < q_hat in fp32; the inverse-CDF draw
-// accumulates exact 64-bit fixed-point weights (2^-52 units), so the chosen
-// index does not depend on the summation order.  The near-tie windows of the
-// decisions (1e-5) are far wider than these errors.
+// approximate exp2 (relative error ~2^-22); the accept test compares
+// u * p_hat < q_hat in fp32; the residual max(0, q_hat - p_hat) is evaluated
+// with relative accuracy (ResidualFn: the logit differences in float-float,
+// ln(S_p / S_q) from float-float sums); the inverse-CDF draws accumulate exact
+// fixed-point weights, so the chosen index does not depend on the summation
+// order.  No fp64 on the device (a small fraction of the fp32 rate here).  The
+// near-tie windows of the decisions (1e-5) are far wider than these errors.
 #include <algorithm>
 #include <cmath>
 
