@@ -1252,7 +1252,7 @@ __global__ void __launch_bounds__(kWinNT, 2) stats_win_kernel(const SampParams P
             if (live && d < wlim) atomicAdd(&sm.win[d], 1u);
             if (sum) {
               const float lv = __uint_as_float(h ? (wd[q] & 0xFFFF0000u) : (wd[q] << 16));
-              const float dl = __fsub_rn(lv, M);                        // -inf -> weight 0
+              const float dl = fmaxf(__fsub_rn(lv, M), -1.0e30f);       // -inf: weight 0, never NaN
               const float wv = fast_exp2(__fmaf_rn(dl, mc_hi, __fmul_rn(dl, mc_lo)));
               vs = __fadd_rn(vs, live ? wv : 0.0f);
             }
@@ -1282,7 +1282,11 @@ __global__ void __launch_bounds__(kWinNT, 2) stats_win_kernel(const SampParams P
             if (d0 < wlim) atomicAdd(&sm.win[d0], 1u);
             if (d1 < wlim) atomicAdd(&sm.win[d1], 1u);
             const float2 lv = make_float2(__uint_as_float(wd[q] << 16), __uint_as_float(wd[q] & 0xFFFF0000u));
-            const float2 dl = __fadd2_rn(lv, nm2);                     // -inf -> weight 0
+            // a masked (-inf) logit: the difference is clamped to a huge
+            // negative finite value, so that -inf * c_hi + (-inf) * c_lo (c_lo
+            // may be negative) cannot give NaN; its weight is 0
+            float2 dl = __fadd2_rn(lv, nm2);
+            dl = make_float2(fmaxf(dl.x, -1.0e30f), fmaxf(dl.y, -1.0e30f));
             const float2 ag = __ffma2_rn(dl, ch2, __fmul2_rn(dl, cl2));
             vs2 = __fadd2_rn(vs2, make_float2(fast_exp2(ag.x), fast_exp2(ag.y)));
           }
@@ -2205,8 +2209,8 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     wa = 0;
     wb = 0;
     gterm = 0.0f;
-    if (use == 1) {
-      wa = fix63(rf.qhat(lq));
+    if (use == 1) {                                // (a masked token weighs 0)
+      wa = lq == -INFINITY ? 0ull : fix63(rf.qhat(lq));
       return;
     }
     const float lp = LT<T>::val(bd);

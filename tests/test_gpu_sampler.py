@@ -189,6 +189,32 @@ def test_bad_tokens_nonfinite_and_masked_rows(api):
     assert np.all(toks[cu[5]:cu[6]][toks[cu[5]:cu[6]] >= 0] >= 400)
 
 
+@pytest.mark.parametrize("top_p", [1.0, 0.9])
+def test_masked_tokens_at_any_temperature(api, top_p):
+    """Masked (-inf) logits at T = 0.8, whose log2(e)/T splits into a float
+    pair with a negative low part (so an unguarded -inf * c_hi + -inf * c_lo
+    would be NaN), on a vocabulary that is not a multiple of 8 (the last
+    vector of a row is padded with -inf): the cluster path (top_p 1) and the
+    window statistics (top_p 0.9)."""
+    inp = sampler_inputs("bass_b8", B=6, V=32003, gen_seed=51, temperature=0.8, top_p=top_p)
+    cu = inp["cu_q"]
+    rng = np.random.default_rng(52)
+    for r in range(inp["target_logits"].shape[0]):
+        inp["target_logits"][r, rng.choice(32003, size=2000, replace=False)] = np.uint16(0xFF80)
+    for r in range(inp["draft_logits"].shape[0]):
+        inp["draft_logits"][r, rng.choice(32003, size=3000, replace=False)] = np.uint16(0xFF80)
+    inp["draft_tokens"] = np.where(
+        W.bf16_bits_to_f32(inp["draft_logits"][np.arange(len(inp["draft_tokens"])), inp["draft_tokens"]]) == -np.inf,
+        0, inp["draft_tokens"]).astype(np.int32)
+    d, ref, _ = check(api, inp)
+    assert ref["status"] == 0 and np.all(d.num_accepted.cpu().numpy() >= 0)
+    toks = d.out_tokens.cpu().numpy()
+    for i in range(inp["B"]):
+        n = int(d.num_accepted[i])
+        x = int(toks[cu[i] + n])
+        assert W.bf16_bits_to_f32(inp["target_logits"][cu[i] + n, x]) > -np.inf
+
+
 def test_deterministic_and_seq_id_keyed(api):
     inp = sampler_inputs("ragged_gqa_b32", B=16, V=2048, gen_seed=21)
     a = run_sampler(api, inp)
