@@ -1165,9 +1165,29 @@ __global__ void __launch_bounds__(kWinNT, 2) stats_win_kernel(const SampParams P
   }
   // ---- pass 1: the largest value, NaN propagating (elements past V read as
   // -inf: no maximum unless every logit is -inf)
+  // Greedy rows also keep each thread's first index of its running maximum
+  // (a thread's vectors come in increasing order, so a later equal value
+  // never replaces it; values are compared, so -0 and +0 are equal).
   uint32_t mx2 = 0xFF80FF80u;
-  win_stream<STAGES>(row, V, NV, aligned, ring, [&](int, const uint4 &x) {
-    mx2 = bmax2_nan(mx2, bmax2_nan(bmax2_nan(x.x, x.y), bmax2_nan(x.z, x.w)));
+  const bool greedy = Tr == 0.0f;
+  float gbest = -INFINITY;
+  int gidx = INT_MAX;
+  win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
+    const uint32_t v2 = bmax2_nan(bmax2_nan(x.x, x.y), bmax2_nan(x.z, x.w));
+    mx2 = bmax2_nan(mx2, v2);
+    if (greedy) {
+      const float vm = fmaxf(__uint_as_float(v2 << 16), __uint_as_float(v2 & 0xFFFF0000u));
+      if (vm > gbest) {
+        uint32_t b[8];
+        unpack<uint16_t>(x, b);
+        int e0 = 7;
+#pragma unroll
+        for (int e = 7; e >= 0; --e)
+          if (LT<uint16_t>::val(b[e]) == vm) e0 = e;
+        gbest = vm;
+        gidx = v * 8 + e0;
+      }
+    }
   });
   const uint32_t mb = bmax2_nan(mx2, mx2 >> 16) & 0xFFFFu;
   // a NaN maximum takes the largest key, so the reduction keeps it
@@ -1186,16 +1206,9 @@ __global__ void __launch_bounds__(kWinNT, 2) stats_win_kernel(const SampParams P
     if (tid == 0)
       write_stats_ff(out, M, 0u, false, FF{0.0f, 0.0f}, 0.0f, 0.0f, -1, FF{0.0f, 0.0f}, 0.0f, 0.0f);
   } else if (Tr == 0.0f) {
-    // ---- greedy: one-hot at the lowest index holding the maximum (values
-    // compared, so -0 and +0 are equal); a thread's vectors come in order
-    int first = INT_MAX;
-    win_stream<STAGES>(row, V, NV, aligned, ring, [&](int v, const uint4 &x) {
-      uint32_t b[8];
-      unpack<uint16_t>(x, b);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (first == INT_MAX && LT<uint16_t>::val(b[e]) == M) first = v * 8 + e;
-    });
+    // ---- greedy: one-hot at the lowest index holding the maximum: the
+    // smallest first index among the threads whose running maximum is it
+    int first = gbest == M ? gidx : INT_MAX;
     first = __reduce_min_sync(0xffffffffu, first);
     __syncthreads();
     if (l == 0) sm.redu[0][w] = static_cast<uint32_t>(first);
@@ -1704,6 +1717,16 @@ __global__ void __launch_bounds__(kDrawNT, 3) draw_kernel(const SampParams P) {
   dw.pp = mode == 0 ? rowprob_of(sp) : dw.pq;
   dw.mode = mode;
   dw.onehot = dw.pq.amax >= 0 || dw.pp.amax >= 0;
+  if (dw.pq.amax >= 0 && (mode == 1 || dw.pp.amax >= 0)) {
+    // greedy rows (one-hot q_hat and p_hat): the bonus draw, and the residual
+    // of a rejection, are one-hot at the target row's maximum; when both rows
+    // peak at the same index the residual is empty and the draw takes q_hat
+    if (c == 0 && tid == 0) {
+      if (mode == 0 && dw.pp.amax == dw.pq.amax) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
+      a.out_tokens[r0 + n] = dw.pq.amax;
+    }
+    return;
+  }
   dw.rf.init(__ldcg(&sq->lmax), mode == 0 ? __ldcg(&sp->lmax) : 0.0f, __ldcg(&sq->c_hi),
              __ldcg(&sq->c_lo), FF{__ldcg(&sq->it_hi), __ldcg(&sq->it_lo)},
              __ldcg(&sq->it_hi) == 1.0f && __ldcg(&sq->it_lo) == 0.0f, sizeof(T) == 4);
