@@ -1646,7 +1646,7 @@ __device__ int chunk_walk(const T *trow, const T *drow, int V, int v0, int v1,
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kDrawNT, 3) draw_kernel(const SampParams P) {
+__global__ void __launch_bounds__(kDrawNT, 4) draw_kernel(const SampParams P) {
   __shared__ DrawSmem sm;
   __shared__ u128 scan_red[kDrawNT / 32];
   // launched early behind the histogram statistics: nothing is read before
