@@ -1921,6 +1921,47 @@ struct Ex2c {
   }
 };
 
+// expm1_fast(x) without a branch: both of its forms, then the one it would
+// take (the same operations, so the same bits).  Unrolled over a vector, the
+// elements' chains interleave instead of running one after another.
+__device__ __forceinline__ float expm1_sel(float x) {
+  float p = 1.0f / 40320.0f;
+  p = __fmaf_rn(p, x, 1.0f / 5040.0f);
+  p = __fmaf_rn(p, x, 1.0f / 720.0f);
+  p = __fmaf_rn(p, x, 1.0f / 120.0f);
+  p = __fmaf_rn(p, x, 1.0f / 24.0f);
+  p = __fmaf_rn(p, x, 1.0f / 6.0f);
+  p = __fmaf_rn(p, x, 0.5f);
+  p = __fmaf_rn(p, x, 1.0f);
+  const float taylor = __fmul_rn(p, x);
+  const float viaexp = __fsub_rn(fast_exp2(__fmul_rn(x, 1.4426950408889634f)), 1.0f);
+  return fabsf(x) < 0.35f ? taylor : viaexp;
+}
+
+// fix63(r) for r in [0, 2) by one conversion: r * 2^63 is exact (a power of
+// two) and below 2^64, and truncation toward zero is the floor that fix63's
+// shifts take; subnormal r and -0 give 0 in both.  The draw weights lie in
+// [0, 1] (probabilities and their parts), so the fast loops use this form and
+// the walker's recomputation (fix63) sees the same integers.
+__device__ __forceinline__ unsigned long long fix63_cvt(float r) {
+  return __float2ull_rz(__fmul_rn(r, 0x1p63f));
+}
+
+// Whether any element of a row vector is -inf (a masked token, or past V).
+template <typename T>
+__device__ __forceinline__ bool vec_has_neg_inf(const uint4 x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  bool any = false;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (LT<T>::EPV == 8)
+      any = any || (w[k] & 0xFFFFu) == 0xFF80u || (w[k] >> 16) == 0xFF80u;
+    else
+      any = any || w[k] == 0xFF800000u;
+  }
+  return any;
+}
+
 // (m, s) <- merge of two (max, sum of weights relative to max) pairs.
 __device__ __forceinline__ void ms_merge(float &m, float &s, float m2, float s2, const Ex2c &e) {
   const float mn = fmaxf(m, m2);
@@ -2270,17 +2311,43 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     for (int v = ra; v < rb; ++v) {
       const uint4 xq = load_vec<T>(rq, V, v0 + v, alq);
       const uint4 xd = use != 1 ? load_vec<T>(rd, V, v0 + v, ald) : xq;
+      const bool masked = vec_has_neg_inf<T>(xq) || (use == 0 && vec_has_neg_inf<T>(xd));
+      if (use == 0 && !masked) {
+        // every logit finite: weights() of use 0 without branches
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float lq = LT<T>::val(elem_bits<T>(xq, e)), lp = LT<T>::val(elem_bits<T>(xd, e));
+          const float qh = rf.qhat(lq);
+          const float d = rf.arg(lq, lp, rf.L);
+          const float em = expm1_sel(d);
+          const float gt = __fmul_rn(qh, em);
+          const bool neg = d < 0.0f;
+          sa += fix63_cvt(neg ? -gt : 0.0f);
+          sb += fix63_cvt(neg ? __fmaf_rn(qh, em, qh) : 0.0f);
+          dneg = neg ? fminf(dneg, -d) : dneg;
+          dpos = neg ? dpos : fminf(dpos, d);
+          const float y = __fsub_rn(gt, gc);
+          const float t2 = __fadd_rn(gs, y);
+          gc = __fsub_rn(__fsub_rn(t2, gs), y);
+          gs = t2;
+        }
+      } else if (use == 1 && !masked) {
+        // the bonus draw (or the empty-residual fallback): q_hat alone
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) sa += fix63_cvt(rf.qhat(LT<T>::val(elem_bits<T>(xq, e))));
+      } else {
 #pragma unroll 1
-      for (int e = 0; e < EPV; ++e) {
-        unsigned long long wa, wb;
-        float gt;
-        weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), wa, wb, gt);
-        sa += wa;
-        sb += wb;
-        const float y = __fsub_rn(gt, gc);
-        const float t2 = __fadd_rn(gs, y);
-        gc = __fsub_rn(__fsub_rn(t2, gs), y);
-        gs = t2;
+        for (int e = 0; e < EPV; ++e) {
+          unsigned long long wa, wb;
+          float gt;
+          weights(use, elem_bits<T>(xq, e), elem_bits<T>(xd, e), wa, wb, gt);
+          sa += wa;
+          sb += wb;
+          const float y = __fsub_rn(gt, gc);
+          const float t2 = __fadd_rn(gs, y);
+          gc = __fsub_rn(__fsub_rn(t2, gs), y);
+          gs = t2;
+        }
       }
     }
     unsigned long long ta, tb = 0;
