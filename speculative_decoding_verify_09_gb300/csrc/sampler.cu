@@ -254,6 +254,14 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+// The two halves of cluster_sync_all, for a CTA with work left between its
+// last read of another CTA's shared memory and its exit.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 
 // Generic address of `p` in the shared memory of cluster CTA `rank`.
 template <typename X>
@@ -2305,6 +2313,7 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   };
   FF rf_L_exact = FF{0.0f, 0.0f};
   int use = mode;
+  bool arrived = false;                            // at the exit barrier (3)
   for (int round = 0; round < 3; ++round) {
     unsigned long long sa = 0, sb = 0;
     float gs = 0.0f, gc = 0.0f;                    // Kahan sum of G's terms
@@ -2450,6 +2459,11 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
       if (k == 0 && tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: not for a valid row
       break;
     }
+    // The last round: this CTA has read all it needs from the others, so it
+    // arrives at the exit barrier now and the owner walks while the others
+    // leave (the walk touches only this CTA's own shared memory).
+    cluster_arrive();
+    arrived = true;
     if (sm.dec_owner) {                            // uniform within the CTA
       const long long beta = sm.dec_beta;
       const i128 tg = sm.dec_tg;
@@ -2486,7 +2500,8 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     }
     break;
   }
-  cluster_sync_all();                              // (3) no CTA leaves while its totals are read
+  if (!arrived) cluster_arrive();
+  cluster_wait();                                  // (3) no CTA leaves while its totals are read
 }
 
 }  // namespace
