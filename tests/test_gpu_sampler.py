@@ -157,6 +157,35 @@ def test_p_equals_q_accepts_all(api):
     assert np.all(d.num_accepted.cpu().numpy() == np.diff(cu) - 1)
 
 
+@pytest.mark.parametrize("V", [32003, 4096])
+def test_p_equals_q_masked_bonus_draws(api, V):
+    """Every draft accepted (draft rows equal the target rows), so each
+    sequence draws its bonus token from q_hat, with masked (-inf) logits at
+    T = 0.8: in the cluster path the vectors of finite logits take the
+    branch-free run sums and those holding a masked token (or the -inf padding
+    past V = 32003) the general form, and the walk that finds the token
+    recomputes its run with the general form, so the two must give the same
+    integers for the drawn token to match the oracle's."""
+    inp = sampler_inputs("bass_b8", B=6, V=V, gen_seed=61, temperature=0.8)
+    cu = inp["cu_q"]
+    rng = np.random.default_rng(62)
+    for r in range(inp["target_logits"].shape[0]):
+        inp["target_logits"][r, rng.choice(V, size=V // 16, replace=False)] = np.uint16(0xFF80)
+    for i in range(inp["B"]):
+        for j in range(cu[i + 1] - cu[i] - 1):
+            row = inp["target_logits"][cu[i] + j]
+            inp["draft_logits"][cu[i] - i + j] = row
+            if row[inp["draft_tokens"][cu[i] - i + j]] == np.uint16(0xFF80):
+                inp["draft_tokens"][cu[i] - i + j] = int(np.argmax(W.bf16_bits_to_f32(row)))
+    d, ref, _ = check(api, inp)
+    assert ref["status"] == 0
+    assert np.all(d.num_accepted.cpu().numpy() == np.diff(cu) - 1)
+    toks = d.out_tokens.cpu().numpy()
+    for i in range(inp["B"]):
+        x = int(toks[cu[i + 1] - 1])
+        assert W.bf16_bits_to_f32(inp["target_logits"][cu[i + 1] - 1, x]) > -np.inf
+
+
 def test_tiny_top_p_and_tie_heavy_logits(api):
     """Quantized logits (many exact ties) with several top_p values."""
     rng = np.random.default_rng(0)
