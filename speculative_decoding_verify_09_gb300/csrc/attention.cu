@@ -1226,8 +1226,9 @@ __global__ void __launch_bounds__(AttnCfg<D, RS, NB, KV8>::kThreads)
 
 // The same kernel under a 128-register cap (launch bounds of two 256-thread
 // CTAs per SM; it is launched with fewer threads): used for the 16-row
-// configuration, whose uncapped two CTAs per SM would take every register of
-// the SM and leave none for the sampler CTAs the fused step runs beside them.
+// configuration (bf16 and E4M3 K/V), whose uncapped two CTAs per SM would take
+// every register of the SM and leave none for the sampler CTAs the fused step
+// runs beside them.
 template <int D, int RS, int NB, bool KV8>
 __global__ void __launch_bounds__(256, 2) attn_bf16_kernel_cap128(const AttnParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -1466,7 +1467,7 @@ cudaError_t launch_bf16(AttnParams P, const AttnLaunchOpts &o, int max_grid, int
   const int bytes = std::max(P.sm.total, opt.smem_min);
   static_assert(C::kThreads <= 256 || !(RS == 1 && NB == 2), "the capped kernel's bounds");
   auto kern = [] {
-    if constexpr (D == 128 && RS == 1 && NB == 2 && !KV8)
+    if constexpr (D == 128 && RS == 1 && NB == 2)
       return attn_bf16_kernel_cap128<D, RS, NB, KV8>;
     else
       return attn_bf16_kernel<D, RS, NB, KV8>;
