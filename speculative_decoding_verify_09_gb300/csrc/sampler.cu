@@ -254,14 +254,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-// The two halves of cluster_sync_all, for a CTA with work left between its
-// last read of another CTA's shared memory and its exit.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
 
 // Generic address of `p` in the shared memory of cluster CTA `rank`.
 template <typename X>
@@ -1868,23 +1860,27 @@ __global__ void __launch_bounds__(kDrawNT, 4) draw_kernel(const SampParams P) {
 // --------------------------------------------------------------------------
 // Cluster path (no nucleus): one thread-block cluster of kClusterN CTAs per
 // sequence; CTA k owns vocabulary slice k of every row of the sequence.  The
-// phases meet at three cluster barriers and exchange data through distributed
-// shared memory: no global atomics, no fences, no second launch.
+// phases meet at two cluster barriers (one more per extra round of the draw)
+// and exchange data through distributed shared memory: no global atomics, no
+// fences, no second launch.
 //   A  CTA k loads slice k of every row into registers (rows in groups of
-//      8, all loads of a group in flight together); per row the warp max,
-//      then each thread's 2^((l - max) log2(e)/T) summed across the warp,
-//      merged across the CTA as (max, sum) pairs.
-//   B  every CTA merges each row's 16 slice statistics, evaluates the draft
-//      tokens' probabilities and runs the accept tests, so all CTAs hold n
-//      without another barrier; CTA 0 writes the outputs.
+//      kRowGroup, all loads of a group in flight together); per row the warp
+//      max, then each thread's 2^((l - max) log2(e)/T) summed across the warp,
+//      merged across the CTA as (max, sum) pairs.  Barrier (1).
+//   B  every CTA merges each row's kClusterN slice statistics (remote reads),
+//      evaluates the draft tokens' probabilities and runs the accept tests,
+//      so all CTAs hold n without another barrier; CTA 0 writes the outputs.
 //   C  append slice k of the accepted block rows; exact fixed-point sums of
 //      row n (the residual, and q_hat for the empty-residual fallback) per
-//      thread run, re-read from L2, scanned inside the CTA.
+//      thread run, re-read from L2, scanned inside the CTA; each CTA pushes
+//      its slice totals into every CTA's table.  Barrier (2).
 // Shared memory holds only the statistics (a few KB), so a cluster's CTAs fit
 // beside the attention's CTAs on any SM in the fused step.
-//   D  every CTA reads the 16 slice totals and locates the target in
-//      vocabulary order; inside the owner CTA the thread whose run holds it
-//      walks that run.
+//   D  every CTA reads the kClusterN slice totals from its own table and
+//      locates the target in vocabulary order; inside the owner CTA the
+//      thread whose run holds it walks that run.  No CTA touches another's
+//      shared memory after barrier (2), so none waits for the others to
+//      leave.
 // Weights use the SFU's approximate exp2 (relative error ~2^-22) and fp32
 // (max, sum) merges: relative error of a probability stays below ~2e-6, far
 // inside the 1e-5 near-tie windows of the decisions.
@@ -1904,15 +1900,18 @@ struct ClusterSmem {
   float pdraft[kMaxRows];                            // probability of the row's draft token
   uint32_t dbits[kMaxRows];                          // logit bits at the draft token
   int dtok[kMaxRows];
-  float redm[kMaxRows][kClNW], reds[kMaxRows][kClNW];
-  uint32_t redb[kMaxRows][kClNW];
-  unsigned long long tot[2];                         // slice totals of the sums A and B
+  union {                                            // never live together:
+    struct {                                         // phase A: per-warp row statistics
+      float redm[kMaxRows][kClNW], reds[kMaxRows][kClNW];
+      uint32_t redb[kMaxRows][kClNW];
+    } a;
+    ulonglong2 tab[kClusterN][2];                    // phase D: every CTA's slice totals A, B
+  } scr;                                             // and its two float-float sums, pushed by it
   unsigned long long scan64[kClNW];
   unsigned long long dec_pa, dec_pb;                 // prefix of the owner slice
   FF dec_L;                                          // exact ln(S_p / S_q) (recut pass)
   i128 dec_tg;                                       // the target, in units of A + beta B
   long long dec_beta;                                // beta * 2^56
-  FF ssum[2];                                        // slice float-float sums (C1)
   FF redff[2][kClNW];
   FF Lr;                                             // ln(S_p / S_q) of rows n
   int walker;                                        // thread whose run holds the target
@@ -1968,6 +1967,14 @@ __device__ __forceinline__ bool vec_has_neg_inf(const uint4 x) {
       any = any || w[k] == 0xFF800000u;
   }
   return any;
+}
+
+// A float-float as one 64-bit word (hi in the low half) and back.
+__device__ __forceinline__ unsigned long long ff_bits(FF v) {
+  return (static_cast<unsigned long long>(__float_as_uint(v.lo)) << 32) | __float_as_uint(v.hi);
+}
+__device__ __forceinline__ FF ff_of_bits(unsigned long long b) {
+  return FF{__uint_as_float(static_cast<uint32_t>(b)), __uint_as_float(static_cast<uint32_t>(b >> 32))};
 }
 
 // (m, s) <- merge of two (max, sum of weights relative to max) pairs.
@@ -2093,20 +2100,20 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
 #pragma unroll
       for (int u = 0; u < kRowGroup; ++u)
         if (g0 + u < nrows) {
-          sm.redm[g0 + u][w] = mx[u];
-          sm.reds[g0 + u][w] = sx[u];
-          sm.redb[g0 + u][w] = bad[u];
+          sm.scr.a.redm[g0 + u][w] = mx[u];
+          sm.scr.a.reds[g0 + u][w] = sx[u];
+          sm.scr.a.redb[g0 + u][w] = bad[u];
         }
     }
   }
   __syncthreads();
   if (tid < nrows) {
-    float m = sm.redm[tid][0], s = sm.reds[tid][0];
-    uint32_t bd = sm.redb[tid][0];
+    float m = sm.scr.a.redm[tid][0], s = sm.scr.a.reds[tid][0];
+    uint32_t bd = sm.scr.a.redb[tid][0];
 #pragma unroll
     for (int x = 1; x < kClNW; ++x) {
-      ms_merge(m, s, sm.redm[tid][x], sm.reds[tid][x], ex2c);
-      bd |= sm.redb[tid][x];
+      ms_merge(m, s, sm.scr.a.redm[tid][x], sm.scr.a.reds[tid][x], ex2c);
+      bd |= sm.scr.a.redb[tid][x];
     }
     sm.pm[tid] = m;
     sm.ps[tid] = s;
@@ -2313,7 +2320,6 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
   };
   FF rf_L_exact = FF{0.0f, 0.0f};
   int use = mode;
-  bool arrived = false;                            // at the exit barrier (3)
   for (int round = 0; round < 3; ++round) {
     unsigned long long sa = 0, sb = 0;
     float gs = 0.0f, gc = 0.0f;                    // Kahan sum of G's terms
@@ -2375,8 +2381,6 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
       __syncthreads();
     }
     if (tid == 0) {
-      sm.tot[0] = ta;
-      sm.tot[1] = use == 0 ? tb : 0ull;
       FF x = ff_make(0.0f), dd = FF{INFINITY, INFINITY};
       if (use == 0) {
         x = sm.redff[0][0];
@@ -2387,16 +2391,25 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
           dd = FF{fminf(dd.hi, sm.redff[1][q].hi), fminf(dd.lo, sm.redff[1][q].lo)};
         }
       }
-      sm.ssum[0] = x;
-      sm.ssum[1] = dd;
+      // slot k of every CTA's table: this slice's totals and sums, so that
+      // after the barrier each CTA's owner search reads only its own memory
+      const ulonglong2 t0 = make_ulonglong2(ta, use == 0 ? tb : 0ull);
+      const ulonglong2 t1 = make_ulonglong2(ff_bits(x), ff_bits(dd));
+#pragma unroll 1
+      for (int q = 0; q < C; ++q) {
+        ulonglong2 *dst = dsmem(&sm.scr.tab[k][0], static_cast<uint32_t>(q));
+        dst[0] = t0;
+        dst[1] = t1;
+      }
     }
     cluster_sync_all();                            // (2) slice totals and G visible
     // ---- D: every CTA finds the slice holding the target (warp 0)
     if (w == 0) {
-      const unsigned long long a0 = l < C ? *dsmem(&sm.tot[0], l) : 0ull;
-      const unsigned long long b0 = l < C ? *dsmem(&sm.tot[1], l) : 0ull;
-      FF gl = l < C ? *dsmem(&sm.ssum[0], l) : ff_make(0.0f);
-      const FF dl = l < C ? *dsmem(&sm.ssum[1], l) : FF{INFINITY, INFINITY};
+      const ulonglong2 t0 = l < C ? sm.scr.tab[l][0] : make_ulonglong2(0ull, 0ull);
+      const ulonglong2 t1 = l < C ? sm.scr.tab[l][1] : make_ulonglong2(0ull, 0ull);
+      const unsigned long long a0 = t0.x, b0 = t0.y;
+      FF gl = l < C ? ff_of_bits(t1.x) : ff_make(0.0f);
+      const FF dl = l < C ? ff_of_bits(t1.y) : FF{INFINITY, INFINITY};
       FF G = shfl_ff(gl, 0);
 #pragma unroll 1
       for (int q = 1; q < C; ++q) G = ff_add(G, shfl_ff(gl, q));   // the same order everywhere
@@ -2446,24 +2459,22 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     if (sm.dec_use == -2) {                        // exact pass at L (the same in every CTA)
       rf.L = sm.dec_L;
       use = 2;
-      cluster_sync_all();                          // every CTA has read the totals
+      cluster_sync_all();                          // every CTA has read its table (pushed again next round)
       continue;
     }
     if (sm.dec_use < 0) {                          // Z <= 0 (the same in every CTA)
       if (use != 1) {                              // rejected, empty residual: draw from q_hat
         if (k == 0 && tid == 0) set_status(a.dev_status, SV_DEV_EMPTY_RESIDUAL);
         use = 1;
-        cluster_sync_all();                        // every CTA has read the totals
+        cluster_sync_all();                        // every CTA has read its table (pushed again next round)
         continue;
       }
       if (k == 0 && tid == 0) a.out_tokens[r0 + n] = -1;   // empty q_hat: not for a valid row
       break;
     }
-    // The last round: this CTA has read all it needs from the others, so it
-    // arrives at the exit barrier now and the owner walks while the others
-    // leave (the walk touches only this CTA's own shared memory).
-    cluster_arrive();
-    arrived = true;
+    // The last round: every access to another CTA's shared memory (phase B's
+    // reads, the pushed totals) ended before barrier (2), so the CTAs leave
+    // without another cluster barrier and the owner walks alone.
     if (sm.dec_owner) {                            // uniform within the CTA
       const long long beta = sm.dec_beta;
       const i128 tg = sm.dec_tg;
@@ -2500,8 +2511,6 @@ __global__ void __launch_bounds__(kClNT, 4) sampler_cluster_kernel(const SampPar
     }
     break;
   }
-  if (!arrived) cluster_arrive();
-  cluster_wait();                                  // (3) no CTA leaves while its totals are read
 }
 
 }  // namespace
